@@ -1,0 +1,267 @@
+"""CPU oracle of the DSpark fused context-KV write (test infrastructure).
+
+TEST INFRASTRUCTURE ONLY: the test suite, the smoke check and the benchmark's
+CPU-baseline leg are the only users.  The product path never imports this
+package, and this package imports nothing from the product path.
+
+The arithmetic lives in ``ctx_kv_oracle.c`` (plain C, fp64, one row at a
+time); this module only marshals numpy arrays into it with ctypes.  See that
+file's header for the definition it follows (vLLM DSpark context-KV writer
+page, module docstring; DSpark draft model page,
+``precompute_and_store_context_kv``).
+
+Parity status: pinned.  ``tests/test_oracle_pins.py`` ties every step to
+closed forms, invariants, brute force over the fp8 code space and special
+cases that reduce to library routines.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "ctx_kv_oracle.c")
+_LIB_PATH = os.path.join(_HERE, "libctx_kv_oracle.so")
+
+KV_BF16 = 0
+KV_FP8_E4M3 = 1
+HEAD_DIM = 128
+ROW = 256
+
+ERRORS = {
+    0: "ok", -1: "bad argument", -2: "slot beyond the cache", -3: "duplicate valid slot",
+    -4: "position beyond the cos|sin table", -5: "fp8 scale not positive and finite",
+    -6: "alternate buffer too small", -7: "out of memory",
+}
+
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle with gcc (ISO C11, no FMA contraction, so x86-64 and
+    aarch64 hosts evaluate every expression identically)."""
+    with _lock:
+        if force or not os.path.exists(_LIB_PATH) or os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC):
+            tmp = _LIB_PATH + f".tmp{os.getpid()}"
+            cmd = ["gcc", "-std=c11", "-O2", "-ffp-contract=off", "-fno-fast-math",
+                   "-Wall", "-shared", "-fPIC", "-o", tmp, _SRC, "-lm"]
+            subprocess.run(cmd, check=True)
+            os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+class OracleInputs(ctypes.Structure):
+    _fields_ = [
+        ("all_kv", ctypes.c_void_p), ("knorm_w", ctypes.c_void_p),
+        ("positions", ctypes.c_void_p), ("slot_mapping", ctypes.c_void_p),
+        ("cos_sin", ctypes.c_void_p), ("k_scale", ctypes.c_void_p), ("v_scale", ctypes.c_void_p),
+        ("num_ctx", ctypes.c_int64), ("max_pos", ctypes.c_int64), ("num_blocks", ctypes.c_int64),
+        ("num_layers", ctypes.c_int32), ("num_kv_heads", ctypes.c_int32),
+        ("block_size", ctypes.c_int32), ("rotary_dim", ctypes.c_int32),
+        ("kv_dtype", ctypes.c_int32), ("eps", ctypes.c_float),
+    ]
+
+
+def lib():
+    global _lib
+    if _lib is None:
+        build()
+        L = ctypes.CDLL(_LIB_PATH)
+        P = ctypes.c_void_p
+        L.dspark_oracle_bf16_decode.argtypes = [ctypes.c_uint16]
+        L.dspark_oracle_bf16_decode.restype = ctypes.c_double
+        L.dspark_oracle_bf16_rne.argtypes = [ctypes.c_double]
+        L.dspark_oracle_bf16_rne.restype = ctypes.c_uint16
+        L.dspark_oracle_e4m3_decode.argtypes = [ctypes.c_uint8]
+        L.dspark_oracle_e4m3_decode.restype = ctypes.c_double
+        L.dspark_oracle_e4m3_rne_sat.argtypes = [ctypes.c_float]
+        L.dspark_oracle_e4m3_rne_sat.restype = ctypes.c_uint8
+        L.dspark_oracle_gemma_knorm.argtypes = [P, P, ctypes.c_float, P, P]
+        L.dspark_oracle_gemma_knorm.restype = ctypes.c_int
+        L.dspark_oracle_rope_pair.argtypes = [ctypes.c_uint16] * 4 + [P, P]
+        L.dspark_oracle_rope_pair.restype = None
+        L.dspark_oracle_row.argtypes = [P, ctypes.c_int64, ctypes.c_int32, ctypes.c_int32, P, P, P, P]
+        L.dspark_oracle_row.restype = ctypes.c_int
+        L.dspark_oracle_dest_row.argtypes = [ctypes.c_int64, ctypes.c_int32, ctypes.c_int32,
+                                             ctypes.c_int32, ctypes.c_int64]
+        L.dspark_oracle_dest_row.restype = ctypes.c_int64
+        L.dspark_oracle_check_inputs.argtypes = [P]
+        L.dspark_oracle_check_inputs.restype = ctypes.c_int
+        L.dspark_oracle_write.argtypes = [P, P, ctypes.c_int64, ctypes.c_int64, P, P, P,
+                                          ctypes.c_int64, P]
+        L.dspark_oracle_write.restype = ctypes.c_int
+        L.dspark_oracle_rows.argtypes = [P, P, ctypes.c_int64, P, P, P, P, ctypes.c_int64, P]
+        L.dspark_oracle_rows.restype = ctypes.c_int
+        _lib = L
+    return _lib
+
+
+class OracleError(RuntimeError):
+    pass
+
+
+def _check(rc: int):
+    if rc != 0:
+        raise OracleError(f"oracle: {ERRORS.get(rc, rc)}")
+
+
+def _ptr(a: np.ndarray) -> int:
+    assert a.flags["C_CONTIGUOUS"]
+    return a.ctypes.data
+
+
+# ---------------------------------------------------------------- scalars
+
+def bf16_decode(bits: int) -> float:
+    return lib().dspark_oracle_bf16_decode(int(bits))
+
+
+def bf16_rne(x: float) -> int:
+    return int(lib().dspark_oracle_bf16_rne(float(x)))
+
+
+def e4m3_decode(code: int) -> float:
+    return lib().dspark_oracle_e4m3_decode(int(code))
+
+
+def e4m3_rne_sat(x: float) -> int:
+    """Code of the fp32 value nearest to ``x`` (``x`` is first rounded to fp32)."""
+    return int(lib().dspark_oracle_e4m3_rne_sat(float(np.float32(x))))
+
+
+# ---------------------------------------------------------------- steps
+
+def gemma_knorm(k_bits: np.ndarray, w_bits: np.ndarray, eps: float):
+    """Step 2 on one 128-element K row (bf16 bits) -> (y, y_alt, n_ambiguous)."""
+    k = np.ascontiguousarray(k_bits, dtype=np.uint16)
+    w = np.ascontiguousarray(w_bits, dtype=np.uint16)
+    assert k.shape == (HEAD_DIM,) and w.shape == (HEAD_DIM,)
+    y = np.empty(HEAD_DIM, np.uint16)
+    ya = np.empty(HEAD_DIM, np.uint16)
+    n = lib().dspark_oracle_gemma_knorm(_ptr(k), _ptr(w), ctypes.c_float(eps), _ptr(y), _ptr(ya))
+    return y, ya, n
+
+
+def rope_pair(x1: int, x2: int, c: int, s: int):
+    o1 = ctypes.c_uint16()
+    o2 = ctypes.c_uint16()
+    lib().dspark_oracle_rope_pair(int(x1), int(x2), int(c), int(s), ctypes.byref(o1), ctypes.byref(o2))
+    return o1.value, o2.value
+
+
+def dest_row(slot: int, h: int, num_kv_heads: int, block_size: int, num_blocks: int) -> int:
+    return int(lib().dspark_oracle_dest_row(int(slot), int(h), int(num_kv_heads), int(block_size),
+                                            int(num_blocks)))
+
+
+# ---------------------------------------------------------------- whole call
+
+class Problem:
+    """Host copies of one write call's inputs, kept alive for the C side.
+
+    Arrays: all_kv / knorm_w / cos_sin as uint16 bf16 bits, positions and
+    slot_mapping int64, k_scale / v_scale float32 ``[L]``."""
+
+    def __init__(self, all_kv, knorm_w, positions, slot_mapping, cos_sin, k_scale, v_scale,
+                 *, num_blocks: int, block_size: int, rotary_dim: int, kv_dtype: int, eps: float):
+        self.all_kv = np.ascontiguousarray(all_kv, dtype=np.uint16)
+        T, L, two, H, D = self.all_kv.shape
+        assert two == 2 and D == HEAD_DIM
+        self.knorm_w = np.ascontiguousarray(knorm_w, dtype=np.uint16).reshape(L, HEAD_DIM)
+        self.positions = np.ascontiguousarray(positions, dtype=np.int64).reshape(T)
+        self.slot_mapping = np.ascontiguousarray(slot_mapping, dtype=np.int64).reshape(T)
+        self.cos_sin = np.ascontiguousarray(cos_sin, dtype=np.uint16)
+        assert self.cos_sin.ndim == 2 and self.cos_sin.shape[1] == rotary_dim
+        self.k_scale = np.ascontiguousarray(k_scale, dtype=np.float32).reshape(L)
+        self.v_scale = np.ascontiguousarray(v_scale, dtype=np.float32).reshape(L)
+        self.T, self.L, self.H = T, L, H
+        self.num_blocks, self.block_size = int(num_blocks), int(block_size)
+        self.rotary_dim, self.kv_dtype, self.eps = int(rotary_dim), int(kv_dtype), float(eps)
+        self.c = OracleInputs(
+            _ptr(self.all_kv), _ptr(self.knorm_w), _ptr(self.positions), _ptr(self.slot_mapping),
+            _ptr(self.cos_sin), _ptr(self.k_scale), _ptr(self.v_scale),
+            T, self.cos_sin.shape[0], self.num_blocks, L, H, self.block_size, self.rotary_dim,
+            self.kv_dtype, ctypes.c_float(self.eps).value,
+        )
+
+    @property
+    def elem_dtype(self):
+        return np.uint8 if self.kv_dtype == KV_FP8_E4M3 else np.uint16
+
+    def check(self):
+        _check(lib().dspark_oracle_check_inputs(ctypes.byref(self.c)))
+
+    def new_caches(self, fill_byte: int = 0xFF):
+        shape = (self.num_blocks, self.H, self.block_size, ROW)
+        out = []
+        for _ in range(self.L):
+            c = np.empty(shape, dtype=self.elem_dtype)
+            c.view(np.uint8).fill(fill_byte)
+            out.append(c)
+        return out
+
+    def write(self, caches, t_begin: int = 0, t_end: int | None = None, alt_cap: int | None = None):
+        """Run the write into host ``caches`` (one array per layer).  Returns
+        the admissible alternates as arrays (layer, element index, value)."""
+        t_end = self.T if t_end is None else t_end
+        for c in caches:
+            assert c.flags["C_CONTIGUOUS"] and c.dtype == self.elem_dtype
+        cap = alt_cap if alt_cap is not None else max(1024, (t_end - t_begin) * self.L * self.H // 4)
+        ptrs = (ctypes.c_void_p * self.L)(*[_ptr(c) for c in caches])
+        al = np.empty(cap, np.int32)
+        ae = np.empty(cap, np.int64)
+        av = np.empty(cap, np.uint16)
+        n = ctypes.c_int64()
+        rc = lib().dspark_oracle_write(ctypes.byref(self.c), ptrs, t_begin, t_end, _ptr(al), _ptr(ae),
+                                       _ptr(av), cap, ctypes.byref(n))
+        _check(rc)
+        k = n.value
+        return al[:k].copy(), ae[:k].copy(), av[:k].copy()
+
+    def rows(self, row_ids):
+        """Stored 256-element rows for flat row ids ``(t*L + l)*H + h``, with
+        alternates as (index into row_ids, dim, value)."""
+        ids = np.ascontiguousarray(row_ids, dtype=np.int64).reshape(-1)
+        n = ids.shape[0]
+        out = np.empty((n, ROW), dtype=self.elem_dtype)
+        cap = max(1024, n * 8)
+        ar = np.empty(cap, np.int64)
+        ad = np.empty(cap, np.int32)
+        av = np.empty(cap, np.uint16)
+        cnt = ctypes.c_int64()
+        rc = lib().dspark_oracle_rows(ctypes.byref(self.c), _ptr(ids), n, _ptr(out), _ptr(ar), _ptr(ad),
+                                      _ptr(av), cap, ctypes.byref(cnt))
+        _check(rc)
+        k = cnt.value
+        return out, (ar[:k].copy(), ad[:k].copy(), av[:k].copy())
+
+    def dest_rows(self, row_ids):
+        """Cache row (within its layer) that each flat row id is stored to,
+        -1 for padding."""
+        ids = np.asarray(row_ids, dtype=np.int64).reshape(-1)
+        t = ids // (self.L * self.H)
+        h = ids % self.H
+        return np.array([dest_row(int(self.slot_mapping[ti]), int(hi), self.H, self.block_size,
+                                  self.num_blocks) for ti, hi in zip(t, h)], dtype=np.int64)
+
+
+def problem_from_inputs(inp) -> Problem:
+    """A Problem from a ``workloads.Inputs`` (CPU torch tensors)."""
+    import torch  # local: the oracle's arithmetic does not use torch
+
+    def bits(x):
+        return x.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
+
+    wl = inp.workload
+    return Problem(
+        bits(inp.all_kv), bits(inp.knorm_w), inp.positions.cpu().numpy(), inp.slot_mapping.cpu().numpy(),
+        bits(inp.cos_sin), inp.k_scale.cpu().numpy(), inp.v_scale.cpu().numpy(),
+        num_blocks=wl.num_blocks, block_size=wl.block_size, rotary_dim=wl.rotary_dim,
+        kv_dtype=KV_FP8_E4M3 if wl.kv_dtype == "fp8_e4m3" else KV_BF16, eps=inp.eps,
+    )

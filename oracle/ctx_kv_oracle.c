@@ -1,0 +1,466 @@
+/*
+ * Plain CPU oracle of the DSpark fused context-KV write.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Only the test suite, the smoke check and the
+ * benchmark's CPU-baseline leg load this library.  It shares no code, header,
+ * table or helper with the CUDA path and is deliberately slow and literal:
+ * one row at a time, fp64 arithmetic, no blocking, no fusion.
+ *
+ * What it computes (vLLM DSpark context-KV writer page, module docstring, and
+ * the DSpark draft model page, MiniMaxM3DSparkModel.precompute_and_store_context_kv):
+ * for every context token t whose slot is >= 0, every layer l and every KV
+ * head h,
+ *   1. k = all_kv[t, l, 0, h, :], v = all_kv[t, l, 1, h, :]   (bf16, 128 each)
+ *   2. Gemma RMSNorm of k:  y = k * rsqrt(mean(k^2) + eps) * (1 + w[l]),
+ *      materialised to bf16 (the page states fp32 evaluation; this oracle
+ *      evaluates in fp64 and reports both bf16 neighbours as admissible when
+ *      the value lies within 2^-18 relative of a rounding midpoint, which
+ *      covers any fp32 evaluation order)
+ *   3. partial NeoX RoPE of the first r dims at position pos[t] from the
+ *      bf16 cos|sin row (cos in [0, r/2), sin in [r/2, r)):
+ *        y'[i]       = y[i] c_i - y[i + r/2] s_i
+ *        y'[i + r/2] = y[i + r/2] c_i + y[i] s_i        for i < r/2,
+ *      each output rounded once to bf16; dims >= r pass through
+ *   4. store: raw bf16 K'|V, or fp8 e4m3 (OCP, round to nearest even,
+ *      saturating at +-448) of x / scale with the division in fp32
+ *   5. the 256-element row K'|V goes to layer l's paged cache
+ *      [num_blocks, nkv, block_size, 256] at block slot / block_size,
+ *      head h, offset slot % block_size.
+ * Slots < 0 are padding: nothing is read or written for them.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#define ORACLE_HEAD_DIM 128
+#define ORACLE_ROW 256
+#define ORACLE_TIE_REL 3.814697265625e-06 /* 2^-18 */
+
+enum { ORACLE_KV_BF16 = 0, ORACLE_KV_FP8_E4M3 = 1 };
+
+enum {
+    ORACLE_OK = 0,
+    ORACLE_ERR_ARG = -1,
+    ORACLE_ERR_SLOT_RANGE = -2,
+    ORACLE_ERR_SLOT_DUP = -3,
+    ORACLE_ERR_POS_RANGE = -4,
+    ORACLE_ERR_SCALE = -5,
+    ORACLE_ERR_ALT_CAP = -6,
+    ORACLE_ERR_NOMEM = -7,
+};
+
+/* Everything one write call reads (host memory). */
+typedef struct {
+    const uint16_t *all_kv;       /* bf16 bits [T][L][2][H][128] */
+    const uint16_t *knorm_w;      /* bf16 bits [L][128] */
+    const int64_t *positions;     /* [T] */
+    const int64_t *slot_mapping;  /* [T], < 0 = padding */
+    const uint16_t *cos_sin;      /* bf16 bits [max_pos][r] */
+    const float *k_scale;         /* [L], read in fp8 mode only */
+    const float *v_scale;         /* [L], read in fp8 mode only */
+    int64_t num_ctx;
+    int64_t max_pos;
+    int64_t num_blocks;
+    int32_t num_layers;
+    int32_t num_kv_heads;
+    int32_t block_size;
+    int32_t rotary_dim;
+    int32_t kv_dtype;
+    float eps;
+} dspark_oracle_inputs;
+
+/* ------------------------------------------------------------------ */
+/* bf16: 1 sign, 8 exponent, 7 stored mantissa bits (the top half of an
+ * IEEE binary32).                                                        */
+
+double dspark_oracle_bf16_decode(uint16_t b)
+{
+    uint32_t u = (uint32_t)b << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return (double)f;
+}
+
+/* Round a real number (given as a double) to the nearest bf16, ties to
+ * even.  8 significant bits; below 2^-126 the spacing stays 2^-133
+ * (subnormals); results above the largest finite bf16 become infinity. */
+uint16_t dspark_oracle_bf16_rne(double x)
+{
+    if (isnan(x))
+        return 0x7FC0;
+    uint16_t sign = signbit(x) ? 0x8000 : 0;
+    double a = fabs(x);
+    if (a == 0.0)
+        return sign;
+    if (isinf(a))
+        return sign | 0x7F80;
+    int e2;
+    frexp(a, &e2);               /* a in [2^(e2-1), 2^e2) */
+    int ulp_exp = (e2 - 1) - 7;  /* 7 fraction bits */
+    if (ulp_exp < -133)
+        ulp_exp = -133;
+    double q = ldexp(a, -ulp_exp);      /* exact: a power-of-two scaling */
+    double whole = floor(q);
+    double rem = q - whole;             /* exact */
+    if (rem > 0.5 || (rem == 0.5 && fmod(whole, 2.0) != 0.0))
+        whole += 1.0;
+    double r = ldexp(whole, ulp_exp);
+    if (r > 3.3895313892515355e38)      /* (2 - 2^-7) * 2^127 */
+        return sign | 0x7F80;
+    float f = (float)r;                 /* exact: r has <= 8 significant bits */
+    uint32_t u;
+    memcpy(&u, &f, sizeof u);
+    return sign | (uint16_t)(u >> 16);
+}
+
+/* ------------------------------------------------------------------ */
+/* OCP FP8 E4M3: 1 sign, 4 exponent (bias 7), 3 mantissa bits; no infinities;
+ * S.1111.111 is NaN, so the largest finite magnitude is 1.75 * 2^8 = 448;
+ * exponent field 0 holds subnormals m/8 * 2^-6.                           */
+
+double dspark_oracle_e4m3_decode(uint8_t c)
+{
+    int s = c >> 7, e = (c >> 3) & 0xF, m = c & 7;
+    double v;
+    if (e == 0xF && m == 7)
+        return NAN;
+    if (e == 0)
+        v = ldexp((double)m / 8.0, -6);
+    else
+        v = ldexp(1.0 + (double)m / 8.0, e - 7);
+    return s ? -v : v;
+}
+
+/* fp32 value -> e4m3 code, round to nearest even, saturating to +-448 (also
+ * for infinities); NaN -> 0x7F. */
+uint8_t dspark_oracle_e4m3_rne_sat(float xf)
+{
+    double x = (double)xf;
+    if (isnan(x))
+        return 0x7F;
+    uint8_t sign = signbit(x) ? 0x80 : 0;
+    double a = fabs(x);
+    if (a >= 448.0)
+        return sign | 0x7E;
+    if (a == 0.0)
+        return sign;
+    int e2;
+    frexp(a, &e2);
+    int e = e2 - 1;                        /* a in [2^e, 2^(e+1)) */
+    int ulp_exp = (e < -6 ? -6 : e) - 3;   /* 3 fraction bits; subnormal spacing 2^-9 */
+    double q = ldexp(a, -ulp_exp);
+    double whole = floor(q);
+    double rem = q - whole;
+    if (rem > 0.5 || (rem == 0.5 && fmod(whole, 2.0) != 0.0))
+        whole += 1.0;
+    double v = ldexp(whole, ulp_exp);      /* <= 448 since a < 448 */
+    if (v == 0.0)
+        return sign;
+    frexp(v, &e2);
+    e = e2 - 1;
+    if (e < -6)
+        return sign | (uint8_t)ldexp(v, 9);            /* subnormal: m = v / 2^-9 */
+    int m = (int)(ldexp(v, -e) * 8.0) - 8;             /* v = (1 + m/8) 2^e */
+    return sign | (uint8_t)(((e + 7) << 3) | m);
+}
+
+/* ------------------------------------------------------------------ */
+/* Step 2: Gemma RMSNorm of one K row.  y[d] is the bf16 rounding (ties to
+ * even) of the exact value; y_alt[d] is the other bf16 neighbour when the
+ * exact value lies within ORACLE_TIE_REL (relative) of a rounding midpoint,
+ * else y[d] again.  Returns the number of such ambiguous dims. */
+int dspark_oracle_gemma_knorm(const uint16_t *k, const uint16_t *w, float eps,
+                              uint16_t *y, uint16_t *y_alt)
+{
+    double ss = 0.0;
+    for (int d = 0; d < ORACLE_HEAD_DIM; d++) {
+        double kd = dspark_oracle_bf16_decode(k[d]);
+        ss += kd * kd;
+    }
+    double inv = 1.0 / sqrt(ss / (double)ORACLE_HEAD_DIM + (double)eps);
+    int amb = 0;
+    for (int d = 0; d < ORACLE_HEAD_DIM; d++) {
+        double v = dspark_oracle_bf16_decode(k[d]) * inv *
+                   (1.0 + dspark_oracle_bf16_decode(w[d]));
+        uint16_t dn = dspark_oracle_bf16_rne(v * (1.0 - ORACLE_TIE_REL));
+        uint16_t up = dspark_oracle_bf16_rne(v * (1.0 + ORACLE_TIE_REL));
+        y[d] = dspark_oracle_bf16_rne(v);
+        y_alt[d] = y[d];
+        if (dn != up) {
+            y_alt[d] = y[d] == dn ? up : dn;
+            amb++;
+        }
+    }
+    return amb;
+}
+
+/* Step 3 for one rotated pair (i, i + r/2): exact products in fp64, one
+ * rounding to bf16 per output. */
+void dspark_oracle_rope_pair(uint16_t x1, uint16_t x2, uint16_t c, uint16_t s,
+                             uint16_t *o1, uint16_t *o2)
+{
+    double a = dspark_oracle_bf16_decode(x1), b = dspark_oracle_bf16_decode(x2);
+    double cc = dspark_oracle_bf16_decode(c), ss = dspark_oracle_bf16_decode(s);
+    *o1 = dspark_oracle_bf16_rne(a * cc - b * ss);
+    *o2 = dspark_oracle_bf16_rne(b * cc + a * ss);
+}
+
+/* Step 4 for one bf16 value: the stored element (bf16 bits or e4m3 code). */
+static uint16_t encode_elem(uint16_t x, int kv_dtype, float scale)
+{
+    if (kv_dtype == ORACLE_KV_BF16)
+        return x;
+    float xf = (float)dspark_oracle_bf16_decode(x);
+    float q = xf / scale; /* fp32 division, correctly rounded */
+    return dspark_oracle_e4m3_rne_sat(q);
+}
+
+/* ------------------------------------------------------------------ */
+/* One output row.  out: 256 stored elements (uint16 bf16 bits, or uint8
+ * e4m3 codes when kv_dtype is fp8).  Every other admissible value of a K
+ * element (from a bf16 tie in the norm) is appended to alt_dim/alt_val
+ * (room for 3 * 128 entries); *n_alt receives their count. */
+int dspark_oracle_row(const dspark_oracle_inputs *in, int64_t t, int32_t l, int32_t h,
+                      void *out, int32_t *alt_dim, uint16_t *alt_val, int32_t *n_alt)
+{
+    const int L = in->num_layers, H = in->num_kv_heads, r = in->rotary_dim;
+    if (t < 0 || t >= in->num_ctx || l < 0 || l >= L || h < 0 || h >= H)
+        return ORACLE_ERR_ARG;
+    const int64_t base = (((t * L + l) * 2 + 0) * H + h) * ORACLE_HEAD_DIM;
+    const int64_t vbase = (((t * L + l) * 2 + 1) * H + h) * ORACLE_HEAD_DIM;
+    const uint16_t *k = in->all_kv + base;
+    const uint16_t *v = in->all_kv + vbase;
+    const uint16_t *w = in->knorm_w + (int64_t)l * ORACLE_HEAD_DIM;
+    const int64_t pos = in->positions[t];
+    if (pos < 0 || pos >= in->max_pos)
+        return ORACLE_ERR_POS_RANGE;
+    const uint16_t *cs = in->cos_sin + pos * r;
+    const float ks = in->kv_dtype == ORACLE_KV_FP8_E4M3 ? in->k_scale[l] : 1.0f;
+    const float vs = in->kv_dtype == ORACLE_KV_FP8_E4M3 ? in->v_scale[l] : 1.0f;
+
+    uint16_t y[ORACLE_HEAD_DIM], y_alt[ORACLE_HEAD_DIM];
+    dspark_oracle_gemma_knorm(k, w, in->eps, y, y_alt);
+
+    uint16_t res[ORACLE_ROW];
+    int na = 0;
+    for (int d = 0; d < ORACLE_HEAD_DIM; d++) {
+        /* candidate K' values of dim d; the first is the primary one, built
+         * from the correctly rounded norm outputs */
+        uint16_t cand[4];
+        int nc = 0;
+        if (d < r) {
+            const int half = r / 2;
+            const int lower = d < half;
+            const int i = lower ? d : d - half;        /* frequency index */
+            const int p = lower ? d + half : d - half; /* partner dim */
+            const uint16_t c = cs[i], s = cs[half + i];
+            const uint16_t self_c[2] = {y[d], y_alt[d]};
+            const uint16_t part_c[2] = {y[p], y_alt[p]};
+            const int ns = y_alt[d] != y[d] ? 2 : 1;
+            const int np = y_alt[p] != y[p] ? 2 : 1;
+            for (int a = 0; a < ns; a++)
+                for (int b = 0; b < np; b++) {
+                    uint16_t o1, o2;
+                    if (lower) {
+                        dspark_oracle_rope_pair(self_c[a], part_c[b], c, s, &o1, &o2);
+                        cand[nc++] = o1;
+                    } else {
+                        dspark_oracle_rope_pair(part_c[b], self_c[a], c, s, &o1, &o2);
+                        cand[nc++] = o2;
+                    }
+                }
+        } else {
+            cand[nc++] = y[d];
+            if (y_alt[d] != y[d])
+                cand[nc++] = y_alt[d];
+        }
+        uint16_t enc[4];
+        for (int j = 0; j < nc; j++)
+            enc[j] = encode_elem(cand[j], in->kv_dtype, ks);
+        res[d] = enc[0];
+        for (int j = 1; j < nc; j++) {
+            int seen = enc[j] == enc[0];
+            for (int q = 1; q < j; q++)
+                seen |= enc[q] == enc[j];
+            if (!seen) {
+                if (alt_dim)
+                    alt_dim[na] = d;
+                if (alt_val)
+                    alt_val[na] = enc[j];
+                na++;
+            }
+        }
+    }
+    for (int d = 0; d < ORACLE_HEAD_DIM; d++)
+        res[ORACLE_HEAD_DIM + d] = encode_elem(v[d], in->kv_dtype, vs);
+
+    if (in->kv_dtype == ORACLE_KV_FP8_E4M3) {
+        uint8_t *o8 = (uint8_t *)out;
+        for (int d = 0; d < ORACLE_ROW; d++)
+            o8[d] = (uint8_t)res[d];
+    } else {
+        memcpy(out, res, sizeof res);
+    }
+    if (n_alt)
+        *n_alt = na;
+    return ORACLE_OK;
+}
+
+/* Step 5: the row of layer l's cache [num_blocks, H, block_size, 256] that
+ * (slot, h) addresses, counted in 256-element rows; -1 for padding, -2 when
+ * the slot lies beyond the cache. */
+int64_t dspark_oracle_dest_row(int64_t slot, int32_t h, int32_t num_kv_heads,
+                               int32_t block_size, int64_t num_blocks)
+{
+    if (slot < 0)
+        return -1;
+    int64_t block = slot / block_size;
+    int64_t offset = slot % block_size;
+    if (block >= num_blocks)
+        return -2;
+    return (block * num_kv_heads + h) * block_size + offset;
+}
+
+static int cmp_i64(const void *a, const void *b)
+{
+    int64_t x = *(const int64_t *)a, y = *(const int64_t *)b;
+    return (x > y) - (x < y);
+}
+
+/* Preconditions of a write: valid slots unique and inside the cache,
+ * positions of valid tokens inside the cos|sin table, fp8 scales positive
+ * and finite. */
+int dspark_oracle_check_inputs(const dspark_oracle_inputs *in)
+{
+    if (!in || in->num_ctx < 0 || in->num_layers <= 0 || in->num_kv_heads <= 0 ||
+        in->block_size <= 0 || in->num_blocks <= 0 || in->max_pos <= 0)
+        return ORACLE_ERR_ARG;
+    if (in->rotary_dim <= 0 || in->rotary_dim > ORACLE_HEAD_DIM || in->rotary_dim % 2)
+        return ORACLE_ERR_ARG;
+    if (in->kv_dtype != ORACLE_KV_BF16 && in->kv_dtype != ORACLE_KV_FP8_E4M3)
+        return ORACLE_ERR_ARG;
+    const int64_t cap = in->num_blocks * in->block_size;
+    int64_t nv = 0;
+    for (int64_t t = 0; t < in->num_ctx; t++) {
+        int64_t s = in->slot_mapping[t];
+        if (s < 0)
+            continue;
+        if (s >= cap)
+            return ORACLE_ERR_SLOT_RANGE;
+        if (in->positions[t] < 0 || in->positions[t] >= in->max_pos)
+            return ORACLE_ERR_POS_RANGE;
+        nv++;
+    }
+    if (in->kv_dtype == ORACLE_KV_FP8_E4M3)
+        for (int l = 0; l < in->num_layers; l++)
+            if (!(in->k_scale[l] > 0.0f) || !(in->v_scale[l] > 0.0f) ||
+                isinf(in->k_scale[l]) || isinf(in->v_scale[l]))
+                return ORACLE_ERR_SCALE;
+    int64_t *sorted = (int64_t *)malloc((size_t)(nv ? nv : 1) * sizeof(int64_t));
+    if (!sorted)
+        return ORACLE_ERR_NOMEM;
+    nv = 0;
+    for (int64_t t = 0; t < in->num_ctx; t++)
+        if (in->slot_mapping[t] >= 0)
+            sorted[nv++] = in->slot_mapping[t];
+    qsort(sorted, (size_t)nv, sizeof(int64_t), cmp_i64);
+    int rc = ORACLE_OK;
+    for (int64_t i = 1; i < nv; i++)
+        if (sorted[i] == sorted[i - 1]) {
+            rc = ORACLE_ERR_SLOT_DUP;
+            break;
+        }
+    free(sorted);
+    return rc;
+}
+
+/* The whole write for tokens [t_begin, t_end): every valid row computed by
+ * dspark_oracle_row and stored into caches[l] (host buffers, one per layer,
+ * each [num_blocks, H, block_size, 256] of the cache dtype).  Admissible
+ * alternates are reported as (layer, element index in that layer's cache,
+ * value), up to alt_cap of them; *n_alt receives how many there were in
+ * total.  Returns ORACLE_ERR_ALT_CAP (after writing everything) when more
+ * alternates existed than fit. */
+int dspark_oracle_write(const dspark_oracle_inputs *in, void *const *caches,
+                        int64_t t_begin, int64_t t_end,
+                        int32_t *alt_layer, int64_t *alt_elem, uint16_t *alt_val,
+                        int64_t alt_cap, int64_t *n_alt)
+{
+    int rc = dspark_oracle_check_inputs(in);
+    if (rc != ORACLE_OK)
+        return rc;
+    if (t_begin < 0 || t_end > in->num_ctx || t_begin > t_end)
+        return ORACLE_ERR_ARG;
+    const int L = in->num_layers, H = in->num_kv_heads;
+    const size_t esz = in->kv_dtype == ORACLE_KV_FP8_E4M3 ? 1 : 2;
+    int64_t total_alt = 0;
+    int32_t rd[3 * ORACLE_HEAD_DIM];
+    uint16_t rv[3 * ORACLE_HEAD_DIM];
+    uint16_t row[ORACLE_ROW];
+    for (int64_t t = t_begin; t < t_end; t++) {
+        int64_t slot = in->slot_mapping[t];
+        if (slot < 0)
+            continue; /* padding: not written */
+        for (int l = 0; l < L; l++) {
+            for (int h = 0; h < H; h++) {
+                int32_t na = 0;
+                rc = dspark_oracle_row(in, t, l, h, row, rd, rv, &na);
+                if (rc != ORACLE_OK)
+                    return rc;
+                int64_t dst = dspark_oracle_dest_row(slot, h, H, in->block_size, in->num_blocks);
+                uint8_t *layer = (uint8_t *)caches[l];
+                memcpy(layer + (size_t)dst * ORACLE_ROW * esz, row, ORACLE_ROW * esz);
+                for (int j = 0; j < na; j++) {
+                    if (total_alt < alt_cap) {
+                        alt_layer[total_alt] = l;
+                        alt_elem[total_alt] = dst * ORACLE_ROW + rd[j];
+                        alt_val[total_alt] = rv[j];
+                    }
+                    total_alt++;
+                }
+            }
+        }
+    }
+    if (n_alt)
+        *n_alt = total_alt;
+    return total_alt > alt_cap ? ORACLE_ERR_ALT_CAP : ORACLE_OK;
+}
+
+/* Rows (t, l, h) given as flat indices (t * L + l) * H + h, whatever their
+ * slot: out is [n][256] stored elements; alternates as (index into the row
+ * list, dim, value). */
+int dspark_oracle_rows(const dspark_oracle_inputs *in, const int64_t *row_ids, int64_t n,
+                       void *out, int64_t *alt_row, int32_t *alt_dim, uint16_t *alt_val,
+                       int64_t alt_cap, int64_t *n_alt)
+{
+    const int L = in->num_layers, H = in->num_kv_heads;
+    const size_t esz = in->kv_dtype == ORACLE_KV_FP8_E4M3 ? 1 : 2;
+    int64_t total_alt = 0;
+    int32_t rd[3 * ORACLE_HEAD_DIM];
+    uint16_t rv[3 * ORACLE_HEAD_DIM];
+    for (int64_t i = 0; i < n; i++) {
+        int64_t id = row_ids[i];
+        if (id < 0 || id >= in->num_ctx * L * H)
+            return ORACLE_ERR_ARG;
+        int64_t t = id / ((int64_t)L * H);
+        int32_t l = (int32_t)((id / H) % L);
+        int32_t h = (int32_t)(id % H);
+        int32_t na = 0;
+        int rc = dspark_oracle_row(in, t, l, h, (uint8_t *)out + (size_t)i * ORACLE_ROW * esz,
+                                   rd, rv, &na);
+        if (rc != ORACLE_OK)
+            return rc;
+        for (int j = 0; j < na; j++) {
+            if (total_alt < alt_cap) {
+                alt_row[total_alt] = i;
+                alt_dim[total_alt] = rd[j];
+                alt_val[total_alt] = rv[j];
+            }
+            total_alt++;
+        }
+    }
+    if (n_alt)
+        *n_alt = total_alt;
+    return total_alt > alt_cap ? ORACLE_ERR_ALT_CAP : ORACLE_OK;
+}

@@ -1,0 +1,8 @@
+"""Seeded synthetic inputs shared by the oracle-side tests, the CUDA path's
+tests and the benchmark.  Holds no arithmetic of the write itself."""
+
+from .synth import (  # noqa: F401
+    HEAD_DIM, ROW_ELEMS, PREFILL_BYTE, KV_BF16, KV_FP8, Workload, WORKLOADS,
+    WORKLOADS_BY_NAME, Inputs, generate, make_caches, take_tokens,
+    rope_cos_sin_cache, compulsory_bytes, describe,
+)

@@ -1,0 +1,403 @@
+"""Benchmark of the DSpark fused context-KV write on GB300.
+
+One step = one dspark_ctx_kv_write call over one batch of the workload (all
+layers, all heads, one kernel launch).  Default workload: long context
+(65,536 tokens = 256 requests x 256 at random offsets below 131,072; 5 layers,
+4 KV heads, rotary_dim 16, block size 128, bf16 cache), the largest
+single-GPU workload, whose inputs (671 MB of all_kv) and written rows
+(671 MB) both exceed the 129 MB L2.
+
+Printed (rank 0, one JSON line): metric/value (compulsory GB/s of the whole
+job), rows/s, the kernel's roofline against the measured HBM copy peak, an
+end-to-end figure through the public API with host buffers (pinned host to
+device copies of each step's inputs and a device to host read of the step's
+error word inside the timed region), the CPU oracle as a baseline on a
+bounded sample, and the SM clocks sampled during the timed region.
+
+--impl reference times the CPU oracle (the reference arm of this build).
+Multi-GPU (torchrun): every rank runs its own replica of the workload (the
+write has no exchange step), so scaling is weak.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+import workloads as wk  # noqa: E402
+
+METRIC = "context-KV write GB/s and rows/s on 1 GB300; % of HBM roofline"
+UNIT = "GB/s"
+KERNEL_SRC = os.path.join(ROOT, "speculative_decoding_draft_ctx_gb300", "csrc", "ctx_kv_kernel.cu")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+FALLBACK_HBM_GBS = 6800.0
+
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=4000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--config", default="long_context", choices=[w.name for w in wk.WORKLOADS])
+    ap.add_argument("--e2e-steps", type=int, default=30)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0, help="oracle sample budget")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    return ap.parse_args(argv)
+
+
+# ---------------------------------------------------------------- helpers
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_sha() -> str:
+    with open(KERNEL_SRC, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def recorded_traffic(workload: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel source."""
+    try:
+        with open(TRAFFIC_FILE) as f:
+            d = json.load(f)
+    except (OSError, ValueError):
+        return None
+    e = d.get(workload)
+    if not e or e.get("kernel_sha") != kernel_sha():
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled every 100 ms."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.proc = None
+        try:
+            uuid = str(torch.cuda.get_device_properties(device_index).uuid)
+            sel = uuid if uuid.startswith("GPU-") else f"GPU-{uuid}"
+        except Exception:
+            sel = str(device_index)
+        self.cmd = ["nvidia-smi", "-i", sel, f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                    "-lms", "100"]
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(self.cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.25)
+        return self
+
+    def __exit__(self, *exc):
+        self.out = ""
+        if self.proc is not None:
+            time.sleep(0.15)
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                self.out, _ = self.proc.communicate()
+        return False
+
+    def summary(self):
+        sms, maxs, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in (self.out or "").strip().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sms.append(float(parts[0]))
+                maxs.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[4:8]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sms:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sms), "sm_max_mhz": max(maxs), "reasons": sorted(reasons),
+                "samples": len(sms)}
+
+
+def l2_bytes() -> int:
+    try:
+        return int(torch.cuda.get_device_properties(torch.cuda.current_device()).L2_cache_size)
+    except Exception:
+        return 129 * 2**20
+
+
+# ---------------------------------------------------------------- CPU oracle
+
+class OracleSample:
+    """The oracle's write over the first `tokens` tokens of a workload, set
+    up once and timed per run."""
+
+    def __init__(self, inp: wk.Inputs, tokens: int):
+        import oracle
+
+        self.sub = wk.take_tokens(inp, tokens)
+        self.p = oracle.problem_from_inputs(self.sub)
+        p = self.p
+        # host caches stay untouched except for the sampled rows (lazily backed)
+        shape = (p.num_blocks, p.H, p.block_size, 256)
+        self.caches = [np.empty(shape, dtype=p.elem_dtype) for _ in range(p.L)]
+        nv = self.sub.num_valid_tokens
+        self.bytes = wk.compulsory_bytes(self.sub.workload, nv)
+        self.rows = nv * p.L * p.H
+        self.tokens = tokens
+
+    def run(self) -> float:
+        t0 = time.perf_counter()
+        self.p.write(self.caches, alt_cap=1 << 20)
+        return time.perf_counter() - t0
+
+
+def calibrate_tokens(inp: wk.Inputs, seconds: float) -> int:
+    probe = min(inp.workload.num_ctx, 256)
+    s = OracleSample(inp, probe)
+    s.run()
+    per_tok = max(s.run() / probe, 1e-7)
+    return int(max(1, min(inp.workload.num_ctx, seconds / per_tok)))
+
+
+def cpu_baseline(inp: wk.Inputs, seconds: float):
+    n = calibrate_tokens(inp, seconds)
+    s = OracleSample(inp, n)
+    dt = s.run()
+    return {
+        "value": s.bytes / dt / 1e9, "unit": UNIT, "cores": 1, "kind": "oracle",
+        "rows_per_s": s.rows / dt, "seconds": dt,
+        "sample": f"first {n} of {inp.workload.num_ctx} tokens ({s.rows} valid rows), one thread, plain C oracle",
+    }
+
+
+def run_reference(args):
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    wl = wk.WORKLOADS_BY_NAME[args.config]
+    inp = wk.generate(wl)
+    budget = 90.0  # seconds of oracle work for the whole run
+    per_step = budget / max(1, args.steps + args.warmup)
+    n = calibrate_tokens(inp, per_step)
+    sample = OracleSample(inp, n)
+    for _ in range(args.warmup):
+        sample.run()
+    total_t = sum(sample.run() for _ in range(args.steps))
+    total_b = sample.bytes * args.steps
+    total_r = sample.rows * args.steps
+    value = total_b / total_t / 1e9
+    sample = f"first {n} of {wl.num_ctx} tokens per step, one thread, plain C oracle"
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total_t / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": dict(wk.describe(wl), sample_tokens=n),
+        "rows_per_s": total_r / total_t,
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ---------------------------------------------------------------- GPU
+
+def run_ours(args):
+    import speculative_decoding_draft_ctx_gb300 as dk
+
+    ws, rank, local = dist_env()
+    if not torch.cuda.is_available():
+        raise RuntimeError("bench.py needs a CUDA device")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    pg = None
+    if ws > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl", device_id=dev)
+        pg = dist
+    dk.lib()
+
+    wl = wk.WORKLOADS_BY_NAME[args.config]
+    base = wk.generate(wl, seed=wl.seed + 1000 * rank)
+    fp8 = wl.kv_dtype == wk.KV_FP8
+    nvalid = base.num_valid_tokens
+    step_bytes = wk.compulsory_bytes(wl, nvalid)
+    step_rows = nvalid * wl.num_layers * wl.num_kv_heads
+
+    # input sets rotated across steps so that each step's reads and writes
+    # miss L2 (one set when the workload alone is larger than L2)
+    foot = base.all_kv.numel() * 2 + step_rows * 256 * wl.elem_size
+    n_sets = max(1, math.ceil(3 * l2_bytes() / foot))
+    sets = []
+    for i in range(n_sets):
+        inp = base if i == 0 else wk.generate(wl, seed=wl.seed + 1000 * rank + i)
+        sets.append(inp.to(dev))
+    k_scales = [sets[0].k_scale[l:l + 1].clone() for l in range(wl.num_layers)]
+    v_scales = [sets[0].v_scale[l:l + 1].clone() for l in range(wl.num_layers)]
+    caches = wk.make_caches(wl, device=dev, fill=None)
+    writer = dk.ContextKVWriter(caches, k_scales, v_scales, "fp8" if fp8 else "auto")
+    stream = torch.cuda.current_stream()
+
+    def step(i):
+        d = sets[i % n_sets]
+        writer(d.all_kv, d.knorm_w, d.eps, d.positions, d.cos_sin, wl.rotary_dim, d.slot_mapping)
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    t_begin = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    if pg:
+        pg.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        t_begin.record(stream)
+        for i in range(args.steps):
+            starts[i].record(stream)
+            step(i)
+            ends[i].record(stream)
+        t_end.record(stream)
+        torch.cuda.synchronize()
+    if pg:
+        pg.barrier()
+    total_ms = t_begin.elapsed_time(t_end)
+    launch_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    if pg:
+        t = torch.tensor([total_ms], device=dev)
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        total_ms = float(t.item())
+    avg_launch_ms = sum(launch_ms) / len(launch_ms)
+    value = step_bytes * args.steps * ws / (total_ms * 1e-3) / 1e9
+    rows_per_s = step_rows * args.steps * ws / (total_ms * 1e-3)
+
+    peak, peak_kind = measured_peaks()
+    achieved = step_bytes / (avg_launch_ms * 1e-3) / 1e9
+    traffic = recorded_traffic(wl.name)
+
+    # end to end through the public API: pinned host inputs copied in, the
+    # step's error word read back, every step
+    e2e = None
+    if not args.no_e2e:
+        host = wk.generate(wl, seed=wl.seed + 1000 * rank)
+        h_kv = host.all_kv.pin_memory()
+        h_pos = host.positions.pin_memory()
+        h_slot = host.slot_mapping.pin_memory()
+        d = sets[0]
+        flags = torch.zeros(1, dtype=torch.int32, device=dev)
+        h_flags = torch.zeros(1, dtype=torch.int32).pin_memory()
+        ne = max(1, args.e2e_steps)
+
+        def e2e_step():
+            d.all_kv.copy_(h_kv, non_blocking=True)
+            d.positions.copy_(h_pos, non_blocking=True)
+            d.slot_mapping.copy_(h_slot, non_blocking=True)
+            writer(d.all_kv, d.knorm_w, d.eps, d.positions, d.cos_sin, wl.rotary_dim, d.slot_mapping,
+                   error_flags=flags)
+            h_flags.copy_(flags, non_blocking=True)
+
+        for _ in range(3):
+            e2e_step()
+        torch.cuda.synchronize()
+        if pg:
+            pg.barrier()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(ne):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        e_ms = e0.elapsed_time(e1)
+        if pg:
+            t = torch.tensor([e_ms], device=dev)
+            pg.all_reduce(t, op=pg.ReduceOp.MAX)
+            e_ms = float(t.item())
+        if int(h_flags.item()) != 0:
+            raise RuntimeError(f"write reported error flags {int(h_flags.item())}")
+        e2e = {"value": step_bytes * ne * ws / (e_ms * 1e-3) / 1e9, "unit": UNIT,
+               "h2d_bytes_per_step": h_kv.numel() * 2 + h_pos.numel() * 8 + h_slot.numel() * 8,
+               "d2h_bytes_per_step": 4, "steps": ne, "ms_per_step": e_ms / ne}
+
+    cpu = None
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(base, args.cpu_seconds)
+
+    if rank == 0:
+        clocks = clk.summary()
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": dict(wk.describe(wl), parallelism=f"replicas{ws}", input_sets=n_sets,
+                           l2=("inputs larger than L2" if n_sets == 1 else
+                               f"{n_sets} input sets rotated, footprint > 3x L2")),
+            "rows_per_s": rows_per_s,
+            "bytes_per_step": step_bytes,
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                         "frac": achieved / peak, "traffic": traffic, "peak_source": peak_kind,
+                         "frac_of_8tbs": achieved / 8000.0},
+            "cpu_baseline": cpu,
+            "e2e": e2e,
+            "clocks": clocks,
+            "gpu_launches": args.steps,
+            "kernel_avg_us": avg_launch_ms * 1e3,
+        }
+        print(json.dumps(line), flush=True)
+    if pg:
+        pg.destroy_process_group()
+    return 0
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,189 @@
+/*
+ * dspark_ctx_kv.h -- C ABI of the GB300 (sm_103a) DSpark fused context-KV write.
+ *
+ * One call norms, ropes and stores the context K/V of every draft layer:
+ * it reads K and V of each (token, layer, kv-head) row from the fused
+ * projection output, applies the layer's Gemma RMSNorm to K (fp32, then
+ * rounded to bf16), applies partial NeoX RoPE to the leading rotary_dim dims
+ * of K at the token's position, and stores K|V into the layer's paged cache,
+ * as raw bf16 or as OCP fp8 e4m3 of x / scale.  Tokens whose slot is < 0 are
+ * padding and are neither read nor written.
+ *
+ * Defining passages: vLLM DSpark context-KV writer page (module docstring:
+ * layouts, norm, RoPE, fp8 rule, padding, cache/scale offset tables;
+ * DSparkContextKVWriter._validate, _ensure_tables, __call__;
+ * rotary_dims_supported) and the DSpark draft model page
+ * (MiniMaxM3DSparkModel.precompute_and_store_context_kv, _shared_slot_mapping).
+ *
+ * Conventions for every function below:
+ *  - Pointers documented as "device" must point to device memory of the
+ *    current CUDA device; "host" pointers to host memory.
+ *  - The caller owns every buffer.  dspark_ctx_kv_write allocates nothing,
+ *    synchronises nothing and copies nothing, so it may be captured into a
+ *    CUDA graph.
+ *  - Functions return a dspark_status; none throws, aborts or exits.
+ *    dspark_ctx_kv_last_error() describes the most recent failure of the
+ *    calling thread.
+ */
+#ifndef DSPARK_CTX_KV_H
+#define DSPARK_CTX_KV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define DSPARK_HEAD_DIM 128
+#define DSPARK_CACHE_ROW 256 /* K at [0, 128), V at [128, 256) */
+
+/* Cache element type: raw bf16, or uint8 bytes holding OCP fp8 e4m3 codes. */
+typedef enum { DSPARK_KV_BF16 = 0, DSPARK_KV_FP8_E4M3 = 1 } dspark_kv_dtype;
+
+typedef enum {
+    DSPARK_OK = 0,
+    DSPARK_ERR_INVALID_ARG = 1,            /* null pointer, negative size, bad eps, mismatch */
+    DSPARK_ERR_UNSUPPORTED_ROTARY_DIM = 2, /* rotary_dim not 16, 32 or 64 (head_dim 128) */
+    DSPARK_ERR_BLOCK_SIZE = 3,             /* block_size not a positive power of two */
+    DSPARK_ERR_ALIGNMENT = 4,              /* a buffer or layer offset misaligned */
+    DSPARK_ERR_DTYPE = 5,                  /* unknown kv dtype, or cache dtype mismatch */
+    DSPARK_ERR_CAPTURING = 6,              /* table rebuild requested while capturing */
+    DSPARK_ERR_CUDA = 7,                   /* a CUDA runtime call failed */
+} dspark_status;
+
+/* Bits the kernel ORs into *error_flags (dspark_ctx_kv_write_ex).  A row
+ * whose slot or position is out of range is skipped (nothing is written for
+ * it) and reported; in-range rows are unaffected. */
+#define DSPARK_FLAG_SLOT_RANGE 0x1u /* slot >= num_blocks * block_size */
+#define DSPARK_FLAG_POS_RANGE 0x2u  /* position < 0 or >= max_pos (valid slot) */
+
+/*
+ * dspark_ctx_kv_write -- the fused write (writer page, module docstring and
+ * DSparkContextKVWriter.__call__; one launch for all layers).
+ *
+ *  all_kv        device, bf16 [num_ctx, L, 2, nkv, 128] contiguous, 16-byte
+ *                aligned: [t, l, 0, h, :] is K, [t, l, 1, h, :] is V.
+ *  knorm_w       device, bf16 [L, 128] contiguous, 16-byte aligned: the
+ *                per-layer Gemma K-norm weights w, applied as (1 + w).
+ *  positions     device, int64 [num_ctx]: rotary position of each token
+ *                (shared by all layers).
+ *  slot_mapping  device, int64 [num_ctx], shared by all layers; < 0 marks
+ *                padding.  Valid slots must be distinct and below
+ *                num_blocks * block_size (duplicates race; out-of-range rows
+ *                are skipped and flagged).
+ *  num_ctx       number of tokens; 0 returns DSPARK_OK without a launch.
+ *  cos_sin       device, bf16 [max_pos, rotary_dim] contiguous, 16-byte
+ *                aligned: cos(pos * f_i) in [0, r/2), sin in [r/2, r).
+ *  max_pos       rows of cos_sin (positions outside [0, max_pos) are
+ *                skipped and flagged).
+ *  layer0_cache  device, layer 0's cache [num_blocks, nkv, block_size, 256]
+ *                of bf16 or uint8 (fp8), 16-byte aligned.  Layer l's cache
+ *                starts cache_offsets[l] elements after it.
+ *  num_blocks    blocks per layer cache.
+ *  cache_offsets device, int64 [L]: element offset of each layer's cache from
+ *                layer0_cache (multiples of 16 elements, may be negative;
+ *                cache_offsets[0] is normally 0).  See the table builder.
+ *  k_scales,     device, [L] arrays of device pointers to each layer's fp32
+ *  v_scales      k / v scale (read when the kernel runs, so a graph replay
+ *                sees current values).  Ignored (may be NULL) for bf16.
+ *  L, nkv        draft layers and KV heads per layer (>= 1).
+ *  block_size    tokens per cache block: a power of two.
+ *  rotary_dim    16, 32 or 64.
+ *  eps           the norm's epsilon (finite, >= 0).
+ *  kv_dtype      a dspark_kv_dtype.
+ *  stream        the CUDA stream the kernel is enqueued on.
+ */
+int dspark_ctx_kv_write(const void *all_kv, const void *knorm_w, const int64_t *positions,
+                        const int64_t *slot_mapping, int64_t num_ctx, const void *cos_sin,
+                        int64_t max_pos, void *layer0_cache, int64_t num_blocks,
+                        const int64_t *cache_offsets, const float *const *k_scales,
+                        const float *const *v_scales, int L, int nkv, int block_size,
+                        int rotary_dim, float eps, int kv_dtype, cudaStream_t stream);
+
+/* As dspark_ctx_kv_write, and the kernel ORs DSPARK_FLAG_* bits into
+ * *error_flags (device, 4-byte aligned; NULL disables reporting).  The
+ * caller clears the word; the call never does. */
+int dspark_ctx_kv_write_ex(const void *all_kv, const void *knorm_w, const int64_t *positions,
+                           const int64_t *slot_mapping, int64_t num_ctx, const void *cos_sin,
+                           int64_t max_pos, void *layer0_cache, int64_t num_blocks,
+                           const int64_t *cache_offsets, const float *const *k_scales,
+                           const float *const *v_scales, int L, int nkv, int block_size,
+                           int rotary_dim, float eps, int kv_dtype, unsigned int *error_flags,
+                           cudaStream_t stream);
+
+/* 1 when the kernel handles this head (writer page, rotary_dims_supported:
+ * head_dim 128 and rotary_dim 16, 32 or 64), else 0. */
+int dspark_ctx_kv_rotary_dims_supported(int rotary_dim, int head_dim);
+
+/*
+ * Per-layer cache description for the layout check (writer page,
+ * DSparkContextKVWriter._validate).  All fields describe the caller's
+ * tensors; nothing is dereferenced.
+ */
+typedef struct {
+    const void *data;      /* device address of the layer's cache */
+    int64_t shape[4];      /* [num_blocks, nkv, block_size, 256] expected */
+    int64_t stride[4];     /* in elements */
+    int32_t ndim;
+    int32_t elem_size;     /* bytes per element */
+    int32_t cache_dtype;   /* dspark_kv_dtype of the cache tensor's element type
+                              (bf16 -> DSPARK_KV_BF16, uint8 -> DSPARK_KV_FP8_E4M3,
+                              anything else -> -1) */
+    int32_t kv_dtype;      /* the layer's configured kv dtype (dspark_kv_dtype, -1 unknown) */
+    const void *k_scale;   /* device address of the fp32 k scale */
+    const void *v_scale;
+    int32_t scales_ok;     /* 1 when both scales are fp32 tensors on the GPU */
+} dspark_cache_desc;
+
+/* DSPARK_OK when the layers form a layout the write supports: at least one
+ * layer; 4-D contiguous caches with last dim 256; power-of-two block size;
+ * fp8 caches are uint8 and bf16 caches are bf16; fp32 device scales; all
+ * layers share shape, stride and dtype; every cache starts a multiple of 16
+ * elements from layer 0's.  Otherwise the status of the first violation. */
+int dspark_ctx_kv_validate_layers(int L, const dspark_cache_desc *layers);
+
+/*
+ * Offset/pointer tables (writer page, DSparkContextKVWriter._ensure_tables):
+ * cache_offsets[L] (int64 element offsets from layer 0's cache) and the k /
+ * v scale pointer tables, in device memory owned by the object.  The tables
+ * are rebuilt only when the key (every layer's cache and scale address and
+ * the element size) changes, so launches captured in a CUDA graph keep
+ * addressing the same memory.
+ */
+typedef struct dspark_ctx_kv_tables dspark_ctx_kv_tables;
+
+/* Allocates the object and its device tables (cudaMalloc on the current
+ * device: call outside stream capture). */
+int dspark_ctx_kv_tables_create(int L, dspark_ctx_kv_tables **out);
+
+/* layer_caches, k_scale_ptrs, v_scale_ptrs: host arrays [L] of device
+ * addresses.  Same key as the last successful update: DSPARK_OK, nothing
+ * enqueued.  New key: validates alignment (16 elements) and enqueues the
+ * host-to-device copy of the new tables on `stream`, unless `stream` is
+ * capturing, which returns DSPARK_ERR_CAPTURING and keeps the old tables.
+ * The tables must not be updated while launches that read them are still
+ * running on another stream. */
+int dspark_ctx_kv_tables_update(dspark_ctx_kv_tables *tables, void *const *layer_caches,
+                                size_t elem_size, const float *const *k_scale_ptrs,
+                                const float *const *v_scale_ptrs, cudaStream_t stream);
+
+const int64_t *dspark_ctx_kv_tables_cache_offsets(const dspark_ctx_kv_tables *tables);
+const float *const *dspark_ctx_kv_tables_k_scales(const dspark_ctx_kv_tables *tables);
+const float *const *dspark_ctx_kv_tables_v_scales(const dspark_ctx_kv_tables *tables);
+/* Number of times the tables were (re)built: 0 before the first update. */
+int64_t dspark_ctx_kv_tables_builds(const dspark_ctx_kv_tables *tables);
+void dspark_ctx_kv_tables_destroy(dspark_ctx_kv_tables *tables);
+
+/* Text of the calling thread's most recent error ("" if none). */
+const char *dspark_ctx_kv_last_error(void);
+/* Name of a dspark_status value. */
+const char *dspark_ctx_kv_status_string(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DSPARK_CTX_KV_H */

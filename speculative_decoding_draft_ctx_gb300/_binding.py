@@ -1,0 +1,249 @@
+"""ctypes binding of libdspark_ctx_kv.so (include/dspark_ctx_kv.h).
+
+Argument marshalling only: tensors become device addresses and sizes, the
+current torch stream becomes the cudaStream_t, and a non-zero status becomes
+a DSparkError.  Every step of the write runs in the library's kernel; there
+is no other implementation to fall back to, so a missing or unloadable
+library raises at first use.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+from . import build as _build
+
+KV_BF16 = 0
+KV_FP8_E4M3 = 1
+HEAD_DIM = 128
+CACHE_ROW = 256
+
+STATUS = {
+    0: "DSPARK_OK", 1: "DSPARK_ERR_INVALID_ARG", 2: "DSPARK_ERR_UNSUPPORTED_ROTARY_DIM",
+    3: "DSPARK_ERR_BLOCK_SIZE", 4: "DSPARK_ERR_ALIGNMENT", 5: "DSPARK_ERR_DTYPE",
+    6: "DSPARK_ERR_CAPTURING", 7: "DSPARK_ERR_CUDA",
+}
+STATUS_CODE = {v: k for k, v in STATUS.items()}
+FLAG_SLOT_RANGE = 0x1
+FLAG_POS_RANGE = 0x2
+
+# every function the header declares
+EXPORTS = (
+    "dspark_ctx_kv_write", "dspark_ctx_kv_write_ex", "dspark_ctx_kv_rotary_dims_supported",
+    "dspark_ctx_kv_validate_layers", "dspark_ctx_kv_tables_create", "dspark_ctx_kv_tables_update",
+    "dspark_ctx_kv_tables_cache_offsets", "dspark_ctx_kv_tables_k_scales",
+    "dspark_ctx_kv_tables_v_scales", "dspark_ctx_kv_tables_builds", "dspark_ctx_kv_tables_destroy",
+    "dspark_ctx_kv_last_error", "dspark_ctx_kv_status_string",
+)
+
+
+class DSparkError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"{STATUS.get(status, status)}: {message}")
+        self.status = status
+        self.name = STATUS.get(status, str(status))
+
+
+class CacheDesc(ctypes.Structure):
+    _fields_ = [
+        ("data", ctypes.c_void_p), ("shape", ctypes.c_int64 * 4), ("stride", ctypes.c_int64 * 4),
+        ("ndim", ctypes.c_int32), ("elem_size", ctypes.c_int32), ("cache_dtype", ctypes.c_int32),
+        ("kv_dtype", ctypes.c_int32), ("k_scale", ctypes.c_void_p), ("v_scale", ctypes.c_void_p),
+        ("scales_ok", ctypes.c_int32),
+    ]
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def library_path() -> str:
+    return _build.LIB_PATH
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded library.  Raises when it has not been built."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        path = _build.LIB_PATH
+        if not os.path.exists(path):
+            raise RuntimeError(f"{path} is missing: build it first (speculative_decoding_draft_ctx_gb300.build.build())")
+        L = ctypes.CDLL(path)
+        P, I, I64 = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64
+        write_args = [P, P, P, P, I64, P, I64, P, I64, P, P, P, I, I, I, I, ctypes.c_float, I]
+        L.dspark_ctx_kv_write.argtypes = write_args + [P]
+        L.dspark_ctx_kv_write.restype = I
+        L.dspark_ctx_kv_write_ex.argtypes = write_args + [P, P]
+        L.dspark_ctx_kv_write_ex.restype = I
+        L.dspark_ctx_kv_rotary_dims_supported.argtypes = [I, I]
+        L.dspark_ctx_kv_rotary_dims_supported.restype = I
+        L.dspark_ctx_kv_validate_layers.argtypes = [I, ctypes.POINTER(CacheDesc)]
+        L.dspark_ctx_kv_validate_layers.restype = I
+        L.dspark_ctx_kv_tables_create.argtypes = [I, ctypes.POINTER(P)]
+        L.dspark_ctx_kv_tables_create.restype = I
+        L.dspark_ctx_kv_tables_update.argtypes = [P, P, ctypes.c_size_t, P, P, P]
+        L.dspark_ctx_kv_tables_update.restype = I
+        for n in ("dspark_ctx_kv_tables_cache_offsets", "dspark_ctx_kv_tables_k_scales",
+                  "dspark_ctx_kv_tables_v_scales"):
+            getattr(L, n).argtypes = [P]
+            getattr(L, n).restype = P
+        L.dspark_ctx_kv_tables_builds.argtypes = [P]
+        L.dspark_ctx_kv_tables_builds.restype = I64
+        L.dspark_ctx_kv_tables_destroy.argtypes = [P]
+        L.dspark_ctx_kv_tables_destroy.restype = None
+        L.dspark_ctx_kv_last_error.argtypes = []
+        L.dspark_ctx_kv_last_error.restype = ctypes.c_char_p
+        L.dspark_ctx_kv_status_string.argtypes = [I]
+        L.dspark_ctx_kv_status_string.restype = ctypes.c_char_p
+        _lib = L
+        return L
+
+
+def check(status: int):
+    if status != 0:
+        raise DSparkError(status, lib().dspark_ctx_kv_last_error().decode())
+
+
+def _addr(x) -> int:
+    """Device address of a tensor, or an int address as is (0 = NULL)."""
+    if x is None:
+        return 0
+    if isinstance(x, int):
+        return x
+    return x.data_ptr()
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        import torch
+
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def kv_dtype_code(kv_dtype) -> int:
+    if kv_dtype in (KV_BF16, "bf16", "auto", "bfloat16"):
+        return KV_BF16
+    if kv_dtype in (KV_FP8_E4M3, "fp8", "fp8_e4m3"):
+        return KV_FP8_E4M3
+    return -1
+
+
+def dspark_ctx_kv_write(all_kv, knorm_w, positions, slot_mapping, num_ctx, cos_sin, max_pos,
+                        layer0_cache, num_blocks, cache_offsets, k_scales, v_scales, L, nkv,
+                        block_size, rotary_dim, eps, kv_dtype, stream=None):
+    """``dspark_ctx_kv_write`` of the C ABI: tensors (or int addresses) in,
+    DSparkError on a non-OK status."""
+    check(lib().dspark_ctx_kv_write(
+        _addr(all_kv), _addr(knorm_w), _addr(positions), _addr(slot_mapping), int(num_ctx),
+        _addr(cos_sin), int(max_pos), _addr(layer0_cache), int(num_blocks), _addr(cache_offsets),
+        _addr(k_scales), _addr(v_scales), int(L), int(nkv), int(block_size), int(rotary_dim),
+        float(eps), kv_dtype_code(kv_dtype), _stream(stream)))
+
+
+def dspark_ctx_kv_write_ex(all_kv, knorm_w, positions, slot_mapping, num_ctx, cos_sin, max_pos,
+                           layer0_cache, num_blocks, cache_offsets, k_scales, v_scales, L, nkv,
+                           block_size, rotary_dim, eps, kv_dtype, error_flags, stream=None):
+    """``dspark_ctx_kv_write_ex``: as dspark_ctx_kv_write, plus the device
+    error word (an int32 tensor of one element, or an address)."""
+    check(lib().dspark_ctx_kv_write_ex(
+        _addr(all_kv), _addr(knorm_w), _addr(positions), _addr(slot_mapping), int(num_ctx),
+        _addr(cos_sin), int(max_pos), _addr(layer0_cache), int(num_blocks), _addr(cache_offsets),
+        _addr(k_scales), _addr(v_scales), int(L), int(nkv), int(block_size), int(rotary_dim),
+        float(eps), kv_dtype_code(kv_dtype), _addr(error_flags), _stream(stream)))
+
+
+def dspark_ctx_kv_rotary_dims_supported(rotary_dim: int, head_dim: int) -> bool:
+    return bool(lib().dspark_ctx_kv_rotary_dims_supported(int(rotary_dim), int(head_dim)))
+
+
+def dspark_ctx_kv_status_string(status: int) -> str:
+    return lib().dspark_ctx_kv_status_string(int(status)).decode()
+
+
+def dspark_ctx_kv_last_error() -> str:
+    return lib().dspark_ctx_kv_last_error().decode()
+
+
+def cache_desc(cache, kv_cache_dtype, k_scale, v_scale) -> CacheDesc:
+    """Describe one layer's cache tensor and scales for the layout check."""
+    import torch
+
+    d = CacheDesc()
+    bound = isinstance(cache, torch.Tensor) and cache.numel() > 0
+    d.data = cache.data_ptr() if bound else 0
+    nd = cache.dim() if isinstance(cache, torch.Tensor) else 0
+    d.ndim = nd
+    for i in range(min(nd, 4)):
+        d.shape[i] = cache.shape[i]
+        d.stride[i] = cache.stride(i)
+    if isinstance(cache, torch.Tensor):
+        d.elem_size = cache.element_size()
+        d.cache_dtype = {torch.bfloat16: KV_BF16, torch.uint8: KV_FP8_E4M3}.get(cache.dtype, -1)
+    d.kv_dtype = kv_dtype_code(kv_cache_dtype)
+
+    def fp32_cuda(s):
+        return isinstance(s, torch.Tensor) and s.dtype == torch.float32 and s.is_cuda
+
+    d.scales_ok = int(fp32_cuda(k_scale) and fp32_cuda(v_scale))
+    d.k_scale = k_scale.data_ptr() if isinstance(k_scale, torch.Tensor) else 0
+    d.v_scale = v_scale.data_ptr() if isinstance(v_scale, torch.Tensor) else 0
+    return d
+
+
+def dspark_ctx_kv_validate_layers(descs) -> None:
+    arr = (CacheDesc * len(descs))(*descs)
+    check(lib().dspark_ctx_kv_validate_layers(len(descs), arr))
+
+
+class Tables:
+    """Owner of one dspark_ctx_kv_tables object."""
+
+    def __init__(self, L: int):
+        h = ctypes.c_void_p()
+        check(lib().dspark_ctx_kv_tables_create(int(L), ctypes.byref(h)))
+        self._h = h
+        self.L = int(L)
+
+    def update(self, caches, k_scales, v_scales, stream=None):
+        L = self.L
+        cp = (ctypes.c_void_p * L)(*[_addr(c) for c in caches])
+        kp = (ctypes.c_void_p * L)(*[_addr(s) for s in k_scales]) if k_scales is not None else None
+        vp = (ctypes.c_void_p * L)(*[_addr(s) for s in v_scales]) if v_scales is not None else None
+        esize = caches[0].element_size() if hasattr(caches[0], "element_size") else 2
+        check(lib().dspark_ctx_kv_tables_update(self._h, cp, esize, kp, vp, _stream(stream)))
+
+    @property
+    def cache_offsets(self) -> int:
+        return lib().dspark_ctx_kv_tables_cache_offsets(self._h) or 0
+
+    @property
+    def k_scales(self) -> int:
+        return lib().dspark_ctx_kv_tables_k_scales(self._h) or 0
+
+    @property
+    def v_scales(self) -> int:
+        return lib().dspark_ctx_kv_tables_v_scales(self._h) or 0
+
+    @property
+    def builds(self) -> int:
+        return int(lib().dspark_ctx_kv_tables_builds(self._h))
+
+    def close(self):
+        if self._h is not None and self._h.value:
+            lib().dspark_ctx_kv_tables_destroy(self._h)
+        self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

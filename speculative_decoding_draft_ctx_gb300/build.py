@@ -1,0 +1,82 @@
+"""In-tree build of libdspark_ctx_kv.so for sm_103a (no cmake, no torch
+extension machinery): the kernel TU is compiled by nvcc and the host TU by
+g++ in parallel, then linked by nvcc against the static CUDA runtime."""
+
+from __future__ import annotations
+
+import os
+import shutil
+import subprocess
+import sys
+import threading
+from concurrent.futures import ThreadPoolExecutor
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+ROOT = os.path.dirname(PKG)
+CSRC = os.path.join(PKG, "csrc")
+INCLUDE = os.path.join(ROOT, "include")
+BUILD_DIR = os.path.join(PKG, "_build")
+LIB_NAME = "libdspark_ctx_kv.so"
+LIB_PATH = os.path.join(PKG, LIB_NAME)
+
+ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
+KERNEL_SRC = os.path.join(CSRC, "ctx_kv_kernel.cu")
+API_SRC = os.path.join(CSRC, "ctx_kv_api.cpp")
+HEADERS = [os.path.join(CSRC, "ctx_kv_internal.h"), os.path.join(INCLUDE, "dspark_ctx_kv.h")]
+
+_lock = threading.Lock()
+
+
+def cuda_home() -> str:
+    home = os.environ.get("CUDA_HOME") or os.environ.get("CUDA_PATH")
+    if home:
+        return home
+    nvcc = shutil.which("nvcc")
+    if nvcc:
+        return os.path.dirname(os.path.dirname(os.path.realpath(nvcc)))
+    return "/usr/local/cuda"
+
+
+def _stale() -> bool:
+    if not os.path.exists(LIB_PATH):
+        return True
+    t = os.path.getmtime(LIB_PATH)
+    return any(os.path.getmtime(s) > t for s in [KERNEL_SRC, API_SRC, *HEADERS])
+
+
+def _run(cmd):
+    r = subprocess.run(cmd, capture_output=True, text=True)
+    if r.returncode != 0:
+        raise RuntimeError(f"build step failed ({' '.join(cmd)}):\n{r.stdout}\n{r.stderr}")
+    return r.stdout + r.stderr
+
+
+def build(force: bool = False, verbose: bool = False) -> str:
+    """Compile the library if a source is newer than it; returns its path."""
+    with _lock:
+        if not force and not _stale():
+            return LIB_PATH
+        os.makedirs(BUILD_DIR, exist_ok=True)
+        home = cuda_home()
+        nvcc = os.path.join(home, "bin", "nvcc")
+        kobj = os.path.join(BUILD_DIR, "ctx_kv_kernel.o")
+        aobj = os.path.join(BUILD_DIR, "ctx_kv_api.o")
+        kcmd = [nvcc, *ARCH, "-lineinfo", "-O3", "-std=c++17", "-Xcompiler", "-fPIC",
+                "-I", INCLUDE, "-c", KERNEL_SRC, "-o", kobj]
+        if verbose:
+            kcmd.insert(1, "-Xptxas=-v")
+        acmd = ["g++", "-O2", "-std=c++17", "-fPIC", "-Wall", "-I", os.path.join(home, "include"),
+                "-I", INCLUDE, "-c", API_SRC, "-o", aobj]
+        with ThreadPoolExecutor(2) as ex:
+            outs = list(ex.map(_run, [kcmd, acmd]))
+        if verbose:
+            sys.stderr.write(outs[0])
+        tmp = LIB_PATH + f".tmp{os.getpid()}"
+        _run([nvcc, *ARCH, "-shared", "-o", tmp, kobj, aobj, "-lpthread", "-ldl", "-lrt"])
+        os.replace(tmp, LIB_PATH)
+        return LIB_PATH
+
+
+if __name__ == "__main__":
+    build(force=True, verbose="-v" in sys.argv)
+    print(LIB_PATH)

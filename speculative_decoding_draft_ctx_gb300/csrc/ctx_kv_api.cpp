@@ -1,0 +1,324 @@
+// C-ABI host layer of the DSpark fused context-KV write: argument checks,
+// the layout check, the capture-safe offset/pointer tables and the launch.
+//
+// Defining passages: vLLM DSpark context-KV writer page --
+// DSparkContextKVWriter._validate (layout rules), .supported, _ensure_tables
+// (per-layer cache element offsets and scale addresses, rebuilt only when the
+// data_ptrs change so CUDA-graph replays keep addressing the same memory),
+// __call__ (num_ctx == 0 launches nothing), rotary_dims_supported (head_dim
+// 128, rotary_dim 16/32/64).
+#include "../../include/dspark_ctx_kv.h"
+
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <new>
+#include <vector>
+
+#include "ctx_kv_internal.h"
+
+namespace {
+
+thread_local char g_last_error[512] = "";
+
+int fail(int status, const char *fmt, ...)
+{
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_last_error, sizeof g_last_error, fmt, ap);
+    va_end(ap);
+    return status;
+}
+
+int ok()
+{
+    g_last_error[0] = '\0';
+    return DSPARK_OK;
+}
+
+bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+bool pow2(int64_t v) { return v > 0 && (v & (v - 1)) == 0; }
+
+int log2_exact(int64_t v)
+{
+    int n = 0;
+    while ((int64_t(1) << n) < v)
+        n++;
+    return n;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *dspark_ctx_kv_last_error(void) { return g_last_error; }
+
+const char *dspark_ctx_kv_status_string(int status)
+{
+    switch (status) {
+    case DSPARK_OK: return "DSPARK_OK";
+    case DSPARK_ERR_INVALID_ARG: return "DSPARK_ERR_INVALID_ARG";
+    case DSPARK_ERR_UNSUPPORTED_ROTARY_DIM: return "DSPARK_ERR_UNSUPPORTED_ROTARY_DIM";
+    case DSPARK_ERR_BLOCK_SIZE: return "DSPARK_ERR_BLOCK_SIZE";
+    case DSPARK_ERR_ALIGNMENT: return "DSPARK_ERR_ALIGNMENT";
+    case DSPARK_ERR_DTYPE: return "DSPARK_ERR_DTYPE";
+    case DSPARK_ERR_CAPTURING: return "DSPARK_ERR_CAPTURING";
+    case DSPARK_ERR_CUDA: return "DSPARK_ERR_CUDA";
+    default: return "DSPARK_ERR_UNKNOWN";
+    }
+}
+
+int dspark_ctx_kv_rotary_dims_supported(int rotary_dim, int head_dim)
+{
+    return head_dim == DSPARK_HEAD_DIM && (rotary_dim == 16 || rotary_dim == 32 || rotary_dim == 64);
+}
+
+int dspark_ctx_kv_write_ex(const void *all_kv, const void *knorm_w, const int64_t *positions,
+                           const int64_t *slot_mapping, int64_t num_ctx, const void *cos_sin,
+                           int64_t max_pos, void *layer0_cache, int64_t num_blocks,
+                           const int64_t *cache_offsets, const float *const *k_scales,
+                           const float *const *v_scales, int L, int nkv, int block_size,
+                           int rotary_dim, float eps, int kv_dtype, unsigned int *error_flags,
+                           cudaStream_t stream)
+{
+    // Scalar checks first: they need no device and no pointer.
+    if (num_ctx < 0)
+        return fail(DSPARK_ERR_INVALID_ARG, "num_ctx %lld < 0", (long long)num_ctx);
+    if (L <= 0 || nkv <= 0)
+        return fail(DSPARK_ERR_INVALID_ARG, "L=%d nkv=%d must be >= 1", L, nkv);
+    if (num_blocks <= 0 || max_pos <= 0)
+        return fail(DSPARK_ERR_INVALID_ARG, "num_blocks=%lld max_pos=%lld must be >= 1",
+                    (long long)num_blocks, (long long)max_pos);
+    if (!dspark_ctx_kv_rotary_dims_supported(rotary_dim, DSPARK_HEAD_DIM))
+        return fail(DSPARK_ERR_UNSUPPORTED_ROTARY_DIM, "rotary_dim %d not in {16, 32, 64}", rotary_dim);
+    if (!pow2(block_size))
+        return fail(DSPARK_ERR_BLOCK_SIZE, "block size %d is not a power of two", block_size);
+    if (kv_dtype != DSPARK_KV_BF16 && kv_dtype != DSPARK_KV_FP8_E4M3)
+        return fail(DSPARK_ERR_DTYPE, "kv dtype %d unknown", kv_dtype);
+    if (!(eps >= 0.0f) || std::isinf(eps))
+        return fail(DSPARK_ERR_INVALID_ARG, "eps must be finite and >= 0");
+    const int64_t capacity = num_blocks * (int64_t)block_size;
+    if (capacity / block_size != num_blocks || num_blocks > (INT64_MAX / nkv) / block_size / DSPARK_CACHE_ROW)
+        return fail(DSPARK_ERR_INVALID_ARG, "cache of %lld blocks too large", (long long)num_blocks);
+    if (num_ctx > (INT64_MAX / L) / nkv / (2 * DSPARK_HEAD_DIM))
+        return fail(DSPARK_ERR_INVALID_ARG, "num_ctx %lld too large", (long long)num_ctx);
+    if (num_ctx == 0)
+        return ok();  // nothing to store, and no launch
+
+    if (!all_kv || !knorm_w || !positions || !slot_mapping || !cos_sin || !layer0_cache || !cache_offsets)
+        return fail(DSPARK_ERR_INVALID_ARG, "null buffer pointer");
+    if (kv_dtype == DSPARK_KV_FP8_E4M3 && (!k_scales || !v_scales))
+        return fail(DSPARK_ERR_INVALID_ARG, "fp8 cache needs k_scales and v_scales");
+    if (!aligned(all_kv, 16) || !aligned(knorm_w, 16) || !aligned(cos_sin, 16) || !aligned(layer0_cache, 16))
+        return fail(DSPARK_ERR_ALIGNMENT, "all_kv, knorm_w, cos_sin and layer0_cache must be 16-byte aligned");
+    if (!aligned(positions, 8) || !aligned(slot_mapping, 8) || !aligned(cache_offsets, 8) ||
+        (k_scales && !aligned(k_scales, 8)) || (v_scales && !aligned(v_scales, 8)))
+        return fail(DSPARK_ERR_ALIGNMENT, "int64 and pointer tables must be 8-byte aligned");
+    if (error_flags && !aligned(error_flags, 4))
+        return fail(DSPARK_ERR_ALIGNMENT, "error_flags must be 4-byte aligned");
+
+    dspark::CtxKvParams p{};
+    p.all_kv = static_cast<const uint16_t *>(all_kv);
+    p.knorm_w = static_cast<const uint16_t *>(knorm_w);
+    p.positions = positions;
+    p.slot_mapping = slot_mapping;
+    p.cos_sin = static_cast<const uint16_t *>(cos_sin);
+    p.cache0 = static_cast<unsigned char *>(layer0_cache);
+    p.cache_offsets = cache_offsets;
+    p.k_scales = k_scales;
+    p.v_scales = v_scales;
+    p.error_flags = error_flags;
+    p.num_ctx = num_ctx;
+    p.max_pos = max_pos;
+    p.capacity = capacity;
+    p.num_layers = L;
+    p.num_kv_heads = nkv;
+    p.block_size_log2 = log2_exact(block_size);
+    p.eps = eps;
+    cudaError_t e = dspark::launch_ctx_kv_write(p, rotary_dim, kv_dtype == DSPARK_KV_FP8_E4M3, stream);
+    if (e != cudaSuccess)
+        return fail(DSPARK_ERR_CUDA, "launch failed: %s", cudaGetErrorString(e));
+    return ok();
+}
+
+int dspark_ctx_kv_write(const void *all_kv, const void *knorm_w, const int64_t *positions,
+                        const int64_t *slot_mapping, int64_t num_ctx, const void *cos_sin,
+                        int64_t max_pos, void *layer0_cache, int64_t num_blocks,
+                        const int64_t *cache_offsets, const float *const *k_scales,
+                        const float *const *v_scales, int L, int nkv, int block_size,
+                        int rotary_dim, float eps, int kv_dtype, cudaStream_t stream)
+{
+    return dspark_ctx_kv_write_ex(all_kv, knorm_w, positions, slot_mapping, num_ctx, cos_sin, max_pos,
+                                  layer0_cache, num_blocks, cache_offsets, k_scales, v_scales, L, nkv,
+                                  block_size, rotary_dim, eps, kv_dtype, nullptr, stream);
+}
+
+int dspark_ctx_kv_validate_layers(int L, const dspark_cache_desc *layers)
+{
+    if (L <= 0 || !layers)
+        return fail(DSPARK_ERR_INVALID_ARG, "no layers");
+    const dspark_cache_desc &ref = layers[0];
+    for (int l = 0; l < L; l++) {
+        const dspark_cache_desc &a = layers[l];
+        if (a.kv_dtype != DSPARK_KV_BF16 && a.kv_dtype != DSPARK_KV_FP8_E4M3)
+            return fail(DSPARK_ERR_DTYPE, "layer %d: kv_cache_dtype unsupported", l);
+        if (!a.data)
+            return fail(DSPARK_ERR_INVALID_ARG, "layer %d: KV cache not bound", l);
+        if (a.ndim != 4 || a.shape[3] != DSPARK_CACHE_ROW)
+            return fail(DSPARK_ERR_INVALID_ARG, "layer %d: unexpected cache shape", l);
+        for (int d = 0; d < 4; d++)
+            if (a.shape[d] <= 0)
+                return fail(DSPARK_ERR_INVALID_ARG, "layer %d: KV cache not bound (empty)", l);
+        if (!pow2(a.shape[2]))
+            return fail(DSPARK_ERR_BLOCK_SIZE, "layer %d: block size %lld is not a power of two", l,
+                        (long long)a.shape[2]);
+        int64_t expect = 1;
+        for (int d = 3; d >= 0; d--) {
+            if (a.shape[d] != 1 && a.stride[d] != expect)
+                return fail(DSPARK_ERR_INVALID_ARG, "layer %d: cache is not contiguous", l);
+            expect *= a.shape[d];
+        }
+        if (a.kv_dtype == DSPARK_KV_FP8_E4M3) {
+            if (a.cache_dtype != DSPARK_KV_FP8_E4M3 || a.elem_size != 1)
+                return fail(DSPARK_ERR_DTYPE, "layer %d: fp8 cache is not uint8", l);
+        } else if (a.cache_dtype != DSPARK_KV_BF16 || a.elem_size != 2) {
+            return fail(DSPARK_ERR_DTYPE, "layer %d: cache is not bf16", l);
+        }
+        if (!a.scales_ok || !a.k_scale || !a.v_scale)
+            return fail(DSPARK_ERR_INVALID_ARG, "layer %d: k/v scale is not a CUDA fp32 tensor", l);
+        bool same = a.ndim == ref.ndim && a.elem_size == ref.elem_size &&
+                    a.cache_dtype == ref.cache_dtype && a.kv_dtype == ref.kv_dtype;
+        for (int d = 0; d < 4; d++)
+            same = same && a.shape[d] == ref.shape[d] && a.stride[d] == ref.stride[d];
+        if (!same)
+            return fail(DSPARK_ERR_INVALID_ARG, "layers do not share cache shape/stride/dtype");
+        const int64_t delta = (int64_t)(reinterpret_cast<uintptr_t>(a.data) - reinterpret_cast<uintptr_t>(ref.data));
+        if (delta % (16 * (int64_t)a.elem_size) != 0)
+            return fail(DSPARK_ERR_ALIGNMENT, "layer caches are not 16-element aligned to each other");
+    }
+    return ok();
+}
+
+}  // extern "C"
+
+// --------------------------------------------------------------------------
+// Offset / pointer tables.
+
+struct dspark_ctx_kv_tables {
+    int L = 0;
+    int device = -1;
+    int64_t *d_offsets = nullptr;         // [L]
+    const float **d_scales = nullptr;     // [2L]: k then v
+    std::vector<uintptr_t> key;           // caches, k scales, v scales, elem size
+    int64_t builds = 0;
+};
+
+extern "C" {
+
+int dspark_ctx_kv_tables_create(int L, dspark_ctx_kv_tables **out)
+{
+    if (!out || L <= 0)
+        return fail(DSPARK_ERR_INVALID_ARG, "tables_create: L=%d", L);
+    *out = nullptr;
+    auto *t = new (std::nothrow) dspark_ctx_kv_tables();
+    if (!t)
+        return fail(DSPARK_ERR_INVALID_ARG, "tables_create: out of host memory");
+    t->L = L;
+    cudaError_t e = cudaGetDevice(&t->device);
+    if (e == cudaSuccess)
+        e = cudaMalloc(reinterpret_cast<void **>(&t->d_offsets), sizeof(int64_t) * L);
+    if (e == cudaSuccess)
+        e = cudaMalloc(reinterpret_cast<void **>(&t->d_scales), sizeof(float *) * 2 * L);
+    if (e != cudaSuccess) {
+        cudaFree(t->d_offsets);
+        delete t;
+        return fail(DSPARK_ERR_CUDA, "tables_create: %s", cudaGetErrorString(e));
+    }
+    *out = t;
+    return ok();
+}
+
+int dspark_ctx_kv_tables_update(dspark_ctx_kv_tables *t, void *const *layer_caches, size_t elem_size,
+                                const float *const *k_scale_ptrs, const float *const *v_scale_ptrs,
+                                cudaStream_t stream)
+{
+    if (!t || !layer_caches)
+        return fail(DSPARK_ERR_INVALID_ARG, "tables_update: null argument");
+    if (elem_size != 1 && elem_size != 2)
+        return fail(DSPARK_ERR_DTYPE, "tables_update: element size %zu", elem_size);
+    const int L = t->L;
+    std::vector<uintptr_t> key(3 * L + 1);
+    for (int l = 0; l < L; l++) {
+        key[l] = reinterpret_cast<uintptr_t>(layer_caches[l]);
+        key[L + l] = k_scale_ptrs ? reinterpret_cast<uintptr_t>(k_scale_ptrs[l]) : 0;
+        key[2 * L + l] = v_scale_ptrs ? reinterpret_cast<uintptr_t>(v_scale_ptrs[l]) : 0;
+    }
+    key[3 * L] = elem_size;
+    if (key == t->key)
+        return ok();  // same memory as the tables already describe
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    cudaError_t e = cudaStreamIsCapturing(stream, &cap);
+    if (e != cudaSuccess)
+        return fail(DSPARK_ERR_CUDA, "tables_update: %s", cudaGetErrorString(e));
+    if (cap != cudaStreamCaptureStatusNone)
+        return fail(DSPARK_ERR_CAPTURING, "tables_update: the caches moved while the stream is capturing");
+    std::vector<int64_t> offs(L);
+    std::vector<const float *> scales(2 * L);
+    const uintptr_t base = key[0];
+    for (int l = 0; l < L; l++) {
+        if (!key[l])
+            return fail(DSPARK_ERR_INVALID_ARG, "tables_update: layer %d cache is null", l);
+        const int64_t delta = (int64_t)(key[l] - base);
+        if (delta % (int64_t)(16 * elem_size) != 0)
+            return fail(DSPARK_ERR_ALIGNMENT, "layer caches are not 16-element aligned to each other");
+        offs[l] = delta / (int64_t)elem_size;
+        scales[l] = k_scale_ptrs ? k_scale_ptrs[l] : nullptr;
+        scales[L + l] = v_scale_ptrs ? v_scale_ptrs[l] : nullptr;
+    }
+    // Pageable host source: the call returns once the bytes are staged, so
+    // the vectors may go out of scope; the copies are ordered on `stream`.
+    e = cudaMemcpyAsync(t->d_offsets, offs.data(), sizeof(int64_t) * L, cudaMemcpyHostToDevice, stream);
+    if (e == cudaSuccess)
+        e = cudaMemcpyAsync(t->d_scales, scales.data(), sizeof(float *) * 2 * L, cudaMemcpyHostToDevice, stream);
+    if (e != cudaSuccess)
+        return fail(DSPARK_ERR_CUDA, "tables_update: %s", cudaGetErrorString(e));
+    t->key.swap(key);
+    t->builds++;
+    return ok();
+}
+
+const int64_t *dspark_ctx_kv_tables_cache_offsets(const dspark_ctx_kv_tables *t)
+{
+    return t ? t->d_offsets : nullptr;
+}
+
+const float *const *dspark_ctx_kv_tables_k_scales(const dspark_ctx_kv_tables *t)
+{
+    return t ? t->d_scales : nullptr;
+}
+
+const float *const *dspark_ctx_kv_tables_v_scales(const dspark_ctx_kv_tables *t)
+{
+    return t ? t->d_scales + t->L : nullptr;
+}
+
+int64_t dspark_ctx_kv_tables_builds(const dspark_ctx_kv_tables *t) { return t ? t->builds : 0; }
+
+void dspark_ctx_kv_tables_destroy(dspark_ctx_kv_tables *t)
+{
+    if (!t)
+        return;
+    int prev = -1;
+    bool switched = cudaGetDevice(&prev) == cudaSuccess && prev != t->device && t->device >= 0 &&
+                    cudaSetDevice(t->device) == cudaSuccess;
+    cudaFree(t->d_offsets);
+    cudaFree(t->d_scales);
+    if (switched)
+        cudaSetDevice(prev);
+    delete t;
+}
+
+}  // extern "C"

@@ -1,0 +1,81 @@
+"""The user-facing writer object, shaped like the pages' DSparkContextKVWriter.
+
+vLLM DSpark context-KV writer page: ``DSparkContextKVWriter(attn_layers)``
+validates the layers' cache layout, ``supported(attn_layers)`` reports
+whether the fused write can serve them, and calling the writer with
+``(all_kv, k_norm_weight, eps, positions, cos_sin_cache, rotary_dim,
+slot_mapping)`` stores every layer's context K/V.  Here the layers are given
+as their cache tensors and fp32 scale tensors; the layout check, the offset /
+pointer tables and the write all run in the C library.
+"""
+
+from __future__ import annotations
+
+from ._binding import (
+    HEAD_DIM, DSparkError, Tables, cache_desc, dspark_ctx_kv_rotary_dims_supported,
+    dspark_ctx_kv_validate_layers, dspark_ctx_kv_write, dspark_ctx_kv_write_ex, kv_dtype_code,
+)
+
+
+def rotary_dims_supported(rotary_dim: int, head_dim: int) -> bool:
+    """The kernel rotates the leading 16, 32 or 64 dims of a 128-dim head."""
+    return dspark_ctx_kv_rotary_dims_supported(rotary_dim, head_dim)
+
+
+class ContextKVWriter:
+    """Writes precomputed context K/V into every draft layer's paged cache.
+
+    ``kv_caches[l]``: ``[num_blocks, nkv, block_size, 256]`` bf16 (``"auto"``)
+    or uint8 (``"fp8"``); ``k_scales[l]``, ``v_scales[l]``: fp32 CUDA tensors.
+    The offset tables are rebuilt only when a cache or scale moves, and never
+    while the current stream is capturing a CUDA graph.
+    """
+
+    def __init__(self, kv_caches, k_scales, v_scales, kv_cache_dtype="auto"):
+        self.kv_caches = list(kv_caches)
+        self.k_scales = list(k_scales)
+        self.v_scales = list(v_scales)
+        self.kv_cache_dtype = kv_cache_dtype
+        dspark_ctx_kv_validate_layers(self._descs())
+        c0 = self.kv_caches[0]
+        self.num_layers = len(self.kv_caches)
+        self.num_blocks, self.num_kv_heads, self.block_size = (int(s) for s in c0.shape[:3])
+        self._dtype = kv_dtype_code(kv_cache_dtype)
+        self._tables = Tables(self.num_layers)
+
+    def _descs(self):
+        return [cache_desc(c, self.kv_cache_dtype, k, v)
+                for c, k, v in zip(self.kv_caches, self.k_scales, self.v_scales)]
+
+    @staticmethod
+    def supported(kv_caches, k_scales, v_scales, kv_cache_dtype="auto") -> bool:
+        try:
+            dspark_ctx_kv_validate_layers([cache_desc(c, kv_cache_dtype, k, v)
+                                           for c, k, v in zip(kv_caches, k_scales, v_scales)])
+        except DSparkError:
+            return False
+        return len(kv_caches) > 0
+
+    @property
+    def tables(self) -> Tables:
+        return self._tables
+
+    def ensure_tables(self, stream=None):
+        self._tables.update(self.kv_caches, self.k_scales, self.v_scales, stream)
+
+    def __call__(self, all_kv, k_norm_weight, eps, positions, cos_sin_cache, rotary_dim, slot_mapping,
+                 stream=None, error_flags=None):
+        num_ctx, L, two, nkv, hd = all_kv.shape
+        if L != self.num_layers or nkv != self.num_kv_heads or two != 2 or hd != HEAD_DIM:
+            raise DSparkError(1, f"all_kv shape {tuple(all_kv.shape)} does not match the layers")
+        if num_ctx == 0:
+            return
+        self.ensure_tables(stream)
+        t = self._tables
+        args = (all_kv, k_norm_weight, positions, slot_mapping, num_ctx, cos_sin_cache,
+                cos_sin_cache.shape[0], self.kv_caches[0], self.num_blocks, t.cache_offsets,
+                t.k_scales, t.v_scales, L, nkv, self.block_size, rotary_dim, eps, self._dtype)
+        if error_flags is None:
+            dspark_ctx_kv_write(*args, stream=stream)
+        else:
+            dspark_ctx_kv_write_ex(*args, error_flags, stream=stream)

@@ -1,0 +1,158 @@
+"""The C-ABI library without a GPU: it loads, exports every function that
+include/*.h declares, and turns each rule of the writer's layout check and
+of the call's preconditions into its status code before any CUDA call
+(vLLM DSpark context-KV writer page: _validate, __call__,
+rotary_dims_supported).  No test here launches a kernel."""
+
+import ctypes
+import glob
+import os
+import re
+
+import pytest
+
+import speculative_decoding_draft_ctx_gb300 as dk
+from speculative_decoding_draft_ctx_gb300 import build as kbuild
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    kbuild.build()
+    return dk.lib()
+
+
+def declared_functions():
+    names = set()
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        src = open(h).read()
+        src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+        for m in re.finditer(r"^[A-Za-z_][\w\s\*]*?\b(dspark_\w+)\s*\(", src, flags=re.M):
+            names.add(m.group(1))
+    return names
+
+
+def test_every_declared_symbol_is_exported(L):
+    names = declared_functions()
+    assert "dspark_ctx_kv_write" in names and len(names) >= 10
+    missing = [n for n in names if not hasattr(L, n)]
+    assert not missing
+    assert names == set(dk.EXPORTS)
+
+
+def test_library_is_the_in_tree_build(L):
+    assert os.path.dirname(os.path.abspath(L._name)) == os.path.join(ROOT, "speculative_decoding_draft_ctx_gb300")
+
+
+FAKE = 0x10000  # an aligned address that is never dereferenced: every call below fails validation
+
+
+def call(**over):
+    a = dict(all_kv=FAKE, knorm_w=FAKE, positions=FAKE, slot_mapping=FAKE, num_ctx=4, cos_sin=FAKE,
+             max_pos=64, layer0_cache=FAKE, num_blocks=4, cache_offsets=FAKE, k_scales=FAKE,
+             v_scales=FAKE, L=2, nkv=2, block_size=16, rotary_dim=32, eps=1e-6, kv_dtype=0)
+    a.update(over)
+    with pytest.raises(dk.DSparkError) as ei:
+        dk.dspark_ctx_kv_write(**a, stream=0)
+    return ei.value.name
+
+
+@pytest.mark.parametrize("r", [0, 8, 48, 96, 128, -16])
+def test_unsupported_rotary_dims(L, r):
+    assert call(rotary_dim=r) == "DSPARK_ERR_UNSUPPORTED_ROTARY_DIM"
+
+
+def test_rotary_dims_supported_rule(L):
+    for r in (16, 32, 64):
+        assert dk.rotary_dims_supported(r, 128)
+        assert not dk.rotary_dims_supported(r, 64)
+    assert not dk.rotary_dims_supported(128, 128)
+
+
+@pytest.mark.parametrize("bs", [0, 3, 12, 48, -16])
+def test_block_size_must_be_power_of_two(L, bs):
+    assert call(block_size=bs) == "DSPARK_ERR_BLOCK_SIZE"
+
+
+@pytest.mark.parametrize("over", [dict(num_ctx=-1), dict(L=0), dict(nkv=0), dict(num_blocks=0),
+                                  dict(max_pos=0), dict(eps=-1.0), dict(eps=float("nan")),
+                                  dict(eps=float("inf")), dict(all_kv=0), dict(cos_sin=0),
+                                  dict(positions=0), dict(slot_mapping=0), dict(layer0_cache=0),
+                                  dict(cache_offsets=0), dict(kv_dtype=1, k_scales=0),
+                                  dict(num_ctx=1 << 60)])
+def test_invalid_arguments(L, over):
+    assert call(**over) == "DSPARK_ERR_INVALID_ARG"
+
+
+@pytest.mark.parametrize("over", [dict(all_kv=FAKE + 8), dict(knorm_w=FAKE + 2), dict(cos_sin=FAKE + 4),
+                                  dict(layer0_cache=FAKE + 8), dict(positions=FAKE + 4),
+                                  dict(slot_mapping=FAKE + 1), dict(cache_offsets=FAKE + 4)])
+def test_misaligned_buffers(L, over):
+    assert call(**over) == "DSPARK_ERR_ALIGNMENT"
+
+
+@pytest.mark.parametrize("kv", [2, -1, 7])
+def test_unknown_kv_dtype(L, kv):
+    assert call(kv_dtype=kv) == "DSPARK_ERR_DTYPE"
+
+
+def test_zero_tokens_is_ok_without_a_device(L):
+    dk.dspark_ctx_kv_write(0, 0, 0, 0, 0, 0, 64, 0, 4, 0, 0, 0, 2, 2, 16, 32, 1e-6, 0, stream=0)
+    assert dk.dspark_ctx_kv_last_error() == ""
+
+
+def test_status_strings(L):
+    for code, name in dk.STATUS.items():
+        assert dk.dspark_ctx_kv_status_string(code) == name
+
+
+def desc(data=FAKE, shape=(8, 2, 16, 256), stride=None, elem=2, cache_dtype=0, kv=0, scales_ok=1, ndim=4):
+    d = dk.CacheDesc()
+    d.data = data
+    d.ndim = ndim
+    if stride is None:
+        stride = (shape[1] * shape[2] * shape[3], shape[2] * shape[3], shape[3], 1)
+    for i in range(4):
+        d.shape[i] = shape[i]
+        d.stride[i] = stride[i]
+    d.elem_size, d.cache_dtype, d.kv_dtype = elem, cache_dtype, kv
+    d.k_scale = d.v_scale = FAKE
+    d.scales_ok = scales_ok
+    return d
+
+
+def status_of(descs):
+    try:
+        dk.dspark_ctx_kv_validate_layers(descs)
+        return "DSPARK_OK"
+    except dk.DSparkError as e:
+        return e.name
+
+
+def test_layout_rules(L):
+    span = 8 * 2 * 16 * 256 * 2
+    assert status_of([desc(), desc(data=FAKE + span)]) == "DSPARK_OK"
+    assert status_of([desc(elem=1, cache_dtype=1, kv=1), desc(data=FAKE + span, elem=1, cache_dtype=1, kv=1)]) == "DSPARK_OK"
+    assert status_of([]) == "DSPARK_ERR_INVALID_ARG"
+    assert status_of([desc(data=0)]) == "DSPARK_ERR_INVALID_ARG"  # not bound
+    assert status_of([desc(shape=(0, 2, 16, 256))]) == "DSPARK_ERR_INVALID_ARG"
+    assert status_of([desc(shape=(8, 2, 16, 128))]) == "DSPARK_ERR_INVALID_ARG"
+    assert status_of([desc(ndim=3)]) == "DSPARK_ERR_INVALID_ARG"
+    assert status_of([desc(shape=(8, 2, 24, 256))]) == "DSPARK_ERR_BLOCK_SIZE"
+    assert status_of([desc(stride=(2 * 16 * 256, 256, 2 * 256, 1))]) == "DSPARK_ERR_INVALID_ARG"
+    assert status_of([desc(kv=1)]) == "DSPARK_ERR_DTYPE"  # fp8 cache that is not uint8
+    assert status_of([desc(elem=1, cache_dtype=1)]) == "DSPARK_ERR_DTYPE"  # bf16 kv on uint8
+    assert status_of([desc(kv=-1)]) == "DSPARK_ERR_DTYPE"
+    assert status_of([desc(scales_ok=0)]) == "DSPARK_ERR_INVALID_ARG"
+    assert status_of([desc(), desc(data=FAKE + span, shape=(4, 2, 16, 256))]) == "DSPARK_ERR_INVALID_ARG"
+    assert status_of([desc(), desc(data=FAKE + span + 16)]) == "DSPARK_ERR_ALIGNMENT"  # 8 elements off
+    assert status_of([desc(), desc(data=FAKE - span)]) == "DSPARK_OK"  # negative offset is fine
+
+
+def test_tables_reject_bad_arguments_without_device(L):
+    h = ctypes.c_void_p()
+    assert L.dspark_ctx_kv_tables_create(0, ctypes.byref(h)) == dk.STATUS_CODE["DSPARK_ERR_INVALID_ARG"]
+    assert L.dspark_ctx_kv_tables_update(None, None, 2, None, None, None) == dk.STATUS_CODE["DSPARK_ERR_INVALID_ARG"]
+    assert L.dspark_ctx_kv_tables_builds(None) == 0
+    L.dspark_ctx_kv_tables_destroy(None)

@@ -58,7 +58,31 @@ def parse_args(argv=None):
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="oracle sample budget")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--num-ctx", type=int, default=None,
+                    help="run a smaller case of the workload (profiling captures): fewer tokens")
+    ap.add_argument("--num-blocks", type=int, default=None, help="with --num-ctx: fewer cache blocks")
+    ap.add_argument("--graph", action="store_true",
+                    help="replay the timed steps from one CUDA graph (launch-bound small workloads)")
     return ap.parse_args(argv)
+
+
+def select_workload(args) -> wk.Workload:
+    """The named workload, or a smaller case of it with the same recipe."""
+    wl = wk.WORKLOADS_BY_NAME[args.config]
+    if args.num_ctx is None and args.num_blocks is None:
+        return wl
+    T = args.num_ctx or wl.num_ctx
+    over = {"num_ctx": T, "name": f"{wl.name}[num_ctx={T}"}
+    if wl.requests:
+        if T % wl.tokens_per_request:
+            raise SystemExit("--num-ctx must be a multiple of the tokens per request")
+        over["requests"] = T // wl.tokens_per_request
+    over["pad_count"] = round(wl.pad_count * T / wl.num_ctx)
+    if args.num_blocks:
+        over["num_blocks"] = args.num_blocks
+        over["name"] += f",num_blocks={args.num_blocks}"
+    over["name"] += "]"
+    return wl.with_(**over)
 
 
 # ---------------------------------------------------------------- helpers
@@ -213,7 +237,7 @@ def run_reference(args):
     ws, rank, _ = dist_env()
     if rank != 0:
         return 0
-    wl = wk.WORKLOADS_BY_NAME[args.config]
+    wl = select_workload(args)
     inp = wk.generate(wl)
     budget = 90.0  # seconds of oracle work for the whole run
     per_step = budget / max(1, args.steps + args.warmup)
@@ -258,7 +282,7 @@ def run_ours(args):
         pg = dist
     dk.lib()
 
-    wl = wk.WORKLOADS_BY_NAME[args.config]
+    wl = select_workload(args)
     base = wk.generate(wl, seed=wl.seed + 1000 * rank)
     fp8 = wl.kv_dtype == wk.KV_FP8
     nvalid = base.num_valid_tokens
@@ -291,21 +315,39 @@ def run_ours(args):
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     t_begin = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
+    graph = None
+    if args.graph:
+        # the timed steps as one graph: one launch per step, no host gaps
+        side = torch.cuda.Stream()
+        side.wait_stream(stream)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=side):
+            for i in range(args.steps):
+                step(i)
+        stream.wait_stream(side)
+        graph.replay()  # untimed warm replay
+        torch.cuda.synchronize()
     if pg:
         pg.barrier()
     torch.cuda.synchronize()
     with ClockSampler(local) as clk:
         t_begin.record(stream)
-        for i in range(args.steps):
-            starts[i].record(stream)
-            step(i)
-            ends[i].record(stream)
+        if graph is not None:
+            graph.replay()
+        else:
+            for i in range(args.steps):
+                starts[i].record(stream)
+                step(i)
+                ends[i].record(stream)
         t_end.record(stream)
         torch.cuda.synchronize()
     if pg:
         pg.barrier()
     total_ms = t_begin.elapsed_time(t_end)
-    launch_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    if graph is not None:
+        launch_ms = [total_ms / args.steps]
+    else:
+        launch_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
     if pg:
         t = torch.tensor([total_ms], device=dev)
         pg.all_reduce(t, op=pg.ReduceOp.MAX)
@@ -373,6 +415,7 @@ def run_ours(args):
             "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
             "config": dict(wk.describe(wl), parallelism=f"replicas{ws}", input_sets=n_sets,
+                           timing="one CUDA graph of all steps" if graph is not None else "CUDA events per launch",
                            l2=("inputs larger than L2" if n_sets == 1 else
                                f"{n_sets} input sets rotated, footprint > 3x L2")),
             "rows_per_s": rows_per_s,

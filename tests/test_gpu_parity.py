@@ -211,6 +211,7 @@ def test_zero_and_constant_rows(oracle_lib):
     _parity(inp)
 
 
+@pytest.mark.filterwarnings("ignore:The CUDA Graph is empty")
 def test_cuda_graph_capture_and_replay(oracle_lib):
     """The write captured in a CUDA graph replays against new input values in
     the same buffers; the tables are not rebuilt on the same key, and a moved

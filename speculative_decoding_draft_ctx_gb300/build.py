@@ -21,6 +21,7 @@ LIB_PATH = os.path.join(PKG, LIB_NAME)
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 KERNEL_SRC = os.path.join(CSRC, "ctx_kv_kernel.cu")
+TMA_SRC = os.path.join(CSRC, "ctx_kv_tma.cu")
 API_SRC = os.path.join(CSRC, "ctx_kv_api.cpp")
 HEADERS = [os.path.join(CSRC, "ctx_kv_internal.h"), os.path.join(INCLUDE, "dspark_ctx_kv.h")]
 
@@ -41,7 +42,7 @@ def _stale() -> bool:
     if not os.path.exists(LIB_PATH):
         return True
     t = os.path.getmtime(LIB_PATH)
-    return any(os.path.getmtime(s) > t for s in [KERNEL_SRC, API_SRC, *HEADERS])
+    return any(os.path.getmtime(s) > t for s in [KERNEL_SRC, TMA_SRC, API_SRC, *HEADERS])
 
 
 def _run(cmd):
@@ -59,20 +60,25 @@ def build(force: bool = False, verbose: bool = False) -> str:
         os.makedirs(BUILD_DIR, exist_ok=True)
         home = cuda_home()
         nvcc = os.path.join(home, "bin", "nvcc")
-        kobj = os.path.join(BUILD_DIR, "ctx_kv_kernel.o")
+        objs, cmds = [], []
+        for src in (KERNEL_SRC, TMA_SRC):
+            obj = os.path.join(BUILD_DIR, os.path.basename(src)[:-3] + ".o")
+            cmd = [nvcc, *ARCH, "-lineinfo", "-O3", "-std=c++17", "-Xcompiler", "-fPIC",
+                   "-I", INCLUDE, "-c", src, "-o", obj]
+            if verbose:
+                cmd.insert(1, "-Xptxas=-v")
+            objs.append(obj)
+            cmds.append(cmd)
         aobj = os.path.join(BUILD_DIR, "ctx_kv_api.o")
-        kcmd = [nvcc, *ARCH, "-lineinfo", "-O3", "-std=c++17", "-Xcompiler", "-fPIC",
-                "-I", INCLUDE, "-c", KERNEL_SRC, "-o", kobj]
+        cmds.append(["g++", "-O2", "-std=c++17", "-fPIC", "-Wall", "-I", os.path.join(home, "include"),
+                     "-I", INCLUDE, "-c", API_SRC, "-o", aobj])
+        objs.append(aobj)
+        with ThreadPoolExecutor(len(cmds)) as ex:
+            outs = list(ex.map(_run, cmds))
         if verbose:
-            kcmd.insert(1, "-Xptxas=-v")
-        acmd = ["g++", "-O2", "-std=c++17", "-fPIC", "-Wall", "-I", os.path.join(home, "include"),
-                "-I", INCLUDE, "-c", API_SRC, "-o", aobj]
-        with ThreadPoolExecutor(2) as ex:
-            outs = list(ex.map(_run, [kcmd, acmd]))
-        if verbose:
-            sys.stderr.write(outs[0])
+            sys.stderr.write(outs[0] + outs[1])
         tmp = LIB_PATH + f".tmp{os.getpid()}"
-        _run([nvcc, *ARCH, "-shared", "-o", tmp, kobj, aobj, "-lpthread", "-ldl", "-lrt"])
+        _run([nvcc, *ARCH, "-shared", "-o", tmp, *objs, "-lpthread", "-ldl", "-lrt"])
         os.replace(tmp, LIB_PATH)
         return LIB_PATH
 

@@ -38,6 +38,16 @@ int ok()
     return DSPARK_OK;
 }
 
+// Which kernel serves a call: the pipelined one where the shape allows,
+// else the generic one.  DSPARK_CTX_KV_KERNEL=generic pins the generic
+// kernel for the calls made while it is set (both compute the same result;
+// the tests run each).
+bool force_generic()
+{
+    const char *e = std::getenv("DSPARK_CTX_KV_KERNEL");
+    return e && std::strcmp(e, "generic") == 0;
+}
+
 bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
 bool pow2(int64_t v) { return v > 0 && (v & (v - 1)) == 0; }
@@ -138,7 +148,10 @@ int dspark_ctx_kv_write_ex(const void *all_kv, const void *knorm_w, const int64_
     p.num_kv_heads = nkv;
     p.block_size_log2 = log2_exact(block_size);
     p.eps = eps;
-    cudaError_t e = dspark::launch_ctx_kv_write(p, rotary_dim, kv_dtype == DSPARK_KV_FP8_E4M3, stream);
+    const bool fp8 = kv_dtype == DSPARK_KV_FP8_E4M3;
+    cudaError_t e = (!force_generic() && dspark::tma_path_supported(p))
+                        ? dspark::launch_ctx_kv_write_tma(p, rotary_dim, fp8, stream)
+                        : dspark::launch_ctx_kv_write(p, rotary_dim, fp8, stream);
     if (e != cudaSuccess)
         return fail(DSPARK_ERR_CUDA, "launch failed: %s", cudaGetErrorString(e));
     return ok();

@@ -35,7 +35,13 @@ struct CtxKvParams {
     float eps;
 };
 
-// Enqueues the write on `stream`.  Returns cudaSuccess or the launch error.
+// Generic kernel (any layer count and head count): enqueues the write on
+// `stream`.  Returns cudaSuccess or the launch error.
 cudaError_t launch_ctx_kv_write(const CtxKvParams &p, int rotary_dim, bool fp8, cudaStream_t stream);
+
+// Pipelined bulk-copy kernel: handles up to 32 layers and up to 64 KV heads
+// (one layer's K|V rows of a token fit a 32 KB stage).
+bool tma_path_supported(const CtxKvParams &p);
+cudaError_t launch_ctx_kv_write_tma(const CtxKvParams &p, int rotary_dim, bool fp8, cudaStream_t stream);
 
 }  // namespace dspark

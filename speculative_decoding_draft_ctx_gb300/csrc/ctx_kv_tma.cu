@@ -1,0 +1,585 @@
+// sm_103a pipelined kernel of the DSpark fused context-KV write (the fast
+// path; ctx_kv_kernel.cu keeps the generic one).
+//
+// Defining passage: vLLM DSpark context-KV writer page, module docstring (one
+// launch for all draft layers: Gemma RMSNorm of K in fp32 materialised to
+// bf16, partial NeoX RoPE at the token's position, K|V stored into each
+// layer's [num_blocks, nkv, block_size, 256] cache as bf16 or fp8 e4m3 of
+// x / scale, slots < 0 not written).
+//
+// Data movement.  all_kv[t, l0 : l0 + Lp] -- every K and V row of Lp layers of
+// one token -- is one contiguous block of Lp * nkv * 512 bytes.  Each CTA runs
+// a ring of shared-memory stages: a producer warp reads the slot and position
+// of its next tokens, skips padding (nothing of a padded token is read), and
+// for each valid (token, layer piece) issues one bulk asynchronous copy
+// (cp.async.bulk, completing on an mbarrier) of the block plus one of the
+// token's cos|sin row.  Eight consumer warps wait on the stage's barrier,
+// compute from shared memory and store straight to the caches, then release
+// the stage.  Bytes in flight per SM are bounded by shared memory, not by
+// registers, so the HBM queue stays full with few warps.
+//
+// Compute mapping.  A consumer warp handles 4 rows per instruction: 8 lanes
+// per row, each lane holding dims [8q, 8q+8) and [64+8q, 64+8q+8) of K and of
+// V (q = lane % 8), so every 16-byte shared load is conflict-free and every
+// 16-byte (bf16) or 8-byte (fp8) global store of a warp covers 4 whole
+// 128-byte (64-byte) segments.  Sum of squares: 16 FMAs + 3 xor shuffles
+// within the row's 8 lanes.  RoPE (only dims < 64 can rotate): the partner of
+// dim d is d +- r/2, r/16 lanes away within the row's 8 lanes.  fp8: the
+// quotient x / scale is formed from the correctly rounded reciprocal of the
+// scale with one FMA correction step (Markstein's method: q0 = x*(1/s),
+// e = x - q0*s exactly, q = q0 + e*(1/s)), which yields the correctly rounded
+// fp32 quotient, then a saturating RNE pack to e4m3 pairs.
+//
+// Every wait on an mbarrier is bounded (globaltimer); on expiry the CTA sets
+// DSPARK_FLAG_TIMEOUT, stops, waits (bounded) for its own copies in flight
+// and returns.
+#include <cuda_bf16.h>
+#include <cuda_fp8.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <mutex>
+
+#include "ctx_kv_internal.h"
+
+namespace dspark {
+namespace {
+
+constexpr int kConsumerWarps = 8;
+constexpr int kThreads = 32 * (kConsumerWarps + 1);  // last warp is the producer
+constexpr int kCsBytes = 128;                        // cos|sin row slot (r <= 64 bf16)
+constexpr unsigned kFlagSlot = 0x1u;
+constexpr unsigned kFlagPos = 0x2u;
+constexpr unsigned kFlagTimeout = 0x4u;
+constexpr unsigned long long kTimeoutNs = 4000000000ull;  // 4 s
+constexpr int kMaxTmaLayers = 32;
+
+struct StageHdr {
+    long long unit;  // < 0: end of work
+    long long slot;
+    long long pos;
+    long long pad;
+};
+
+// ------------------------------------------------------------------ PTX helpers
+
+__device__ __forceinline__ uint32_t smem_addr(const void *p)
+{
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ unsigned long long globaltimer()
+{
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count)
+{
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar)
+{
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes)
+{
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_addr(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Waits for the phase of `bar` with the given parity to complete.  Gives up
+// (and raises the CTA's abort word) after kTimeoutNs, or as soon as another
+// warp of the CTA has given up.
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volatile int *abort)
+{
+    if (mbar_try_wait(bar, parity))
+        return true;
+    const unsigned long long t0 = globaltimer();
+    while (true) {
+        if (mbar_try_wait(bar, parity))
+            return true;
+        if (*abort)
+            return false;
+        if (globaltimer() - t0 > kTimeoutNs) {
+            *abort = 1;
+            return false;
+        }
+    }
+}
+
+__device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t bytes, uint64_t *bar)
+{
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            smem_addr(dst)),
+        "l"(src), "r"(bytes), "r"(smem_addr(bar))
+        : "memory");
+}
+
+// A plain load (not asm) so the compiler may schedule the loads of a group
+// together; the mbarrier waits carry "memory" clobbers, so none moves above
+// the wait that makes its stage valid.
+__device__ __forceinline__ uint4 lds128(const void *p) { return *reinterpret_cast<const uint4 *>(p); }
+
+__device__ __forceinline__ void st_stream_v4(void *p, uint4 v)
+{
+    asm volatile("st.global.cs.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z),
+                 "r"(v.w)
+                 : "memory");
+}
+
+__device__ __forceinline__ void st_stream_v2(void *p, uint2 v)
+{
+    asm volatile("st.global.cs.v2.u32 [%0], {%1, %2};" ::"l"(p), "r"(v.x), "r"(v.y) : "memory");
+}
+
+__device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+__device__ __forceinline__ void unpack8(const uint4 &v, float *f)
+{
+    f[0] = bf_lo(v.x), f[1] = bf_hi(v.x), f[2] = bf_lo(v.y), f[3] = bf_hi(v.y);
+    f[4] = bf_lo(v.z), f[5] = bf_hi(v.z), f[6] = bf_lo(v.w), f[7] = bf_hi(v.w);
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
+{
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&v);
+}
+
+// fp32 x / s from r = RN(1/s) with one FMA correction step (Markstein's
+// method): the correctly rounded quotient whenever |x| and |x / s| lie in
+// [2^-90, 2^99] (below, the residual underflows -- quotients that small
+// encode to a signed zero in e4m3 either way).  The first product's magnitude is clamped at 2^100 (sign kept, NaN
+// kept) so that an overflowing x * r cannot turn into inf - inf = NaN; such
+// quotients saturate in e4m3 either way.  The residual is formed as q0*s - x
+// so that a zero quotient keeps the sign of x.  With the saturating e4m3
+// pack, the stored code always equals the code of the IEEE quotient.
+__device__ __forceinline__ float quotient(float x, float s, float r)
+{
+    float q0 = x * r;
+    asm("min.NaN.xorsign.abs.f32 %0, %0, %1;" : "+f"(q0) : "f"(0x1p100f));
+    const float e = fmaf(q0, s, -x);
+    return fmaf(-e, r, q0);
+}
+
+__device__ __forceinline__ uint32_t e4m3x4(float a, float b, float c, float d)
+{
+    const uint32_t lo = __nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3);
+    const uint32_t hi = __nv_cvt_float2_to_fp8x2(make_float2(c, d), __NV_SATFINITE, __NV_E4M3);
+    return lo | (hi << 16);
+}
+
+__device__ __forceinline__ uint2 quantise8(const float *f, float s, float r)
+{
+    float q[8];
+#pragma unroll
+    for (int j = 0; j < 8; j++)
+        q[j] = quotient(f[j], s, r);
+    return make_uint2(e4m3x4(q[0], q[1], q[2], q[3]), e4m3x4(q[4], q[5], q[6], q[7]));
+}
+
+// Shared-memory layout (dynamic): barriers and headers, per-layer tables,
+// then the stages (128-byte aligned).
+struct Layout {
+    uint32_t full, empty, hdr, abort, w1, off, scl, stages, stage_bytes, slab_bytes, total;
+};
+
+__host__ __device__ inline uint32_t align_up(uint32_t v, uint32_t a) { return (v + a - 1) / a * a; }
+
+__host__ __device__ inline Layout make_layout(int L, int S, uint32_t slab_bytes)
+{
+    Layout y;
+    uint32_t o = 0;
+    y.full = o;
+    o += 8 * S;
+    y.empty = o;
+    o += 8 * S;
+    y.hdr = align_up(o, 16);
+    o = y.hdr + sizeof(StageHdr) * S;
+    y.abort = o;
+    o += 16;
+    y.w1 = align_up(o, 16);
+    o = y.w1 + 4 * kHeadDim * L;
+    y.off = align_up(o, 8);
+    o = y.off + 8 * L;
+    y.scl = o;  // k scale, v scale, 1/k, 1/v: 4 floats per layer
+    o += 16 * L;
+    y.stages = align_up(o, 128);
+    y.slab_bytes = slab_bytes;
+    y.stage_bytes = align_up(slab_bytes + kCsBytes, 128);
+    y.total = y.stages + y.stage_bytes * S;
+    return y;
+}
+
+struct TmaParams {
+    CtxKvParams p;
+    int32_t layers_per_piece;  // Lp
+    int32_t pieces;            // ceil(L / Lp)
+    int32_t stages;            // S
+    uint64_t h_magic;          // ceil(2^32 / nkv): row / nkv = (row * h_magic) >> 32 for row < 2^16
+};
+
+template <int ROT, bool FP8>
+__global__ void __launch_bounds__(kThreads, 2) ctx_kv_tma_kernel(const TmaParams tp)
+{
+    extern __shared__ __align__(128) unsigned char smem[];
+    const CtxKvParams &p = tp.p;
+    const int L = p.num_layers, H = p.num_kv_heads, S = tp.stages, NP = tp.pieces, Lp = tp.layers_per_piece;
+    const Layout lay = make_layout(L, S, (uint32_t)Lp * H * 512u);
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + lay.full);
+    uint64_t *empty = reinterpret_cast<uint64_t *>(smem + lay.empty);
+    StageHdr *hdr = reinterpret_cast<StageHdr *>(smem + lay.hdr);
+    volatile int *abort = reinterpret_cast<volatile int *>(smem + lay.abort);
+    float *w1 = reinterpret_cast<float *>(smem + lay.w1);
+    long long *off = reinterpret_cast<long long *>(smem + lay.off);
+    float *scl = reinterpret_cast<float *>(smem + lay.scl);
+    unsigned char *stages = smem + lay.stages;
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    if (tid == 0) {
+        for (int s = 0; s < S; s++) {
+            mbar_init(full + s, 1);
+            mbar_init(empty + s, kConsumerWarps);
+        }
+        *abort = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    // per-layer tables: (1 + w) in fp32, cache offsets, scales and their reciprocals
+    for (int i = tid; i < L * kHeadDim; i += kThreads)
+        w1[i] = 1.0f + __uint_as_float((uint32_t)__ldg(p.knorm_w + i) << 16);
+    for (int l = tid; l < L; l += kThreads) {
+        off[l] = __ldg(p.cache_offsets + l);
+        float ks = 1.0f, vs = 1.0f;
+        if (FP8) {
+            ks = __ldg(reinterpret_cast<const float *>(
+                __ldg(reinterpret_cast<const unsigned long long *>(p.k_scales) + l)));
+            vs = __ldg(reinterpret_cast<const float *>(
+                __ldg(reinterpret_cast<const unsigned long long *>(p.v_scales) + l)));
+        }
+        scl[4 * l + 0] = ks;
+        scl[4 * l + 1] = vs;
+        scl[4 * l + 2] = __frcp_rn(ks);
+        scl[4 * l + 3] = __frcp_rn(vs);
+    }
+    __syncthreads();
+
+    const long long units = p.num_ctx * (long long)NP;
+    const long long G = gridDim.x;
+    unsigned flags = 0;
+
+    if (warp == kConsumerWarps) {
+        // ---------------------------------------------------------- producer
+        uint32_t k = 0;  // stages issued so far (the sentinel excluded)
+        bool ok = true;
+        for (long long base = blockIdx.x; base < units && ok; base += 32 * G) {
+            const long long my_u = base + (long long)lane * G;
+            long long my_slot = -1, my_pos = 0;
+            if (my_u < units) {
+                const long long t = NP == 1 ? my_u : my_u / NP;
+                my_slot = __ldg(p.slot_mapping + t);
+                if (my_slot >= 0) {
+                    my_pos = __ldg(p.positions + t);
+                    const bool first_piece = NP == 1 || my_u % NP == 0;
+                    if (my_slot >= p.capacity) {
+                        if (first_piece)
+                            flags |= kFlagSlot;
+                        my_slot = -1;
+                    } else if (my_pos < 0 || my_pos >= p.max_pos) {
+                        if (first_piece)
+                            flags |= kFlagPos;
+                        my_slot = -1;
+                    }
+                }
+            }
+            for (int i = 0; i < 32; i++) {
+                const long long u = base + (long long)i * G;
+                if (u >= units)
+                    break;
+                const long long slot = __shfl_sync(0xffffffffu, my_slot, i);
+                const long long pos = __shfl_sync(0xffffffffu, my_pos, i);
+                if (slot < 0)
+                    continue;  // padding (or out of range): nothing read, nothing written
+                if (lane == 0) {
+                    const int s = (int)(k % S);
+                    ok = mbar_wait(empty + s, ((k / S) & 1u) ^ 1u, abort);
+                    if (ok) {
+                        const long long t = NP == 1 ? u : u / NP;
+                        const int piece = NP == 1 ? 0 : (int)(u - t * NP);
+                        const int l0 = piece * Lp;
+                        const int lc = min(Lp, L - l0);
+                        const uint32_t slab = (uint32_t)lc * H * 512u;
+                        hdr[s].unit = u;
+                        hdr[s].slot = slot;
+                        hdr[s].pos = pos;
+                        unsigned char *dst = stages + (size_t)s * lay.stage_bytes;
+                        mbar_arrive_expect_tx(full + s, slab + 2u * ROT);
+                        bulk_g2s(dst, p.all_kv + (t * L + l0) * 2LL * H * kHeadDim, slab, full + s);
+                        bulk_g2s(dst + lay.slab_bytes, p.cos_sin + pos * ROT, 2u * ROT, full + s);
+                    }
+                }
+                ok = __shfl_sync(0xffffffffu, ok, 0);
+                if (!ok)
+                    break;
+                k++;
+            }
+        }
+        uint32_t rounds = k;  // barrier rounds used, the sentinel included
+        if (lane == 0) {
+            if (ok) {
+                const int s = (int)(k % S);
+                if (mbar_wait(empty + s, ((k / S) & 1u) ^ 1u, abort)) {
+                    hdr[s].unit = -1;
+                    mbar_arrive(full + s);
+                    rounds = k + 1;
+                }
+            }
+            if (*abort)
+                flags |= kFlagTimeout;
+        }
+        __syncwarp();
+        __syncthreads();
+        // drain: every copy this CTA issued has landed before the CTA exits.
+        // Only the last S rounds can be pending, and a round whose stage was
+        // reused since has completed (its barrier moved on).
+        if (lane == 0) {
+            const uint32_t first = rounds > (uint32_t)S ? rounds - S : 0;
+            for (uint32_t j = first; j < k; j++) {
+                const int s = (int)(j % S);
+                const unsigned long long t0 = globaltimer();
+                while (!mbar_try_wait(full + s, (j / S) & 1u) && globaltimer() - t0 < kTimeoutNs) {
+                }
+            }
+        }
+    } else {
+        // ---------------------------------------------------------- consumers
+        const int q = lane & 7;      // 8-dim chunk of the row's first and second half
+        const int rr = lane >> 3;    // row of the 4-row group
+        constexpr int kPartner = ROT / 16;
+        constexpr int kRotLanes = ROT / 8;
+        const bool rot_lane = q < kRotLanes;
+        const float sgn = (q & kPartner) ? 1.0f : -1.0f;
+        const long long bs = 1LL << p.block_size_log2;
+        const long long bs_mask = bs - 1;
+        long long gctr = 0;  // row groups seen so far, over all stages
+        for (uint32_t k = 0;; k++) {
+            const int s = (int)(k % S);
+            if (!mbar_wait(full + s, (k / S) & 1u, abort))
+                break;
+            const long long u = hdr[s].unit;
+            if (u < 0)
+                break;
+            const long long slot = hdr[s].slot;
+            const long long t = NP == 1 ? u : u / NP;
+            const int l0 = (NP == 1 ? 0 : (int)(u - t * NP)) * Lp;
+            const int lc = min(Lp, L - l0);
+            const int R = lc * H;
+            const int ngroups = (R + 3) >> 2;
+            const unsigned char *stage = stages + (size_t)s * lay.stage_bytes;
+
+            float c[8], sn[8];
+            if (rot_lane) {
+                const unsigned char *cs = stage + lay.slab_bytes + 16 * (q & (kPartner - 1));
+                unpack8(lds128(cs), c);
+                unpack8(lds128(cs + ROT), sn);  // sin half starts r/2 elements = r bytes later
+            } else {
+#pragma unroll
+                for (int j = 0; j < 8; j++)
+                    c[j] = sn[j] = 0.0f;
+            }
+            const long long row_base = (slot >> p.block_size_log2) * H;
+            const long long row_off = slot & bs_mask;
+
+            long long g = gctr + ((warp - gctr % kConsumerWarps) + kConsumerWarps) % kConsumerWarps;
+            for (; g < gctr + ngroups; g += kConsumerWarps) {
+                const int r = (int)(g - gctr) * 4 + rr;
+                const bool active = r < R;
+                const int rc = active ? r : R - 1;
+                const int lr = (int)(((uint64_t)(uint32_t)rc * tp.h_magic) >> 32);
+                const int h = rc - lr * H;
+                const int l = l0 + lr;
+                const unsigned char *krow = stage + ((size_t)(2 * lr) * H + h) * 256;
+                const unsigned char *vrow = krow + (size_t)H * 256;
+                const uint4 ka = lds128(krow + 16 * q), kb = lds128(krow + 128 + 16 * q);
+                const uint4 va = lds128(vrow + 16 * q), vb = lds128(vrow + 128 + 16 * q);
+                float x[16];
+                unpack8(ka, x);
+                unpack8(kb, x + 8);
+                float ss = 0.0f;
+#pragma unroll
+                for (int j = 0; j < 16; j++)
+                    ss = fmaf(x[j], x[j], ss);
+                ss += __shfl_xor_sync(0xffffffffu, ss, 4);
+                ss += __shfl_xor_sync(0xffffffffu, ss, 2);
+                ss += __shfl_xor_sync(0xffffffffu, ss, 1);
+                const float inv = rsqrtf(fmaf(ss, 1.0f / kHeadDim, p.eps));
+                const float *wl = w1 + l * kHeadDim;
+                const float4 wa0 = *reinterpret_cast<const float4 *>(wl + 8 * q);
+                const float4 wa1 = *reinterpret_cast<const float4 *>(wl + 8 * q + 4);
+                const float4 wb0 = *reinterpret_cast<const float4 *>(wl + 64 + 8 * q);
+                const float4 wb1 = *reinterpret_cast<const float4 *>(wl + 64 + 8 * q + 4);
+                const float wv[16] = {wa0.x, wa0.y, wa0.z, wa0.w, wa1.x, wa1.y, wa1.z, wa1.w,
+                                      wb0.x, wb0.y, wb0.z, wb0.w, wb1.x, wb1.y, wb1.z, wb1.w};
+                uint32_t y[8];
+#pragma unroll
+                for (int j = 0; j < 8; j++)
+                    y[j] = pack_bf16x2((x[2 * j] * inv) * wv[2 * j], (x[2 * j + 1] * inv) * wv[2 * j + 1]);
+                // RoPE on the first chunk (dims 8q .. 8q+7); the partner is kPartner lanes away
+                uint32_t ko[4];
+#pragma unroll
+                for (int j = 0; j < 4; j++) {
+                    const uint32_t yp = __shfl_xor_sync(0xffffffffu, y[j], kPartner);
+                    const float a0 = fmaf(bf_lo(y[j]), c[2 * j], sgn * (bf_lo(yp) * sn[2 * j]));
+                    const float a1 = fmaf(bf_hi(y[j]), c[2 * j + 1], sgn * (bf_hi(yp) * sn[2 * j + 1]));
+                    ko[j] = rot_lane ? pack_bf16x2(a0, a1) : y[j];
+                }
+                if (!active)
+                    continue;
+                const long long dst_row = (row_base + h) * bs + row_off;
+                const long long elem = off[l] + dst_row * 256;
+                if (!FP8) {
+                    unsigned char *d = p.cache0 + elem * 2;
+                    st_stream_v4(d + 16 * q, make_uint4(ko[0], ko[1], ko[2], ko[3]));
+                    st_stream_v4(d + 128 + 16 * q, make_uint4(y[4], y[5], y[6], y[7]));
+                    st_stream_v4(d + 256 + 16 * q, va);
+                    st_stream_v4(d + 384 + 16 * q, vb);
+                } else {
+                    const float ks = scl[4 * l], vs = scl[4 * l + 1], rk = scl[4 * l + 2], rv = scl[4 * l + 3];
+                    unsigned char *d = p.cache0 + elem;
+                    float f[8];
+                    unpack8(make_uint4(ko[0], ko[1], ko[2], ko[3]), f);
+                    st_stream_v2(d + 8 * q, quantise8(f, ks, rk));
+                    unpack8(make_uint4(y[4], y[5], y[6], y[7]), f);
+                    st_stream_v2(d + 64 + 8 * q, quantise8(f, ks, rk));
+                    unpack8(va, f);
+                    st_stream_v2(d + 128 + 8 * q, quantise8(f, vs, rv));
+                    unpack8(vb, f);
+                    st_stream_v2(d + 192 + 8 * q, quantise8(f, vs, rv));
+                }
+            }
+            gctr += ngroups;
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(empty + s);
+        }
+        __syncwarp();
+        __syncthreads();
+    }
+    flags = __reduce_or_sync(0xffffffffu, flags);
+    if (lane == 0 && flags && p.error_flags)
+        atomicOr(p.error_flags, flags);
+}
+
+constexpr int kMaxSlabBytes = 32 * 1024;
+constexpr int kStageBudget = 100 * 1024;  // per CTA, two CTAs per SM
+constexpr int kMaxStages = 16;
+
+struct Plan {
+    int Lp, NP, S;
+    Layout lay;
+};
+
+bool plan_for(const CtxKvParams &p, Plan &pl)
+{
+    const int L = p.num_layers, H = p.num_kv_heads;
+    const int row_bytes = H * 512;
+    if (row_bytes > kMaxSlabBytes || L > kMaxTmaLayers)
+        return false;
+    pl.Lp = std::min(L, kMaxSlabBytes / row_bytes);
+    pl.NP = (L + pl.Lp - 1) / pl.Lp;
+    const Layout one = make_layout(L, 1, (uint32_t)pl.Lp * row_bytes);
+    const int fixed = (int)one.stages;
+    int S = (kStageBudget - fixed) / (int)one.stage_bytes;
+    S = S < 2 ? 2 : (S > kMaxStages ? kMaxStages : S);
+    pl.S = S;
+    pl.lay = make_layout(L, S, (uint32_t)pl.Lp * row_bytes);
+    return pl.lay.total <= 113 * 1024;
+}
+
+template <int ROT, bool FP8>
+cudaError_t launch_tma_variant(const TmaParams &tp, uint32_t smem_bytes, cudaStream_t stream)
+{
+    static std::mutex mu;
+    static int sms_cache[64];
+    static uint32_t smem_set[64];
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return e;
+    if (dev < 0 || dev >= 64)
+        return cudaErrorInvalidDevice;
+    int sms;
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        if (sms_cache[dev] == 0) {
+            e = cudaDeviceGetAttribute(&sms_cache[dev], cudaDevAttrMultiProcessorCount, dev);
+            if (e != cudaSuccess)
+                return e;
+        }
+        if (smem_set[dev] < smem_bytes) {
+            e = cudaFuncSetAttribute(ctx_kv_tma_kernel<ROT, FP8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     (int)smem_bytes);
+            if (e != cudaSuccess)
+                return e;
+            smem_set[dev] = smem_bytes;
+        }
+        sms = sms_cache[dev];
+    }
+    const long long units = tp.p.num_ctx * (long long)tp.pieces;
+    const long long want = 2LL * sms;
+    const int blocks = (int)(units < want ? units : want);
+    ctx_kv_tma_kernel<ROT, FP8><<<blocks, kThreads, smem_bytes, stream>>>(tp);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+bool tma_path_supported(const CtxKvParams &p)
+{
+    Plan pl;
+    return plan_for(p, pl);
+}
+
+cudaError_t launch_ctx_kv_write_tma(const CtxKvParams &p, int rotary_dim, bool fp8, cudaStream_t stream)
+{
+    Plan pl;
+    if (!plan_for(p, pl))
+        return cudaErrorInvalidValue;
+    TmaParams tp;
+    tp.p = p;
+    tp.layers_per_piece = pl.Lp;
+    tp.pieces = pl.NP;
+    tp.stages = pl.S;
+    tp.h_magic = (0x100000000ull + p.num_kv_heads - 1) / (uint64_t)p.num_kv_heads;
+    const uint32_t smem = pl.lay.total;
+    switch (rotary_dim) {
+    case 16:
+        return fp8 ? launch_tma_variant<16, true>(tp, smem, stream) : launch_tma_variant<16, false>(tp, smem, stream);
+    case 32:
+        return fp8 ? launch_tma_variant<32, true>(tp, smem, stream) : launch_tma_variant<32, false>(tp, smem, stream);
+    case 64:
+        return fp8 ? launch_tma_variant<64, true>(tp, smem, stream) : launch_tma_variant<64, false>(tp, smem, stream);
+    default:
+        return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace dspark

@@ -20,6 +20,17 @@ from parity import (alt_index_rows, compare_caches, compare_rows, device_inputs,
 pytestmark = pytest.mark.gpu
 
 
+@pytest.fixture(params=["pipelined", "generic"])
+def kernel(request, monkeypatch):
+    """Run the test on the pipelined bulk-copy kernel (the default where the
+    shape allows) and on the generic kernel."""
+    if request.param == "generic":
+        monkeypatch.setenv("DSPARK_CTX_KV_KERNEL", "generic")
+    else:
+        monkeypatch.delenv("DSPARK_CTX_KV_KERNEL", raising=False)
+    return request.param
+
+
 def _parity(inp):
     wl = inp.workload
     fp8 = wl.kv_dtype == wk.KV_FP8
@@ -31,7 +42,7 @@ def _parity(inp):
 
 
 @pytest.mark.parametrize("idx", [0, 1, 2], ids=["tiny", "draft_step", "draft_step_fp8"])
-def test_parity_small_workloads(oracle_lib, idx):
+def test_parity_small_workloads(oracle_lib, kernel, idx):
     _parity(wk.generate(wk.WORKLOADS[idx]))
 
 
@@ -45,11 +56,15 @@ RAGGED = [
     (333, 1, 2, 64, 32, 16, wk.KV_FP8, 0),
     (1000, 2, 4, 16, 16, 80, wk.KV_BF16, 100),
     (257, 4, 8, 64, 64, 8, wk.KV_FP8, 1),
+    (50, 3, 64, 32, 16, 8, wk.KV_FP8, 5),     # one layer per stage: three pieces per token
+    (20, 2, 40, 64, 4, 16, wk.KV_BF16, 2),   # 20 KB per layer: one layer per stage
+    (30, 33, 2, 16, 16, 4, wk.KV_BF16, 0),   # more layers than the pipelined kernel stages
+    (9, 1, 65, 16, 8, 2, wk.KV_FP8, 1),      # a layer larger than a stage
 ]
 
 
 @pytest.mark.parametrize("T,L,H,r,bs,nb,kv,pad", RAGGED)
-def test_parity_ragged_shapes(oracle_lib, T, L, H, r, bs, nb, kv, pad):
+def test_parity_ragged_shapes(oracle_lib, kernel, T, L, H, r, bs, nb, kv, pad):
     wl = wk.Workload(name="ragged", num_ctx=T, num_layers=L, num_kv_heads=H, rotary_dim=r,
                      block_size=bs, num_blocks=nb, max_pos=3000, rope_theta=1e4, kv_dtype=kv,
                      pad_count=pad, kv_std=2.0 if kv == wk.KV_FP8 else 1.0,
@@ -57,7 +72,7 @@ def test_parity_ragged_shapes(oracle_lib, T, L, H, r, bs, nb, kv, pad):
     _parity(wk.generate(wl))
 
 
-def test_parity_prefill_full_size(oracle_lib):
+def test_parity_prefill_full_size(oracle_lib, kernel):
     """Prefill batch (8192 tokens, fp8, r=32, bs=64): every written row."""
     wl = wk.WORKLOADS[3]
     inp = wk.generate(wl)
@@ -121,6 +136,21 @@ def _check_rows(inp, caches, row_ids):
     assert changed == nvalid * H * L
 
 
+def test_fp8_v_codes_are_bit_exact(oracle_lib, kernel):
+    """Beyond the 1-code tolerance: every fp8 V code equals the oracle's,
+    i.e. the kernels' x / scale is the correctly rounded fp32 quotient and
+    the pack rounds to nearest even with saturation, like the oracle."""
+    wl = wk.WORKLOADS[2]
+    inp = wk.generate(wl)
+    caches, _, _ = gpu_write(inp)
+    g = to_numpy_caches(caches, True)
+    _, o, _ = oracle_full(inp)
+    for l in range(wl.num_layers):
+        gl, ol = g[l].reshape(-1, 256), o[l].reshape(-1, 256)
+        wr = ~(ol == 0xFF).all(axis=1)
+        assert np.array_equal(gl[wr, 128:], ol[wr, 128:])
+
+
 def test_zero_tokens_launches_nothing_and_writes_nothing(oracle_lib):
     import speculative_decoding_draft_ctx_gb300 as dk
 
@@ -141,7 +171,7 @@ def test_all_padding_writes_nothing(oracle_lib):
         assert bool((c.view(torch.uint8) == 0xFF).all())
 
 
-def test_out_of_range_rows_are_skipped_and_flagged(oracle_lib):
+def test_out_of_range_rows_are_skipped_and_flagged(oracle_lib, kernel):
     """Rows with a slot beyond the cache or a position beyond the cos|sin
     table are not written and set their bit in the error word; a padded
     token's position is never looked at; every other row is still exact."""
@@ -174,7 +204,7 @@ def test_out_of_range_rows_are_skipped_and_flagged(oracle_lib):
     assert int(flags.item()) == 0
 
 
-def test_layer_caches_in_one_buffer_with_negative_offsets(oracle_lib):
+def test_layer_caches_in_one_buffer_with_negative_offsets(oracle_lib, kernel):
     """Layers carved from one allocation in reverse order: layer l > 0 lies
     before layer 0, so its element offset is negative."""
     import speculative_decoding_draft_ctx_gb300 as dk
@@ -198,7 +228,7 @@ def test_layer_caches_in_one_buffer_with_negative_offsets(oracle_lib):
     assert dk.STATUS_CODE["DSPARK_OK"] == 0
 
 
-def test_zero_and_constant_rows(oracle_lib):
+def test_zero_and_constant_rows(oracle_lib, kernel):
     """Degenerate K rows: all zero (normed to zero), constant (normed to
     1 + w), one-hot; and a token at position 0 (RoPE is the identity)."""
     wl = wk.WORKLOADS[1].with_(num_ctx=32, pad_count=0, num_layers=2)

@@ -22,7 +22,7 @@
 // per row, each lane holding dims [8q, 8q+8) and [64+8q, 64+8q+8) of K and of
 // V (q = lane % 8), so every 16-byte shared load is conflict-free and every
 // 16-byte (bf16) or 8-byte (fp8) global store of a warp covers 4 whole
-// 128-byte (64-byte) segments.  Sum of squares: 16 FMAs + 3 xor shuffles
+// 128-byte (64-byte) segments.  Sum of squares: 8 paired FMAs + 3 xor shuffles
 // within the row's 8 lanes.  RoPE (only dims < 64 can rotate): the partner of
 // dim d is d +- r/2, r/16 lanes away within the row's 8 lanes.  fp8: the
 // quotient x / scale is formed from the correctly rounded reciprocal of the
@@ -150,51 +150,93 @@ __device__ __forceinline__ void st_stream_v2(void *p, uint2 v)
     asm volatile("st.global.cs.v2.u32 [%0], {%1, %2};" ::"l"(p), "r"(v.x), "r"(v.y) : "memory");
 }
 
-__device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
-__device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
-
-__device__ __forceinline__ void unpack8(const uint4 &v, float *f)
-{
-    f[0] = bf_lo(v.x), f[1] = bf_hi(v.x), f[2] = bf_lo(v.y), f[3] = bf_hi(v.y);
-    f[4] = bf_lo(v.z), f[5] = bf_hi(v.z), f[6] = bf_lo(v.w), f[7] = bf_hi(v.w);
-}
-
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
 {
     __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<uint32_t *>(&v);
 }
 
-// fp32 x / s from r = RN(1/s) with one FMA correction step (Markstein's
-// method): the correctly rounded quotient whenever |x| and |x / s| lie in
-// [2^-90, 2^99] (below, the residual underflows -- quotients that small
-// encode to a signed zero in e4m3 either way).  The first product's magnitude is clamped at 2^100 (sign kept, NaN
-// kept) so that an overflowing x * r cannot turn into inf - inf = NaN; such
-// quotients saturate in e4m3 either way.  The residual is formed as q0*s - x
-// so that a zero quotient keeps the sign of x.  With the saturating e4m3
-// pack, the stored code always equals the code of the IEEE quotient.
-__device__ __forceinline__ float quotient(float x, float s, float r)
+// ------------------------------------------------------------------ packed fp32 pairs
+// Blackwell's paired fp32 FMA / multiply / add (fma.rn.f32x2 and friends)
+// process two values per instruction; a pair lives in a 64-bit register.
+
+__device__ __forceinline__ uint64_t pr(float lo, float hi)
 {
-    float q0 = x * r;
-    asm("min.NaN.xorsign.abs.f32 %0, %0, %1;" : "+f"(q0) : "f"(0x1p100f));
-    const float e = fmaf(q0, s, -x);
-    return fmaf(-e, r, q0);
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
 }
 
-__device__ __forceinline__ uint32_t e4m3x4(float a, float b, float c, float d)
+__device__ __forceinline__ void unpr(uint64_t v, float &lo, float &hi)
 {
-    const uint32_t lo = __nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3);
-    const uint32_t hi = __nv_cvt_float2_to_fp8x2(make_float2(c, d), __NV_SATFINITE, __NV_E4M3);
-    return lo | (hi << 16);
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
 }
 
-__device__ __forceinline__ uint2 quantise8(const float *f, float s, float r)
+__device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c)
 {
-    float q[8];
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+
+__device__ __forceinline__ uint64_t mul2(uint64_t a, uint64_t b)
+{
+    uint64_t d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+
+__device__ __forceinline__ uint64_t add2(uint64_t a, uint64_t b)
+{
+    uint64_t d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+
+// bf16 pair (element 2j in the low half) -> fp32 pair, exactly
+__device__ __forceinline__ uint64_t bf2_to_f2(uint32_t w) { return pr(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u)); }
+
+// fp32 pair -> bf16 pair, round to nearest even
+__device__ __forceinline__ uint32_t f2_to_bf2(uint64_t v)
+{
+    float lo, hi;
+    unpr(v, lo, hi);
+    return pack_bf16x2(lo, hi);
+}
+
+// |w| clamped to the bf16 pair `bound` per half, sign and NaN kept
+__device__ __forceinline__ uint32_t clamp_bf2(uint32_t w, uint32_t bound)
+{
+    uint32_t d;
+    asm("min.NaN.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(w), "r"(bound));
+    return d;
+}
+
+// e4m3 codes of x / s for the 8 bf16 values in `v` (two 4-code words).
+// x is first clamped in magnitude to `bound` (a bf16 value >= 448 s, just
+// above 512 s: every clamped quotient still saturates, and x * n cannot
+// overflow).  With n = -RN(1/s), Markstein's FMA correction
+//   p0 = x n,  e = p0 s + x (exact),  p = p0 + e n
+// gives p = -RN(x / s) whenever |x| and |x / s| are at least 2^-90 (below,
+// the residual underflows, and such quotients encode to a signed zero either
+// way).  The saturating RNE pack of p, with every sign bit flipped, is the
+// code of the IEEE quotient x / s; NaN inputs come out as the NaN code 0xFF.
+__device__ __forceinline__ uint2 quantise8(const uint4 &v, uint32_t bound, uint64_t s2, uint64_t n2)
+{
+    const uint32_t w[4] = {clamp_bf2(v.x, bound), clamp_bf2(v.y, bound), clamp_bf2(v.z, bound),
+                           clamp_bf2(v.w, bound)};
+    uint32_t half[4];
 #pragma unroll
-    for (int j = 0; j < 8; j++)
-        q[j] = quotient(f[j], s, r);
-    return make_uint2(e4m3x4(q[0], q[1], q[2], q[3]), e4m3x4(q[4], q[5], q[6], q[7]));
+    for (int j = 0; j < 4; j++) {
+        const uint64_t x = bf2_to_f2(w[j]);
+        const uint64_t p0 = mul2(x, n2);
+        const uint64_t e = fma2(p0, s2, x);
+        const uint64_t p = fma2(e, n2, p0);
+        float lo, hi;
+        unpr(p, lo, hi);
+        half[j] = __nv_cvt_float2_to_fp8x2(make_float2(lo, hi), __NV_SATFINITE, __NV_E4M3);
+    }
+    return make_uint2((half[0] | (half[1] << 16)) ^ 0x80808080u, (half[2] | (half[3] << 16)) ^ 0x80808080u);
 }
 
 // Shared-memory layout (dynamic): barriers and headers, per-layer tables,
@@ -218,11 +260,11 @@ __host__ __device__ inline Layout make_layout(int L, int S, uint32_t slab_bytes)
     y.abort = o;
     o += 16;
     y.w1 = align_up(o, 16);
-    o = y.w1 + 4 * kHeadDim * L;
+    o = y.w1 + 4 * kHeadDim * L;  // 32 float4 slots per layer
     y.off = align_up(o, 8);
     o = y.off + 8 * L;
-    y.scl = o;  // k scale, v scale, 1/k, 1/v: 4 floats per layer
-    o += 16 * L;
+    y.scl = align_up(o, 16);  // per layer: k scale, v scale, -1/k, -1/v, k bound, v bound (8 words)
+    o = y.scl + 32 * L;
     y.stages = align_up(o, 128);
     y.slab_bytes = slab_bytes;
     y.stage_bytes = align_up(slab_bytes + kCsBytes, 128);
@@ -238,6 +280,11 @@ struct TmaParams {
     uint64_t h_magic;          // ceil(2^32 / nkv): row / nkv = (row * h_magic) >> 32 for row < 2^16
 };
 
+// w1 table: float4 slot of (layer l, half jj of an 8-dim chunk, chunk c of
+// the 16 chunks): lane q reads slots c = q (dims 8q..) and c = 8 + q (dims
+// 64 + 8q..), so the 8 lanes of a row read 128 contiguous bytes per load.
+__device__ __forceinline__ int w1_slot(int l, int jj, int c) { return l * 32 + jj * 16 + c; }
+
 template <int ROT, bool FP8>
 __global__ void __launch_bounds__(kThreads, 2) ctx_kv_tma_kernel(const TmaParams tp)
 {
@@ -249,9 +296,9 @@ __global__ void __launch_bounds__(kThreads, 2) ctx_kv_tma_kernel(const TmaParams
     uint64_t *empty = reinterpret_cast<uint64_t *>(smem + lay.empty);
     StageHdr *hdr = reinterpret_cast<StageHdr *>(smem + lay.hdr);
     volatile int *abort = reinterpret_cast<volatile int *>(smem + lay.abort);
-    float *w1 = reinterpret_cast<float *>(smem + lay.w1);
+    float4 *w1 = reinterpret_cast<float4 *>(smem + lay.w1);
     long long *off = reinterpret_cast<long long *>(smem + lay.off);
-    float *scl = reinterpret_cast<float *>(smem + lay.scl);
+    uint32_t *scl = reinterpret_cast<uint32_t *>(smem + lay.scl);
     unsigned char *stages = smem + lay.stages;
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -263,23 +310,6 @@ __global__ void __launch_bounds__(kThreads, 2) ctx_kv_tma_kernel(const TmaParams
         *abort = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
-    // per-layer tables: (1 + w) in fp32, cache offsets, scales and their reciprocals
-    for (int i = tid; i < L * kHeadDim; i += kThreads)
-        w1[i] = 1.0f + __uint_as_float((uint32_t)__ldg(p.knorm_w + i) << 16);
-    for (int l = tid; l < L; l += kThreads) {
-        off[l] = __ldg(p.cache_offsets + l);
-        float ks = 1.0f, vs = 1.0f;
-        if (FP8) {
-            ks = __ldg(reinterpret_cast<const float *>(
-                __ldg(reinterpret_cast<const unsigned long long *>(p.k_scales) + l)));
-            vs = __ldg(reinterpret_cast<const float *>(
-                __ldg(reinterpret_cast<const unsigned long long *>(p.v_scales) + l)));
-        }
-        scl[4 * l + 0] = ks;
-        scl[4 * l + 1] = vs;
-        scl[4 * l + 2] = __frcp_rn(ks);
-        scl[4 * l + 3] = __frcp_rn(vs);
-    }
     __syncthreads();
 
     const long long units = p.num_ctx * (long long)NP;
@@ -288,34 +318,49 @@ __global__ void __launch_bounds__(kThreads, 2) ctx_kv_tma_kernel(const TmaParams
 
     if (warp == kConsumerWarps) {
         // ---------------------------------------------------------- producer
+        // Starts at once: the consumers build their tables meanwhile.  Slots
+        // and positions of the next 32 units are fetched one batch ahead.
+        auto fetch = [&](long long base, long long &slot, long long &pos) {
+            const long long u = base + (long long)lane * G;
+            slot = -1;
+            pos = 0;
+            if (u < units) {
+                const long long t = NP == 1 ? u : u / NP;
+                slot = __ldg(p.slot_mapping + t);
+                pos = __ldg(p.positions + t);
+            }
+        };
+        auto vet = [&](long long base, long long &slot, long long pos) {
+            if (slot < 0)
+                return;
+            const long long u = base + (long long)lane * G;
+            const bool first_piece = NP == 1 || u % NP == 0;
+            if (slot >= p.capacity) {
+                if (first_piece)
+                    flags |= kFlagSlot;
+                slot = -1;
+            } else if (pos < 0 || pos >= p.max_pos) {
+                if (first_piece)
+                    flags |= kFlagPos;
+                slot = -1;
+            }
+        };
         uint32_t k = 0;  // stages issued so far (the sentinel excluded)
         bool ok = true;
-        for (long long base = blockIdx.x; base < units && ok; base += 32 * G) {
-            const long long my_u = base + (long long)lane * G;
-            long long my_slot = -1, my_pos = 0;
-            if (my_u < units) {
-                const long long t = NP == 1 ? my_u : my_u / NP;
-                my_slot = __ldg(p.slot_mapping + t);
-                if (my_slot >= 0) {
-                    my_pos = __ldg(p.positions + t);
-                    const bool first_piece = NP == 1 || my_u % NP == 0;
-                    if (my_slot >= p.capacity) {
-                        if (first_piece)
-                            flags |= kFlagSlot;
-                        my_slot = -1;
-                    } else if (my_pos < 0 || my_pos >= p.max_pos) {
-                        if (first_piece)
-                            flags |= kFlagPos;
-                        my_slot = -1;
-                    }
-                }
-            }
+        long long cur_slot, cur_pos, nxt_slot = -1, nxt_pos = 0;
+        long long base = blockIdx.x;
+        fetch(base, cur_slot, cur_pos);
+        for (; base < units && ok; base += 32 * G) {
+            const long long nbase = base + 32 * G;
+            if (nbase < units)
+                fetch(nbase, nxt_slot, nxt_pos);
+            vet(base, cur_slot, cur_pos);
             for (int i = 0; i < 32; i++) {
                 const long long u = base + (long long)i * G;
                 if (u >= units)
                     break;
-                const long long slot = __shfl_sync(0xffffffffu, my_slot, i);
-                const long long pos = __shfl_sync(0xffffffffu, my_pos, i);
+                const long long slot = __shfl_sync(0xffffffffu, cur_slot, i);
+                const long long pos = __shfl_sync(0xffffffffu, cur_pos, i);
                 if (slot < 0)
                     continue;  // padding (or out of range): nothing read, nothing written
                 if (lane == 0) {
@@ -341,6 +386,8 @@ __global__ void __launch_bounds__(kThreads, 2) ctx_kv_tma_kernel(const TmaParams
                     break;
                 k++;
             }
+            cur_slot = nxt_slot;
+            cur_pos = nxt_pos;
         }
         uint32_t rounds = k;  // barrier rounds used, the sentinel included
         if (lane == 0) {
@@ -371,12 +418,44 @@ __global__ void __launch_bounds__(kThreads, 2) ctx_kv_tma_kernel(const TmaParams
         }
     } else {
         // ---------------------------------------------------------- consumers
+        // per-layer tables: (1 + w) in fp32, cache offsets, scale constants
+        for (int i = tid; i < L * kHeadDim; i += 32 * kConsumerWarps) {
+            const int l = i / kHeadDim, d = i % kHeadDim;
+            const int c = d / 8, j = d % 8;  // chunk c holds dims 8c .. 8c+7
+            reinterpret_cast<float *>(w1)[w1_slot(l, j / 4, c) * 4 + (j % 4)] =
+                1.0f + __uint_as_float((uint32_t)__ldg(p.knorm_w + i) << 16);
+        }
+        for (int l = tid; l < L; l += 32 * kConsumerWarps) {
+            off[l] = __ldg(p.cache_offsets + l);
+            float ks = 1.0f, vs = 1.0f;
+            if (FP8) {
+                ks = __ldg(reinterpret_cast<const float *>(
+                    __ldg(reinterpret_cast<const unsigned long long *>(p.k_scales) + l)));
+                vs = __ldg(reinterpret_cast<const float *>(
+                    __ldg(reinterpret_cast<const unsigned long long *>(p.v_scales) + l)));
+            }
+            // bound: the smallest bf16 >= 512 s, as a bf16 pair
+            auto bound = [](float sc) {
+                uint32_t u = __float_as_uint(512.0f * sc);
+                if (u & 0xffffu)
+                    u = (u & 0xffff0000u) + 0x10000u;
+                return (u >> 16) * 0x10001u;
+            };
+            scl[8 * l + 0] = __float_as_uint(ks);
+            scl[8 * l + 1] = __float_as_uint(vs);
+            scl[8 * l + 2] = __float_as_uint(-__frcp_rn(ks));
+            scl[8 * l + 3] = __float_as_uint(-__frcp_rn(vs));
+            scl[8 * l + 4] = bound(ks);
+            scl[8 * l + 5] = bound(vs);
+        }
+        asm volatile("bar.sync 1, %0;" ::"n"(32 * kConsumerWarps) : "memory");
+
         const int q = lane & 7;      // 8-dim chunk of the row's first and second half
         const int rr = lane >> 3;    // row of the 4-row group
         constexpr int kPartner = ROT / 16;
         constexpr int kRotLanes = ROT / 8;
         const bool rot_lane = q < kRotLanes;
-        const float sgn = (q & kPartner) ? 1.0f : -1.0f;
+        const float sgn = (q & kPartner) ? 1.0f : -1.0f;  // upper half adds, lower subtracts
         const long long bs = 1LL << p.block_size_log2;
         const long long bs_mask = bs - 1;
         long long gctr = 0;  // row groups seen so far, over all stages
@@ -394,85 +473,99 @@ __global__ void __launch_bounds__(kThreads, 2) ctx_kv_tma_kernel(const TmaParams
             const int R = lc * H;
             const int ngroups = (R + 3) >> 2;
             const unsigned char *stage = stages + (size_t)s * lay.stage_bytes;
-
-            float c[8], sn[8];
-            if (rot_lane) {
-                const unsigned char *cs = stage + lay.slab_bytes + 16 * (q & (kPartner - 1));
-                unpack8(lds128(cs), c);
-                unpack8(lds128(cs + ROT), sn);  // sin half starts r/2 elements = r bytes later
-            } else {
-#pragma unroll
-                for (int j = 0; j < 8; j++)
-                    c[j] = sn[j] = 0.0f;
-            }
             const long long row_base = (slot >> p.block_size_log2) * H;
             const long long row_off = slot & bs_mask;
 
             long long g = gctr + ((warp - gctr % kConsumerWarps) + kConsumerWarps) % kConsumerWarps;
-            for (; g < gctr + ngroups; g += kConsumerWarps) {
-                const int r = (int)(g - gctr) * 4 + rr;
-                const bool active = r < R;
-                const int rc = active ? r : R - 1;
-                const int lr = (int)(((uint64_t)(uint32_t)rc * tp.h_magic) >> 32);
-                const int h = rc - lr * H;
-                const int l = l0 + lr;
-                const unsigned char *krow = stage + ((size_t)(2 * lr) * H + h) * 256;
-                const unsigned char *vrow = krow + (size_t)H * 256;
-                const uint4 ka = lds128(krow + 16 * q), kb = lds128(krow + 128 + 16 * q);
-                const uint4 va = lds128(vrow + 16 * q), vb = lds128(vrow + 128 + 16 * q);
-                float x[16];
-                unpack8(ka, x);
-                unpack8(kb, x + 8);
-                float ss = 0.0f;
+            if (g < gctr + ngroups) {
+                // cos and sign * sin pairs of this token for the lane's 8 dims
+                uint64_t c2[4], sn2[4];
+                if (rot_lane) {
+                    const unsigned char *cs = stage + lay.slab_bytes + 16 * (q & (kPartner - 1));
+                    const uint4 cw = lds128(cs), sw = lds128(cs + ROT);  // sin half: r/2 elements later
+                    const uint32_t cwa[4] = {cw.x, cw.y, cw.z, cw.w}, swa[4] = {sw.x, sw.y, sw.z, sw.w};
+                    const uint64_t sg2 = pr(sgn, sgn);
 #pragma unroll
-                for (int j = 0; j < 16; j++)
-                    ss = fmaf(x[j], x[j], ss);
-                ss += __shfl_xor_sync(0xffffffffu, ss, 4);
-                ss += __shfl_xor_sync(0xffffffffu, ss, 2);
-                ss += __shfl_xor_sync(0xffffffffu, ss, 1);
-                const float inv = rsqrtf(fmaf(ss, 1.0f / kHeadDim, p.eps));
-                const float *wl = w1 + l * kHeadDim;
-                const float4 wa0 = *reinterpret_cast<const float4 *>(wl + 8 * q);
-                const float4 wa1 = *reinterpret_cast<const float4 *>(wl + 8 * q + 4);
-                const float4 wb0 = *reinterpret_cast<const float4 *>(wl + 64 + 8 * q);
-                const float4 wb1 = *reinterpret_cast<const float4 *>(wl + 64 + 8 * q + 4);
-                const float wv[16] = {wa0.x, wa0.y, wa0.z, wa0.w, wa1.x, wa1.y, wa1.z, wa1.w,
-                                      wb0.x, wb0.y, wb0.z, wb0.w, wb1.x, wb1.y, wb1.z, wb1.w};
-                uint32_t y[8];
-#pragma unroll
-                for (int j = 0; j < 8; j++)
-                    y[j] = pack_bf16x2((x[2 * j] * inv) * wv[2 * j], (x[2 * j + 1] * inv) * wv[2 * j + 1]);
-                // RoPE on the first chunk (dims 8q .. 8q+7); the partner is kPartner lanes away
-                uint32_t ko[4];
-#pragma unroll
-                for (int j = 0; j < 4; j++) {
-                    const uint32_t yp = __shfl_xor_sync(0xffffffffu, y[j], kPartner);
-                    const float a0 = fmaf(bf_lo(y[j]), c[2 * j], sgn * (bf_lo(yp) * sn[2 * j]));
-                    const float a1 = fmaf(bf_hi(y[j]), c[2 * j + 1], sgn * (bf_hi(yp) * sn[2 * j + 1]));
-                    ko[j] = rot_lane ? pack_bf16x2(a0, a1) : y[j];
-                }
-                if (!active)
-                    continue;
-                const long long dst_row = (row_base + h) * bs + row_off;
-                const long long elem = off[l] + dst_row * 256;
-                if (!FP8) {
-                    unsigned char *d = p.cache0 + elem * 2;
-                    st_stream_v4(d + 16 * q, make_uint4(ko[0], ko[1], ko[2], ko[3]));
-                    st_stream_v4(d + 128 + 16 * q, make_uint4(y[4], y[5], y[6], y[7]));
-                    st_stream_v4(d + 256 + 16 * q, va);
-                    st_stream_v4(d + 384 + 16 * q, vb);
+                    for (int j = 0; j < 4; j++) {
+                        c2[j] = bf2_to_f2(cwa[j]);
+                        sn2[j] = mul2(bf2_to_f2(swa[j]), sg2);
+                    }
                 } else {
-                    const float ks = scl[4 * l], vs = scl[4 * l + 1], rk = scl[4 * l + 2], rv = scl[4 * l + 3];
-                    unsigned char *d = p.cache0 + elem;
-                    float f[8];
-                    unpack8(make_uint4(ko[0], ko[1], ko[2], ko[3]), f);
-                    st_stream_v2(d + 8 * q, quantise8(f, ks, rk));
-                    unpack8(make_uint4(y[4], y[5], y[6], y[7]), f);
-                    st_stream_v2(d + 64 + 8 * q, quantise8(f, ks, rk));
-                    unpack8(va, f);
-                    st_stream_v2(d + 128 + 8 * q, quantise8(f, vs, rv));
-                    unpack8(vb, f);
-                    st_stream_v2(d + 192 + 8 * q, quantise8(f, vs, rv));
+#pragma unroll
+                    for (int j = 0; j < 4; j++)
+                        c2[j] = sn2[j] = 0;
+                }
+                for (; g < gctr + ngroups; g += kConsumerWarps) {
+                    const int r = (int)(g - gctr) * 4 + rr;
+                    const bool active = r < R;
+                    const int rc = active ? r : R - 1;
+                    const int lr = (int)(((uint64_t)(uint32_t)rc * tp.h_magic) >> 32);
+                    const int h = rc - lr * H;
+                    const int l = l0 + lr;
+                    const unsigned char *krow = stage + ((size_t)(2 * lr) * H + h) * 256;
+                    const unsigned char *vrow = krow + (size_t)H * 256;
+                    const uint4 ka = lds128(krow + 16 * q), kb = lds128(krow + 128 + 16 * q);
+                    const uint4 va = lds128(vrow + 16 * q), vb = lds128(vrow + 128 + 16 * q);
+                    const uint32_t kw[8] = {ka.x, ka.y, ka.z, ka.w, kb.x, kb.y, kb.z, kb.w};
+                    uint64_t x2[8];
+#pragma unroll
+                    for (int j = 0; j < 8; j++)
+                        x2[j] = bf2_to_f2(kw[j]);
+                    // sum of squares: two accumulator chains of packed FMAs
+                    uint64_t a0 = mul2(x2[0], x2[0]), a1 = mul2(x2[1], x2[1]);
+#pragma unroll
+                    for (int j = 2; j < 8; j += 2) {
+                        a0 = fma2(x2[j], x2[j], a0);
+                        a1 = fma2(x2[j + 1], x2[j + 1], a1);
+                    }
+                    float slo, shi;
+                    unpr(add2(a0, a1), slo, shi);
+                    float ss = slo + shi;
+                    ss += __shfl_xor_sync(0xffffffffu, ss, 4);
+                    ss += __shfl_xor_sync(0xffffffffu, ss, 2);
+                    ss += __shfl_xor_sync(0xffffffffu, ss, 1);
+                    const float inv = rsqrtf(fmaf(ss, 1.0f / kHeadDim, p.eps));
+                    const uint64_t inv2 = pr(inv, inv);
+                    const float4 wa0 = w1[w1_slot(l, 0, q)], wa1 = w1[w1_slot(l, 1, q)];
+                    const float4 wb0 = w1[w1_slot(l, 0, 8 + q)], wb1 = w1[w1_slot(l, 1, 8 + q)];
+                    const uint64_t w2[8] = {pr(wa0.x, wa0.y), pr(wa0.z, wa0.w), pr(wa1.x, wa1.y), pr(wa1.z, wa1.w),
+                                            pr(wb0.x, wb0.y), pr(wb0.z, wb0.w), pr(wb1.x, wb1.y), pr(wb1.z, wb1.w)};
+                    // y = bf16((k * inv) * (1 + w))
+                    uint32_t y[8];
+#pragma unroll
+                    for (int j = 0; j < 8; j++)
+                        y[j] = f2_to_bf2(mul2(mul2(x2[j], inv2), w2[j]));
+                    // RoPE on the first chunk (dims 8q .. 8q+7); the partner is kPartner lanes away
+                    uint32_t ko[4];
+#pragma unroll
+                    for (int j = 0; j < 4; j++) {
+                        const uint32_t yp = __shfl_xor_sync(0xffffffffu, y[j], kPartner);
+                        const uint64_t rot = fma2(bf2_to_f2(y[j]), c2[j], mul2(bf2_to_f2(yp), sn2[j]));
+                        ko[j] = rot_lane ? f2_to_bf2(rot) : y[j];
+                    }
+                    if (!active)
+                        continue;
+                    const long long dst_row = (row_base + h) * bs + row_off;
+                    const long long elem = off[l] + dst_row * 256;
+                    if (!FP8) {
+                        unsigned char *d = p.cache0 + elem * 2;
+                        st_stream_v4(d + 16 * q, make_uint4(ko[0], ko[1], ko[2], ko[3]));
+                        st_stream_v4(d + 128 + 16 * q, make_uint4(y[4], y[5], y[6], y[7]));
+                        st_stream_v4(d + 256 + 16 * q, va);
+                        st_stream_v4(d + 384 + 16 * q, vb);
+                    } else {
+                        const uint4 c4 = *reinterpret_cast<const uint4 *>(scl + 8 * l);
+                        const uint2 b2 = *reinterpret_cast<const uint2 *>(scl + 8 * l + 4);
+                        const uint64_t ks2 = pr(__uint_as_float(c4.x), __uint_as_float(c4.x));
+                        const uint64_t vs2 = pr(__uint_as_float(c4.y), __uint_as_float(c4.y));
+                        const uint64_t kn2 = pr(__uint_as_float(c4.z), __uint_as_float(c4.z));
+                        const uint64_t vn2 = pr(__uint_as_float(c4.w), __uint_as_float(c4.w));
+                        unsigned char *d = p.cache0 + elem;
+                        st_stream_v2(d + 8 * q, quantise8(make_uint4(ko[0], ko[1], ko[2], ko[3]), b2.x, ks2, kn2));
+                        st_stream_v2(d + 64 + 8 * q, quantise8(make_uint4(y[4], y[5], y[6], y[7]), b2.x, ks2, kn2));
+                        st_stream_v2(d + 128 + 8 * q, quantise8(va, b2.y, vs2, vn2));
+                        st_stream_v2(d + 192 + 8 * q, quantise8(vb, b2.y, vs2, vn2));
+                    }
                 }
             }
             gctr += ngroups;

@@ -54,11 +54,11 @@ constexpr unsigned kFlagTimeout = 0x4u;
 constexpr unsigned long long kTimeoutNs = 4000000000ull;  // 4 s
 constexpr int kMaxTmaLayers = 32;
 
+// What the producer tells the consumers about a stage.
 struct StageHdr {
-    long long unit;  // < 0: end of work
-    long long slot;
-    long long pos;
-    long long pad;
+    long long dst;  // byte offset of the token's row for head 0 within a layer's cache
+    int l0;         // first layer in the stage
+    int rows;       // rows in the stage (layers * nkv); < 0: end of work
 };
 
 // ------------------------------------------------------------------ PTX helpers
@@ -91,15 +91,20 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t by
                  : "memory");
 }
 
+// One poll of a barrier phase.  A waiting warp is suspended by the hardware
+// (up to kSuspendNs) until the phase completes, so waiting warps do not take
+// issue slots from the warps that compute.
+constexpr uint32_t kSuspendNs = 200000;
+
 __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity)
 {
     uint32_t ok;
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
         "selp.u32 %0, 1, 0, p;\n\t}"
         : "=r"(ok)
-        : "r"(smem_addr(bar)), "r"(parity)
+        : "r"(smem_addr(bar)), "r"(parity), "n"(kSuspendNs)
         : "memory");
     return ok != 0;
 }
@@ -124,13 +129,30 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volati
     }
 }
 
-__device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t bytes, uint64_t *bar)
+// Bulk copy global -> shared, completing on `bar`; `policy` is an L2 cache
+// policy (evict-first for data read exactly once).
+__device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t bytes, uint64_t *bar,
+                                         uint64_t policy)
 {
     asm volatile(
-        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::"r"(
             smem_addr(dst)),
-        "l"(src), "r"(bytes), "r"(smem_addr(bar))
+        "l"(src), "r"(bytes), "r"(smem_addr(bar)), "l"(policy)
         : "memory");
+}
+
+__device__ __forceinline__ uint64_t evict_first_policy()
+{
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+
+__device__ __forceinline__ uint64_t evict_last_policy()
+{
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
 }
 
 // A plain load (not asm) so the compiler may schedule the loads of a group
@@ -193,6 +215,25 @@ __device__ __forceinline__ uint64_t add2(uint64_t a, uint64_t b)
     return d;
 }
 
+// RoPE on a bf16 pair: for each half, y * c + yp * sn with a single rounding
+// (the product yp * sn of two bf16 values is exact in fp32, formed as an FMA
+// with -0 so that a zero product keeps its sign).  The operands stay bf16:
+// the mixed-precision fma.rn.f32.bf16 reads register halves directly.
+__device__ __forceinline__ uint64_t rope_bf2(uint32_t y, uint32_t c, uint32_t yp, uint32_t sn)
+{
+    float lo, hi;
+    asm("{\n\t.reg .b16 y0, y1, c0, c1, p0, p1, s0, s1;\n\t.reg .f32 t0, t1;\n\t"
+        "mov.b32 {y0, y1}, %2;\n\tmov.b32 {c0, c1}, %3;\n\t"
+        "mov.b32 {p0, p1}, %4;\n\tmov.b32 {s0, s1}, %5;\n\t"
+        "fma.rn.f32.bf16 t0, p0, s0, 0f80000000;\n\t"
+        "fma.rn.f32.bf16 t1, p1, s1, 0f80000000;\n\t"
+        "fma.rn.f32.bf16 %0, y0, c0, t0;\n\t"
+        "fma.rn.f32.bf16 %1, y1, c1, t1;\n\t}"
+        : "=f"(lo), "=f"(hi)
+        : "r"(y), "r"(c), "r"(yp), "r"(sn));
+    return pr(lo, hi);
+}
+
 // bf16 pair (element 2j in the low half) -> fp32 pair, exactly
 __device__ __forceinline__ uint64_t bf2_to_f2(uint32_t w) { return pr(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u)); }
 
@@ -221,22 +262,36 @@ __device__ __forceinline__ uint32_t clamp_bf2(uint32_t w, uint32_t bound)
 // the residual underflows, and such quotients encode to a signed zero either
 // way).  The saturating RNE pack of p, with every sign bit flipped, is the
 // code of the IEEE quotient x / s; NaN inputs come out as the NaN code 0xFF.
+// Four e4m3 codes in one word, element order a b c d from the low byte up,
+// RNE with saturation, every sign bit flipped.
+__device__ __forceinline__ uint32_t neg_e4m3x4(uint64_t ab, uint64_t cd)
+{
+    float a, b, c, d;
+    unpr(ab, a, b);
+    unpr(cd, c, d);
+    uint32_t w;
+    asm("{\n\t.reg .b16 lo, hi;\n\t"
+        "cvt.rn.satfinite.e4m3x2.f32 lo, %2, %1;\n\t"
+        "cvt.rn.satfinite.e4m3x2.f32 hi, %4, %3;\n\t"
+        "mov.b32 %0, {lo, hi};\n\t}"
+        : "=r"(w)
+        : "f"(a), "f"(b), "f"(c), "f"(d));
+    return w ^ 0x80808080u;
+}
+
 __device__ __forceinline__ uint2 quantise8(const uint4 &v, uint32_t bound, uint64_t s2, uint64_t n2)
 {
     const uint32_t w[4] = {clamp_bf2(v.x, bound), clamp_bf2(v.y, bound), clamp_bf2(v.z, bound),
                            clamp_bf2(v.w, bound)};
-    uint32_t half[4];
+    uint64_t p[4];
 #pragma unroll
     for (int j = 0; j < 4; j++) {
         const uint64_t x = bf2_to_f2(w[j]);
         const uint64_t p0 = mul2(x, n2);
         const uint64_t e = fma2(p0, s2, x);
-        const uint64_t p = fma2(e, n2, p0);
-        float lo, hi;
-        unpr(p, lo, hi);
-        half[j] = __nv_cvt_float2_to_fp8x2(make_float2(lo, hi), __NV_SATFINITE, __NV_E4M3);
+        p[j] = fma2(e, n2, p0);
     }
-    return make_uint2((half[0] | (half[1] << 16)) ^ 0x80808080u, (half[2] | (half[3] << 16)) ^ 0x80808080u);
+    return make_uint2(neg_e4m3x4(p[0], p[1]), neg_e4m3x4(p[2], p[3]));
 }
 
 // Shared-memory layout (dynamic): barriers and headers, per-layer tables,
@@ -261,10 +316,10 @@ __host__ __device__ inline Layout make_layout(int L, int S, uint32_t slab_bytes)
     o += 16;
     y.w1 = align_up(o, 16);
     o = y.w1 + 4 * kHeadDim * L;  // 32 float4 slots per layer
-    y.off = align_up(o, 8);
+    y.off = align_up(o, 8);  // per layer: its cache's base address
     o = y.off + 8 * L;
-    y.scl = align_up(o, 16);  // per layer: k scale, v scale, -1/k, -1/v, k bound, v bound (8 words)
-    o = y.scl + 32 * L;
+    y.scl = align_up(o, 16);  // per layer, 48 bytes: (k, k), (v, v), (-1/k, -1/k), (-1/v, -1/v), k bound, v bound
+    o = y.scl + 48 * L;
     y.stages = align_up(o, 128);
     y.slab_bytes = slab_bytes;
     y.stage_bytes = align_up(slab_bytes + kCsBytes, 128);
@@ -278,6 +333,7 @@ struct TmaParams {
     int32_t pieces;            // ceil(L / Lp)
     int32_t stages;            // S
     uint64_t h_magic;          // ceil(2^32 / nkv): row / nkv = (row * h_magic) >> 32 for row < 2^16
+    int32_t contiguous;        // 1: each CTA takes one contiguous run of units; 0: grid stride
 };
 
 // w1 table: float4 slot of (layer l, half jj of an 8-dim chunk, chunk c of
@@ -297,7 +353,7 @@ __global__ void __launch_bounds__(kThreads, 2) ctx_kv_tma_kernel(const TmaParams
     StageHdr *hdr = reinterpret_cast<StageHdr *>(smem + lay.hdr);
     volatile int *abort = reinterpret_cast<volatile int *>(smem + lay.abort);
     float4 *w1 = reinterpret_cast<float4 *>(smem + lay.w1);
-    long long *off = reinterpret_cast<long long *>(smem + lay.off);
+    unsigned char **layer_base = reinterpret_cast<unsigned char **>(smem + lay.off);
     uint32_t *scl = reinterpret_cast<uint32_t *>(smem + lay.scl);
     unsigned char *stages = smem + lay.stages;
 
@@ -320,11 +376,24 @@ __global__ void __launch_bounds__(kThreads, 2) ctx_kv_tma_kernel(const TmaParams
         // ---------------------------------------------------------- producer
         // Starts at once: the consumers build their tables meanwhile.  Slots
         // and positions of the next 32 units are fetched one batch ahead.
+        // This CTA's units: u_first, u_first + step, ... below u_end (grid
+        // stride, or one contiguous run per CTA).
+        long long u_first, u_end, step;
+        if (tp.contiguous) {
+            const long long per = (units + G - 1) / G;
+            u_first = blockIdx.x * per;
+            u_end = min(units, u_first + per);
+            step = 1;
+        } else {
+            u_first = blockIdx.x;
+            u_end = units;
+            step = G;
+        }
         auto fetch = [&](long long base, long long &slot, long long &pos) {
-            const long long u = base + (long long)lane * G;
+            const long long u = base + (long long)lane * step;
             slot = -1;
             pos = 0;
-            if (u < units) {
+            if (u < u_end) {
                 const long long t = NP == 1 ? u : u / NP;
                 slot = __ldg(p.slot_mapping + t);
                 pos = __ldg(p.positions + t);
@@ -333,7 +402,7 @@ __global__ void __launch_bounds__(kThreads, 2) ctx_kv_tma_kernel(const TmaParams
         auto vet = [&](long long base, long long &slot, long long pos) {
             if (slot < 0)
                 return;
-            const long long u = base + (long long)lane * G;
+            const long long u = base + (long long)lane * step;
             const bool first_piece = NP == 1 || u % NP == 0;
             if (slot >= p.capacity) {
                 if (first_piece)
@@ -345,46 +414,56 @@ __global__ void __launch_bounds__(kThreads, 2) ctx_kv_tma_kernel(const TmaParams
                 slot = -1;
             }
         };
+        const uint64_t stream_once = evict_first_policy();  // all_kv: read exactly once
+        const uint64_t keep = evict_last_policy();          // cos|sin rows: shared by many tokens
         uint32_t k = 0;  // stages issued so far (the sentinel excluded)
+        int ps = 0;          // ring slot of round k
+        uint32_t pph = 0;    // phase parity of round k in that slot
         bool ok = true;
         long long cur_slot, cur_pos, nxt_slot = -1, nxt_pos = 0;
-        long long base = blockIdx.x;
+        long long base = u_first;
         fetch(base, cur_slot, cur_pos);
-        for (; base < units && ok; base += 32 * G) {
-            const long long nbase = base + 32 * G;
-            if (nbase < units)
+        for (; base < u_end && ok; base += 32 * step) {
+            const long long nbase = base + 32 * step;
+            if (nbase < u_end)
                 fetch(nbase, nxt_slot, nxt_pos);
             vet(base, cur_slot, cur_pos);
             for (int i = 0; i < 32; i++) {
-                const long long u = base + (long long)i * G;
-                if (u >= units)
+                const long long u = base + (long long)i * step;
+                if (u >= u_end)
                     break;
                 const long long slot = __shfl_sync(0xffffffffu, cur_slot, i);
                 const long long pos = __shfl_sync(0xffffffffu, cur_pos, i);
                 if (slot < 0)
                     continue;  // padding (or out of range): nothing read, nothing written
                 if (lane == 0) {
-                    const int s = (int)(k % S);
-                    ok = mbar_wait(empty + s, ((k / S) & 1u) ^ 1u, abort);
+                    const int s = ps;
+                    ok = mbar_wait(empty + s, pph ^ 1u, abort);
                     if (ok) {
                         const long long t = NP == 1 ? u : u / NP;
                         const int piece = NP == 1 ? 0 : (int)(u - t * NP);
                         const int l0 = piece * Lp;
                         const int lc = min(Lp, L - l0);
                         const uint32_t slab = (uint32_t)lc * H * 512u;
-                        hdr[s].unit = u;
-                        hdr[s].slot = slot;
-                        hdr[s].pos = pos;
+                        hdr[s].dst = (((slot >> p.block_size_log2) * H << p.block_size_log2) +
+                                      (slot & ((1LL << p.block_size_log2) - 1))) *
+                                     (FP8 ? kRowElems : 2 * kRowElems);
+                        hdr[s].l0 = l0;
+                        hdr[s].rows = lc * H;
                         unsigned char *dst = stages + (size_t)s * lay.stage_bytes;
                         mbar_arrive_expect_tx(full + s, slab + 2u * ROT);
-                        bulk_g2s(dst, p.all_kv + (t * L + l0) * 2LL * H * kHeadDim, slab, full + s);
-                        bulk_g2s(dst + lay.slab_bytes, p.cos_sin + pos * ROT, 2u * ROT, full + s);
+                        bulk_g2s(dst, p.all_kv + (t * L + l0) * 2LL * H * kHeadDim, slab, full + s, stream_once);
+                        bulk_g2s(dst + lay.slab_bytes, p.cos_sin + pos * ROT, 2u * ROT, full + s, keep);
                     }
                 }
                 ok = __shfl_sync(0xffffffffu, ok, 0);
                 if (!ok)
                     break;
                 k++;
+                if (++ps == S) {
+                    ps = 0;
+                    pph ^= 1u;
+                }
             }
             cur_slot = nxt_slot;
             cur_pos = nxt_pos;
@@ -392,9 +471,9 @@ __global__ void __launch_bounds__(kThreads, 2) ctx_kv_tma_kernel(const TmaParams
         uint32_t rounds = k;  // barrier rounds used, the sentinel included
         if (lane == 0) {
             if (ok) {
-                const int s = (int)(k % S);
-                if (mbar_wait(empty + s, ((k / S) & 1u) ^ 1u, abort)) {
-                    hdr[s].unit = -1;
+                const int s = ps;
+                if (mbar_wait(empty + s, pph ^ 1u, abort)) {
+                    hdr[s].rows = -1;
                     mbar_arrive(full + s);
                     rounds = k + 1;
                 }
@@ -426,7 +505,7 @@ __global__ void __launch_bounds__(kThreads, 2) ctx_kv_tma_kernel(const TmaParams
                 1.0f + __uint_as_float((uint32_t)__ldg(p.knorm_w + i) << 16);
         }
         for (int l = tid; l < L; l += 32 * kConsumerWarps) {
-            off[l] = __ldg(p.cache_offsets + l);
+            layer_base[l] = p.cache0 + __ldg(p.cache_offsets + l) * (FP8 ? 1 : 2);
             float ks = 1.0f, vs = 1.0f;
             if (FP8) {
                 ks = __ldg(reinterpret_cast<const float *>(
@@ -441,12 +520,14 @@ __global__ void __launch_bounds__(kThreads, 2) ctx_kv_tma_kernel(const TmaParams
                     u = (u & 0xffff0000u) + 0x10000u;
                 return (u >> 16) * 0x10001u;
             };
-            scl[8 * l + 0] = __float_as_uint(ks);
-            scl[8 * l + 1] = __float_as_uint(vs);
-            scl[8 * l + 2] = __float_as_uint(-__frcp_rn(ks));
-            scl[8 * l + 3] = __float_as_uint(-__frcp_rn(vs));
-            scl[8 * l + 4] = bound(ks);
-            scl[8 * l + 5] = bound(vs);
+            const float kn = -__frcp_rn(ks), vn = -__frcp_rn(vs);
+            uint32_t *e = scl + 12 * l;
+            e[0] = e[1] = __float_as_uint(ks);
+            e[2] = e[3] = __float_as_uint(vs);
+            e[4] = e[5] = __float_as_uint(kn);
+            e[6] = e[7] = __float_as_uint(vn);
+            e[8] = bound(ks);
+            e[9] = bound(vs);
         }
         asm volatile("bar.sync 1, %0;" ::"n"(32 * kConsumerWarps) : "memory");
 
@@ -455,53 +536,39 @@ __global__ void __launch_bounds__(kThreads, 2) ctx_kv_tma_kernel(const TmaParams
         constexpr int kPartner = ROT / 16;
         constexpr int kRotLanes = ROT / 8;
         const bool rot_lane = q < kRotLanes;
-        const float sgn = (q & kPartner) ? 1.0f : -1.0f;  // upper half adds, lower subtracts
-        const long long bs = 1LL << p.block_size_log2;
-        const long long bs_mask = bs - 1;
-        long long gctr = 0;  // row groups seen so far, over all stages
-        for (uint32_t k = 0;; k++) {
-            const int s = (int)(k % S);
-            if (!mbar_wait(full + s, (k / S) & 1u, abort))
+        // bytes between the rows of consecutive heads in a cache
+        const long long head_bytes = (long long)(FP8 ? kRowElems : 2 * kRowElems) << p.block_size_log2;
+        int gmod = 0;  // row groups seen so far, over all stages, modulo the consumer warps
+        int s = 0;          // ring slot of the current round
+        uint32_t ph = 0;    // its phase parity
+        for (;; s = (s + 1 == S) ? 0 : s + 1, ph ^= (s == 0)) {
+            if (!mbar_wait(full + s, ph, abort))
                 break;
-            const long long u = hdr[s].unit;
-            if (u < 0)
+            const StageHdr h_s = hdr[s];
+            const int R = h_s.rows;
+            if (R < 0)
                 break;
-            const long long slot = hdr[s].slot;
-            const long long t = NP == 1 ? u : u / NP;
-            const int l0 = (NP == 1 ? 0 : (int)(u - t * NP)) * Lp;
-            const int lc = min(Lp, L - l0);
-            const int R = lc * H;
             const int ngroups = (R + 3) >> 2;
-            const unsigned char *stage = stages + (size_t)s * lay.stage_bytes;
-            const long long row_base = (slot >> p.block_size_log2) * H;
-            const long long row_off = slot & bs_mask;
-
-            long long g = gctr + ((warp - gctr % kConsumerWarps) + kConsumerWarps) % kConsumerWarps;
-            if (g < gctr + ngroups) {
-                // cos and sign * sin pairs of this token for the lane's 8 dims
-                uint64_t c2[4], sn2[4];
+            const int first = (warp - gmod) & (kConsumerWarps - 1);  // this warp's first group here
+            gmod = (gmod + ngroups) & (kConsumerWarps - 1);
+            if (first < ngroups) {
+                const unsigned char *stage = stages + (size_t)s * lay.stage_bytes;
+                // cos and sign * sin (bf16 pairs) of this token for the lane's 8 dims
+                uint32_t cw[4] = {0, 0, 0, 0}, sw[4] = {0, 0, 0, 0};
                 if (rot_lane) {
                     const unsigned char *cs = stage + lay.slab_bytes + 16 * (q & (kPartner - 1));
-                    const uint4 cw = lds128(cs), sw = lds128(cs + ROT);  // sin half: r/2 elements later
-                    const uint32_t cwa[4] = {cw.x, cw.y, cw.z, cw.w}, swa[4] = {sw.x, sw.y, sw.z, sw.w};
-                    const uint64_t sg2 = pr(sgn, sgn);
-#pragma unroll
-                    for (int j = 0; j < 4; j++) {
-                        c2[j] = bf2_to_f2(cwa[j]);
-                        sn2[j] = mul2(bf2_to_f2(swa[j]), sg2);
-                    }
-                } else {
-#pragma unroll
-                    for (int j = 0; j < 4; j++)
-                        c2[j] = sn2[j] = 0;
+                    const uint4 c4 = lds128(cs), s4 = lds128(cs + ROT);  // sin half: r/2 elements later
+                    const uint32_t flip = (q & kPartner) ? 0u : 0x80008000u;  // lower half subtracts
+                    cw[0] = c4.x, cw[1] = c4.y, cw[2] = c4.z, cw[3] = c4.w;
+                    sw[0] = s4.x ^ flip, sw[1] = s4.y ^ flip, sw[2] = s4.z ^ flip, sw[3] = s4.w ^ flip;
                 }
-                for (; g < gctr + ngroups; g += kConsumerWarps) {
-                    const int r = (int)(g - gctr) * 4 + rr;
+                for (int g = first; g < ngroups; g += kConsumerWarps) {
+                    const int r = g * 4 + rr;
                     const bool active = r < R;
                     const int rc = active ? r : R - 1;
                     const int lr = (int)(((uint64_t)(uint32_t)rc * tp.h_magic) >> 32);
                     const int h = rc - lr * H;
-                    const int l = l0 + lr;
+                    const int l = h_s.l0 + lr;
                     const unsigned char *krow = stage + ((size_t)(2 * lr) * H + h) * 256;
                     const unsigned char *vrow = krow + (size_t)H * 256;
                     const uint4 ka = lds128(krow + 16 * q), kb = lds128(krow + 128 + 16 * q);
@@ -524,7 +591,8 @@ __global__ void __launch_bounds__(kThreads, 2) ctx_kv_tma_kernel(const TmaParams
                     ss += __shfl_xor_sync(0xffffffffu, ss, 4);
                     ss += __shfl_xor_sync(0xffffffffu, ss, 2);
                     ss += __shfl_xor_sync(0xffffffffu, ss, 1);
-                    const float inv = rsqrtf(fmaf(ss, 1.0f / kHeadDim, p.eps));
+                    float inv;  // ss/128 + eps >= eps > 0 (hardware reciprocal square root)
+                    asm("rsqrt.approx.ftz.f32 %0, %1;" : "=f"(inv) : "f"(fmaf(ss, 1.0f / kHeadDim, p.eps)));
                     const uint64_t inv2 = pr(inv, inv);
                     const float4 wa0 = w1[w1_slot(l, 0, q)], wa1 = w1[w1_slot(l, 1, q)];
                     const float4 wb0 = w1[w1_slot(l, 0, 8 + q)], wb1 = w1[w1_slot(l, 1, 8 + q)];
@@ -540,27 +608,22 @@ __global__ void __launch_bounds__(kThreads, 2) ctx_kv_tma_kernel(const TmaParams
 #pragma unroll
                     for (int j = 0; j < 4; j++) {
                         const uint32_t yp = __shfl_xor_sync(0xffffffffu, y[j], kPartner);
-                        const uint64_t rot = fma2(bf2_to_f2(y[j]), c2[j], mul2(bf2_to_f2(yp), sn2[j]));
-                        ko[j] = rot_lane ? f2_to_bf2(rot) : y[j];
+                        const uint32_t rv = f2_to_bf2(rope_bf2(y[j], cw[j], yp, sw[j]));
+                        ko[j] = rot_lane ? rv : y[j];  // both computed: a select, not a branch
                     }
                     if (!active)
                         continue;
-                    const long long dst_row = (row_base + h) * bs + row_off;
-                    const long long elem = off[l] + dst_row * 256;
+                    unsigned char *d = layer_base[l] + h_s.dst + h * head_bytes;
                     if (!FP8) {
-                        unsigned char *d = p.cache0 + elem * 2;
                         st_stream_v4(d + 16 * q, make_uint4(ko[0], ko[1], ko[2], ko[3]));
                         st_stream_v4(d + 128 + 16 * q, make_uint4(y[4], y[5], y[6], y[7]));
                         st_stream_v4(d + 256 + 16 * q, va);
                         st_stream_v4(d + 384 + 16 * q, vb);
                     } else {
-                        const uint4 c4 = *reinterpret_cast<const uint4 *>(scl + 8 * l);
-                        const uint2 b2 = *reinterpret_cast<const uint2 *>(scl + 8 * l + 4);
-                        const uint64_t ks2 = pr(__uint_as_float(c4.x), __uint_as_float(c4.x));
-                        const uint64_t vs2 = pr(__uint_as_float(c4.y), __uint_as_float(c4.y));
-                        const uint64_t kn2 = pr(__uint_as_float(c4.z), __uint_as_float(c4.z));
-                        const uint64_t vn2 = pr(__uint_as_float(c4.w), __uint_as_float(c4.w));
-                        unsigned char *d = p.cache0 + elem;
+                        const ulonglong2 sv = reinterpret_cast<const ulonglong2 *>(scl + 12 * l)[0];
+                        const ulonglong2 nv = reinterpret_cast<const ulonglong2 *>(scl + 12 * l)[1];
+                        const uint2 b2 = *reinterpret_cast<const uint2 *>(scl + 12 * l + 8);
+                        const uint64_t ks2 = sv.x, vs2 = sv.y, kn2 = nv.x, vn2 = nv.y;
                         st_stream_v2(d + 8 * q, quantise8(make_uint4(ko[0], ko[1], ko[2], ko[3]), b2.x, ks2, kn2));
                         st_stream_v2(d + 64 + 8 * q, quantise8(make_uint4(y[4], y[5], y[6], y[7]), b2.x, ks2, kn2));
                         st_stream_v2(d + 128 + 8 * q, quantise8(va, b2.y, vs2, vn2));
@@ -568,7 +631,6 @@ __global__ void __launch_bounds__(kThreads, 2) ctx_kv_tma_kernel(const TmaParams
                     }
                 }
             }
-            gctr += ngroups;
             __syncwarp();
             if (lane == 0)
                 mbar_arrive(empty + s);
@@ -582,8 +644,8 @@ __global__ void __launch_bounds__(kThreads, 2) ctx_kv_tma_kernel(const TmaParams
 }
 
 constexpr int kMaxSlabBytes = 32 * 1024;
-constexpr int kStageBudget = 100 * 1024;  // per CTA, two CTAs per SM
-constexpr int kMaxStages = 16;
+constexpr int kStageBudget = 106 * 1024;  // per CTA, two CTAs per SM
+constexpr int kStages = 3;
 
 struct Plan {
     int Lp, NP, S;
@@ -598,10 +660,14 @@ bool plan_for(const CtxKvParams &p, Plan &pl)
         return false;
     pl.Lp = std::min(L, kMaxSlabBytes / row_bytes);
     pl.NP = (L + pl.Lp - 1) / pl.Lp;
+    // Three stages measured best on the bf16 long-context workload and as good
+    // as four on the fp8 prefill one (a deeper ring of reads in flight slowed
+    // the write-heavy bf16 workload); fewer when three would not leave room
+    // for two CTAs per SM.
     const Layout one = make_layout(L, 1, (uint32_t)pl.Lp * row_bytes);
     const int fixed = (int)one.stages;
     int S = (kStageBudget - fixed) / (int)one.stage_bytes;
-    S = S < 2 ? 2 : (S > kMaxStages ? kMaxStages : S);
+    S = S < 2 ? 2 : (S > kStages ? kStages : S);
     pl.S = S;
     pl.lay = make_layout(L, S, (uint32_t)pl.Lp * row_bytes);
     return pl.lay.total <= 113 * 1024;
@@ -662,6 +728,7 @@ cudaError_t launch_ctx_kv_write_tma(const CtxKvParams &p, int rotary_dim, bool f
     tp.pieces = pl.NP;
     tp.stages = pl.S;
     tp.h_magic = (0x100000000ull + p.num_kv_heads - 1) / (uint64_t)p.num_kv_heads;
+    tp.contiguous = 0;
     const uint32_t smem = pl.lay.total;
     switch (rotary_dim) {
     case 16:

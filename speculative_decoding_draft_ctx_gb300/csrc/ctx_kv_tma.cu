@@ -96,6 +96,14 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t by
 // issue slots from the warps that compute.
 constexpr uint32_t kSuspendNs = 200000;
 
+// Raises the transaction count the current phase of `bar` waits for,
+// without arriving.
+__device__ __forceinline__ void mbar_expect_tx(uint64_t *bar, uint32_t bytes)
+{
+    asm volatile("mbarrier.expect_tx.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(bytes)
+                 : "memory");
+}
+
 __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity)
 {
     uint32_t ok;
@@ -421,9 +429,33 @@ __global__ void __launch_bounds__(kThreads, 2) ctx_kv_tma_kernel(const TmaParams
         uint32_t pph = 0;    // phase parity of round k in that slot
         bool ok = true;
         long long cur_slot, cur_pos, nxt_slot = -1, nxt_pos = 0;
+        // The first S units of the CTA get their K|V block copied before
+        // their slots are known (each takes a stage whatever its slot), which
+        // hides the slot fetch behind the first copies; a padded one among
+        // them is then released unread.
+        auto unit_span = [&](long long u, long long &t, int &l0, uint32_t &slab) {
+            t = NP == 1 ? u : u / NP;
+            l0 = (NP == 1 ? 0 : (int)(u - t * NP)) * Lp;
+            slab = (uint32_t)min(Lp, L - l0) * H * 512u;
+        };
+        int nspec = 0;
+        for (long long u = u_first; u < u_end && nspec < S; u += step)
+            nspec++;
+        if (lane == 0) {
+            for (int i = 0; i < nspec; i++) {
+                long long t;
+                int l0;
+                uint32_t slab;
+                unit_span(u_first + i * step, t, l0, slab);
+                mbar_expect_tx(full + i, slab);
+                bulk_g2s(stages + (size_t)i * lay.stage_bytes, p.all_kv + (t * L + l0) * 2LL * H * kHeadDim, slab,
+                         full + i, stream_once);
+            }
+        }
         long long base = u_first;
+        long long ordinal = 0;  // index of unit `base` in this CTA's sequence
         fetch(base, cur_slot, cur_pos);
-        for (; base < u_end && ok; base += 32 * step) {
+        for (; base < u_end && ok; base += 32 * step, ordinal += 32) {
             const long long nbase = base + 32 * step;
             if (nbase < u_end)
                 fetch(nbase, nxt_slot, nxt_pos);
@@ -434,26 +466,36 @@ __global__ void __launch_bounds__(kThreads, 2) ctx_kv_tma_kernel(const TmaParams
                     break;
                 const long long slot = __shfl_sync(0xffffffffu, cur_slot, i);
                 const long long pos = __shfl_sync(0xffffffffu, cur_pos, i);
-                if (slot < 0)
+                const bool spec = ordinal + i < nspec;
+                if (slot < 0 && !spec)
                     continue;  // padding (or out of range): nothing read, nothing written
                 if (lane == 0) {
                     const int s = ps;
-                    ok = mbar_wait(empty + s, pph ^ 1u, abort);
+                    ok = spec || mbar_wait(empty + s, pph ^ 1u, abort);
                     if (ok) {
-                        const long long t = NP == 1 ? u : u / NP;
-                        const int piece = NP == 1 ? 0 : (int)(u - t * NP);
-                        const int l0 = piece * Lp;
-                        const int lc = min(Lp, L - l0);
-                        const uint32_t slab = (uint32_t)lc * H * 512u;
-                        hdr[s].dst = (((slot >> p.block_size_log2) * H << p.block_size_log2) +
-                                      (slot & ((1LL << p.block_size_log2) - 1))) *
-                                     (FP8 ? kRowElems : 2 * kRowElems);
-                        hdr[s].l0 = l0;
-                        hdr[s].rows = lc * H;
+                        long long t;
+                        int l0;
+                        uint32_t slab;
+                        unit_span(u, t, l0, slab);
                         unsigned char *dst = stages + (size_t)s * lay.stage_bytes;
-                        mbar_arrive_expect_tx(full + s, slab + 2u * ROT);
-                        bulk_g2s(dst, p.all_kv + (t * L + l0) * 2LL * H * kHeadDim, slab, full + s, stream_once);
-                        bulk_g2s(dst + lay.slab_bytes, p.cos_sin + pos * ROT, 2u * ROT, full + s, keep);
+                        if (slot < 0) {
+                            hdr[s].rows = 0;  // a speculatively copied padded unit: release it unread
+                            mbar_arrive(full + s);
+                        } else {
+                            hdr[s].dst = (((slot >> p.block_size_log2) * H << p.block_size_log2) +
+                                          (slot & ((1LL << p.block_size_log2) - 1))) *
+                                         (FP8 ? kRowElems : 2 * kRowElems);
+                            hdr[s].l0 = l0;
+                            hdr[s].rows = (int)(slab / 512u);
+                            if (spec) {
+                                mbar_arrive_expect_tx(full + s, 2u * ROT);
+                            } else {
+                                mbar_arrive_expect_tx(full + s, slab + 2u * ROT);
+                                bulk_g2s(dst, p.all_kv + (t * L + l0) * 2LL * H * kHeadDim, slab, full + s,
+                                         stream_once);
+                            }
+                            bulk_g2s(dst + lay.slab_bytes, p.cos_sin + pos * ROT, 2u * ROT, full + s, keep);
+                        }
                     }
                 }
                 ok = __shfl_sync(0xffffffffu, ok, 0);

@@ -42,7 +42,8 @@ import workloads as wk  # noqa: E402
 
 METRIC = "context-KV write GB/s and rows/s on 1 GB300; % of HBM roofline"
 UNIT = "GB/s"
-KERNEL_SRC = os.path.join(ROOT, "speculative_decoding_draft_ctx_gb300", "csrc", "ctx_kv_kernel.cu")
+KERNEL_SRCS = [os.path.join(ROOT, "speculative_decoding_draft_ctx_gb300", "csrc", f)
+               for f in ("ctx_kv_tma.cu", "ctx_kv_kernel.cu", "ctx_kv_api.cpp", "ctx_kv_internal.h")]
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "ncu_traffic.json")
 FALLBACK_HBM_GBS = 6800.0
 
@@ -94,6 +95,26 @@ def dist_env():
     return ws, rank, local
 
 
+def max_over_ranks(value: float, pg, device) -> float:
+    """The largest `value` over all ranks (the job's time is its slowest rank's)."""
+    if pg is None:
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    pg.all_reduce(t, op=pg.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(units_per_step: float, steps: int, world: int, max_ms: float) -> float:
+    """Units per second of the whole job: every rank processes its own replica
+    of the workload each step (weak scaling), over the slowest rank's time."""
+    return units_per_step * steps * world / (max_ms * 1e-3)
+
+
+def replica_seed(wl: wk.Workload, rank: int, index: int = 0) -> int:
+    """Seed of rank `rank`'s input set `index`: distinct data per replica."""
+    return wl.seed + 1000 * rank + index
+
+
 def measured_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -105,8 +126,13 @@ def measured_peaks():
 
 
 def kernel_sha() -> str:
-    with open(KERNEL_SRC, "rb") as f:
-        return hashlib.sha256(f.read()).hexdigest()[:16]
+    """Hash of the kernel sources: recorded DRAM counters are only reported
+    while it matches the one they were taken on."""
+    h = hashlib.sha256()
+    for path in KERNEL_SRCS:
+        with open(path, "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
 
 
 def recorded_traffic(workload: str):
@@ -283,7 +309,7 @@ def run_ours(args):
     dk.lib()
 
     wl = select_workload(args)
-    base = wk.generate(wl, seed=wl.seed + 1000 * rank)
+    base = wk.generate(wl, seed=replica_seed(wl, rank))
     fp8 = wl.kv_dtype == wk.KV_FP8
     nvalid = base.num_valid_tokens
     step_bytes = wk.compulsory_bytes(wl, nvalid)
@@ -295,7 +321,7 @@ def run_ours(args):
     n_sets = max(1, math.ceil(3 * l2_bytes() / foot))
     sets = []
     for i in range(n_sets):
-        inp = base if i == 0 else wk.generate(wl, seed=wl.seed + 1000 * rank + i)
+        inp = base if i == 0 else wk.generate(wl, seed=replica_seed(wl, rank, i))
         sets.append(inp.to(dev))
     k_scales = [sets[0].k_scale[l:l + 1].clone() for l in range(wl.num_layers)]
     v_scales = [sets[0].v_scale[l:l + 1].clone() for l in range(wl.num_layers)]
@@ -348,13 +374,10 @@ def run_ours(args):
         launch_ms = [total_ms / args.steps]
     else:
         launch_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
-    if pg:
-        t = torch.tensor([total_ms], device=dev)
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(total_ms, pg, dev)
     avg_launch_ms = sum(launch_ms) / len(launch_ms)
-    value = step_bytes * args.steps * ws / (total_ms * 1e-3) / 1e9
-    rows_per_s = step_rows * args.steps * ws / (total_ms * 1e-3)
+    value = whole_job_rate(step_bytes, args.steps, ws, total_ms) / 1e9
+    rows_per_s = whole_job_rate(step_rows, args.steps, ws, total_ms)
 
     peak, peak_kind = measured_peaks()
     achieved = step_bytes / (avg_launch_ms * 1e-3) / 1e9
@@ -364,7 +387,7 @@ def run_ours(args):
     # step's error word read back, every step
     e2e = None
     if not args.no_e2e:
-        host = wk.generate(wl, seed=wl.seed + 1000 * rank)
+        host = wk.generate(wl, seed=replica_seed(wl, rank))
         h_kv = host.all_kv.pin_memory()
         h_pos = host.positions.pin_memory()
         h_slot = host.slot_mapping.pin_memory()
@@ -393,14 +416,10 @@ def run_ours(args):
             e2e_step()
         e1.record(stream)
         torch.cuda.synchronize()
-        e_ms = e0.elapsed_time(e1)
-        if pg:
-            t = torch.tensor([e_ms], device=dev)
-            pg.all_reduce(t, op=pg.ReduceOp.MAX)
-            e_ms = float(t.item())
+        e_ms = max_over_ranks(e0.elapsed_time(e1), pg, dev)
         if int(h_flags.item()) != 0:
             raise RuntimeError(f"write reported error flags {int(h_flags.item())}")
-        e2e = {"value": step_bytes * ne * ws / (e_ms * 1e-3) / 1e9, "unit": UNIT,
+        e2e = {"value": whole_job_rate(step_bytes, ne, ws, e_ms) / 1e9, "unit": UNIT,
                "h2d_bytes_per_step": h_kv.numel() * 2 + h_pos.numel() * 8 + h_slot.numel() * 8,
                "d2h_bytes_per_step": 4, "steps": ne, "ms_per_step": e_ms / ne}
 

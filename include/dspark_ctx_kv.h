@@ -59,6 +59,7 @@ typedef enum {
  * it) and reported; in-range rows are unaffected. */
 #define DSPARK_FLAG_SLOT_RANGE 0x1u /* slot >= num_blocks * block_size */
 #define DSPARK_FLAG_POS_RANGE 0x2u  /* position < 0 or >= max_pos (valid slot) */
+#define DSPARK_FLAG_TIMEOUT 0x4u    /* an internal wait gave up and the kernel stopped early */
 
 /*
  * dspark_ctx_kv_write -- the fused write (writer page, module docstring and

@@ -28,6 +28,7 @@ STATUS = {
 STATUS_CODE = {v: k for k, v in STATUS.items()}
 FLAG_SLOT_RANGE = 0x1
 FLAG_POS_RANGE = 0x2
+FLAG_TIMEOUT = 0x4
 
 # every function the header declares
 EXPORTS = (

@@ -214,6 +214,31 @@ def l2_bytes() -> int:
         return 129 * 2**20
 
 
+def copy_same_bytes(step_bytes: int, dev, stream, launches: int = 50) -> float:
+    """GB/s of PyTorch's own copy kernel when one launch moves the same number
+    of bytes as one write step (half read, half written), timed per launch
+    with CUDA events on rotated buffers that together exceed L2: the
+    streaming rate a single launch of this size reaches on this GPU, for
+    context beside the long-copy peak."""
+    half = max(16, (step_bytes // 2) // 16 * 16)
+    n_sets = max(1, math.ceil(3 * l2_bytes() / (2 * half)))
+    bufs = [(torch.empty(half // 2, dtype=torch.bfloat16, device=dev).fill_(1.0),
+             torch.empty(half // 2, dtype=torch.bfloat16, device=dev)) for _ in range(n_sets)]
+    for i in range(5):
+        bufs[i % n_sets][1].copy_(bufs[i % n_sets][0])
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(launches)]
+    torch.cuda.synchronize()
+    for i, (e0, e1) in enumerate(ev):
+        src, dst = bufs[i % n_sets]
+        e0.record(stream)
+        dst.copy_(src)
+        e1.record(stream)
+    torch.cuda.synchronize()
+    ms = sum(e0.elapsed_time(e1) for e0, e1 in ev) / launches
+    del bufs
+    return 2 * half / (ms * 1e-3) / 1e9
+
+
 # ---------------------------------------------------------------- CPU oracle
 
 class OracleSample:
@@ -382,6 +407,7 @@ def run_ours(args):
     peak, peak_kind = measured_peaks()
     achieved = step_bytes / (avg_launch_ms * 1e-3) / 1e9
     traffic = recorded_traffic(wl.name)
+    copy_gbs = copy_same_bytes(step_bytes, dev, stream)
 
     # end to end through the public API: pinned host inputs copied in, the
     # step's error word read back, every step
@@ -441,7 +467,8 @@ def run_ours(args):
             "bytes_per_step": step_bytes,
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "traffic": traffic, "peak_source": peak_kind,
-                         "frac_of_8tbs": achieved / 8000.0},
+                         "frac_of_8tbs": achieved / 8000.0,
+                         "copy_same_bytes_gbs": copy_gbs, "frac_of_copy_same_bytes": achieved / copy_gbs},
             "cpu_baseline": cpu,
             "e2e": e2e,
             "clocks": clocks,

@@ -26,6 +26,7 @@ import numpy as np
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "ctx_kv_oracle.c")
+_SRC_QK = os.path.join(_HERE, "qk_insert_oracle.c")
 _LIB_PATH = os.path.join(_HERE, "libctx_kv_oracle.so")
 
 KV_BF16 = 0
@@ -47,10 +48,12 @@ def build(force: bool = False) -> str:
     """Compile the oracle with gcc (ISO C11, no FMA contraction, so x86-64 and
     aarch64 hosts evaluate every expression identically)."""
     with _lock:
-        if force or not os.path.exists(_LIB_PATH) or os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC):
+        stale = not os.path.exists(_LIB_PATH) or any(
+            os.path.getmtime(_LIB_PATH) < os.path.getmtime(src) for src in (_SRC, _SRC_QK))
+        if force or stale:
             tmp = _LIB_PATH + f".tmp{os.getpid()}"
             cmd = ["gcc", "-std=c11", "-O2", "-ffp-contract=off", "-fno-fast-math",
-                   "-Wall", "-shared", "-fPIC", "-o", tmp, _SRC, "-lm"]
+                   "-Wall", "-shared", "-fPIC", "-o", tmp, _SRC, _SRC_QK, "-lm"]
             subprocess.run(cmd, check=True)
             os.replace(tmp, _LIB_PATH)
     return _LIB_PATH
@@ -98,6 +101,11 @@ def lib():
         L.dspark_oracle_write.restype = ctypes.c_int
         L.dspark_oracle_rows.argtypes = [P, P, ctypes.c_int64, P, P, P, P, ctypes.c_int64, P]
         L.dspark_oracle_rows.restype = ctypes.c_int
+        L.dspark_oracle_qk_check.argtypes = [P, ctypes.c_int, ctypes.c_int]
+        L.dspark_oracle_qk_check.restype = ctypes.c_int
+        L.dspark_oracle_qk_insert.argtypes = [P, ctypes.c_int64, ctypes.c_int64, P, P, P, P, P, P,
+                                              ctypes.c_int64, P]
+        L.dspark_oracle_qk_insert.restype = ctypes.c_int
         _lib = L
     return _lib
 
@@ -264,4 +272,106 @@ def problem_from_inputs(inp) -> Problem:
         bits(inp.cos_sin), inp.k_scale.cpu().numpy(), inp.v_scale.cpu().numpy(),
         num_blocks=wl.num_blocks, block_size=wl.block_size, rotary_dim=wl.rotary_dim,
         kv_dtype=KV_FP8_E4M3 if wl.kv_dtype == "fp8_e4m3" else KV_BF16, eps=inp.eps,
+    )
+
+
+# ---------------------------------------------------------------- draft-token QK insert
+
+class QkOracleInputs(ctypes.Structure):
+    _fields_ = [
+        ("qkv", ctypes.c_void_p), ("q_norm_w", ctypes.c_void_p), ("k_norm_w", ctypes.c_void_p),
+        ("positions", ctypes.c_void_p), ("slot_mapping", ctypes.c_void_p), ("cos_sin", ctypes.c_void_p),
+        ("num_tokens", ctypes.c_int64), ("max_pos", ctypes.c_int64), ("num_blocks", ctypes.c_int64),
+        ("num_heads", ctypes.c_int32), ("num_kv_heads", ctypes.c_int32), ("block_size", ctypes.c_int32),
+        ("rotary_dim", ctypes.c_int32), ("kv_dtype", ctypes.c_int32), ("eps", ctypes.c_float),
+        ("k_scale", ctypes.c_float), ("v_scale", ctypes.c_float), ("q_scale", ctypes.c_float),
+    ]
+
+
+ALT_QKV, ALT_QFP8, ALT_CACHE = 0, 1, 2
+
+
+class QkProblem:
+    """Host copies of one draft-token QK-norm / RoPE / KV-insert call, kept
+    alive for the C side (``qk_insert_oracle.c`` has the definition).
+
+    Arrays: qkv ``[T, (Hq + 2 Hkv) * 128]``, the two norm weights ``[128]`` and
+    cos_sin as uint16 bf16 bits; positions and slot_mapping int64."""
+
+    def __init__(self, qkv, q_norm_w, k_norm_w, positions, slot_mapping, cos_sin, *, num_heads: int,
+                 num_kv_heads: int, num_blocks: int, block_size: int, rotary_dim: int, kv_dtype: int,
+                 eps: float, k_scale: float = 1.0, v_scale: float = 1.0, q_scale: float = 1.0):
+        self.Hq, self.Hkv = int(num_heads), int(num_kv_heads)
+        self.width = (self.Hq + 2 * self.Hkv) * HEAD_DIM
+        self.qkv = np.ascontiguousarray(qkv, dtype=np.uint16).reshape(-1, self.width)
+        self.T = self.qkv.shape[0]
+        self.q_norm_w = np.ascontiguousarray(q_norm_w, dtype=np.uint16).reshape(HEAD_DIM)
+        self.k_norm_w = np.ascontiguousarray(k_norm_w, dtype=np.uint16).reshape(HEAD_DIM)
+        self.positions = np.ascontiguousarray(positions, dtype=np.int64).reshape(self.T)
+        self.slot_mapping = None if slot_mapping is None else \
+            np.ascontiguousarray(slot_mapping, dtype=np.int64).reshape(self.T)
+        self.cos_sin = np.ascontiguousarray(cos_sin, dtype=np.uint16)
+        assert self.cos_sin.ndim == 2 and self.cos_sin.shape[1] == rotary_dim
+        self.num_blocks, self.block_size = int(num_blocks), int(block_size)
+        self.rotary_dim, self.kv_dtype, self.eps = int(rotary_dim), int(kv_dtype), float(eps)
+        self.k_scale, self.v_scale, self.q_scale = float(k_scale), float(v_scale), float(q_scale)
+        self.c = QkOracleInputs(
+            _ptr(self.qkv), _ptr(self.q_norm_w), _ptr(self.k_norm_w), _ptr(self.positions),
+            _ptr(self.slot_mapping) if self.slot_mapping is not None else None, _ptr(self.cos_sin),
+            self.T, self.cos_sin.shape[0], self.num_blocks, self.Hq, self.Hkv, self.block_size,
+            self.rotary_dim, self.kv_dtype, ctypes.c_float(self.eps).value,
+            ctypes.c_float(self.k_scale).value, ctypes.c_float(self.v_scale).value,
+            ctypes.c_float(self.q_scale).value,
+        )
+
+    @property
+    def elem_dtype(self):
+        return np.uint8 if self.kv_dtype == KV_FP8_E4M3 else np.uint16
+
+    def new_cache(self, fill_byte: int = 0xFF):
+        c = np.empty((self.num_blocks, self.Hkv, self.block_size, ROW), dtype=self.elem_dtype)
+        c.view(np.uint8).fill(fill_byte)
+        return c
+
+    def run(self, cache=None, q_fp8: bool = False, t_begin: int = 0, t_end: int | None = None,
+            qkv_out=None):
+        """Run the call.  Returns (qkv_out, q_fp8_out or None, alternates),
+        alternates as arrays (output ALT_*, element index, value); ``cache``
+        (host, the cache dtype) is written in place when given."""
+        t_end = self.T if t_end is None else t_end
+        if qkv_out is None:
+            qkv_out = self.qkv.copy()
+        assert qkv_out.flags["C_CONTIGUOUS"] and qkv_out.shape == self.qkv.shape
+        qf = np.full((self.T, self.Hq * HEAD_DIM), 0xFF, np.uint8) if q_fp8 else None
+        if cache is not None:
+            assert cache.flags["C_CONTIGUOUS"] and cache.dtype == self.elem_dtype
+        elems = max(1, (t_end - t_begin) * (self.Hq + 2 * self.Hkv) * HEAD_DIM)
+        cap = max(4096, elems // 16)
+        aw = np.empty(cap, np.int32)
+        ae = np.empty(cap, np.int64)
+        av = np.empty(cap, np.uint16)
+        n = ctypes.c_int64()
+        rc = lib().dspark_oracle_qk_insert(
+            ctypes.byref(self.c), t_begin, t_end, _ptr(qkv_out), _ptr(qf) if qf is not None else None,
+            _ptr(cache) if cache is not None else None, _ptr(aw), _ptr(ae), _ptr(av), cap, ctypes.byref(n))
+        _check(rc)
+        k = n.value
+        return qkv_out, qf, (aw[:k].copy(), ae[:k].copy(), av[:k].copy())
+
+
+def qk_problem_from_inputs(inp, with_slots: bool = True) -> QkProblem:
+    """A QkProblem from a ``workloads.QkInputs`` (CPU torch tensors)."""
+    import torch  # local: the oracle's arithmetic does not use torch
+
+    def bits(x):
+        return x.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
+
+    wl = inp.workload
+    return QkProblem(
+        bits(inp.qkv), bits(inp.q_norm_w), bits(inp.k_norm_w), inp.positions.cpu().numpy(),
+        inp.slot_mapping.cpu().numpy() if with_slots else None, bits(inp.cos_sin),
+        num_heads=wl.num_heads, num_kv_heads=wl.num_kv_heads, num_blocks=wl.num_blocks,
+        block_size=wl.block_size, rotary_dim=wl.rotary_dim,
+        kv_dtype=KV_FP8_E4M3 if wl.kv_dtype == "fp8_e4m3" else KV_BF16, eps=inp.eps,
+        k_scale=inp.k_scale, v_scale=inp.v_scale, q_scale=inp.q_scale,
     )

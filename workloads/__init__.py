@@ -6,3 +6,7 @@ from .synth import (  # noqa: F401
     WORKLOADS_BY_NAME, Inputs, generate, make_caches, take_tokens,
     rope_cos_sin_cache, compulsory_bytes, describe,
 )
+from .qk_insert import (  # noqa: F401
+    QUERY_ROWS_PER_REQUEST, QkWorkload, QK_WORKLOADS, QK_WORKLOADS_BY_NAME, QkInputs, generate_qk,
+    make_qk_cache, qk_compulsory_bytes, describe_qk,
+)

@@ -43,7 +43,9 @@ import workloads as wk  # noqa: E402
 METRIC = "context-KV write GB/s and rows/s on 1 GB300; % of HBM roofline"
 UNIT = "GB/s"
 KERNEL_SRCS = [os.path.join(ROOT, "speculative_decoding_draft_ctx_gb300", "csrc", f)
-               for f in ("ctx_kv_tma.cu", "ctx_kv_kernel.cu", "ctx_kv_api.cpp", "ctx_kv_internal.h")]
+               for f in ("ctx_kv_tma.cu", "ctx_kv_kernel.cu", "ctx_kv_api.cpp", "ctx_kv_internal.h",
+                         "ctx_kv_device.cuh")]
+QK_METRIC = "draft-token QK-norm/RoPE/KV-insert GB/s on 1 GB300; % of HBM roofline"
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "ncu_traffic.json")
 FALLBACK_HBM_GBS = 6800.0
 
@@ -54,7 +56,9 @@ def parse_args(argv=None):
     ap.add_argument("--steps", type=int, default=4000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--config", default="long_context", choices=[w.name for w in wk.WORKLOADS])
+    ap.add_argument("--config", default="long_context",
+                    choices=[w.name for w in wk.WORKLOADS] + [w.name for w in wk.QK_WORKLOADS],
+                    help="a context-KV write workload, or a qk_* workload of the draft-token QK insert")
     ap.add_argument("--e2e-steps", type=int, default=30)
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="oracle sample budget")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -284,10 +288,51 @@ def cpu_baseline(inp: wk.Inputs, seconds: float):
     }
 
 
+def run_reference_qk(args):
+    """The reference arm for a draft-token QK-insert workload: the oracle on a
+    bounded sample (the first tokens of the call) per step."""
+    import oracle
+
+    wl = wk.QK_WORKLOADS_BY_NAME[args.config]
+    inp = wk.generate_qk(wl)
+    p = oracle.qk_problem_from_inputs(inp)
+    per_step = 90.0 / max(1, args.steps + args.warmup)
+    probe = min(wl.num_tokens, 14)
+    t = time.perf_counter()
+    p.run(cache=p.new_cache(), q_fp8=wl.q_fp8, t_end=probe)
+    per_tok = max((time.perf_counter() - t) / probe, 1e-7)
+    n = int(max(1, min(wl.num_tokens, per_step / per_tok)))
+    nvalid = int((inp.slot_mapping[:n] >= 0).sum())
+    sample_bytes = wk.qk_compulsory_bytes(wl, nvalid, num_tokens=n)
+    cache = p.new_cache()
+    for _ in range(args.warmup):
+        p.run(cache=cache, q_fp8=wl.q_fp8, t_end=n)
+    total = 0.0
+    for _ in range(args.steps):
+        t = time.perf_counter()
+        p.run(cache=cache, q_fp8=wl.q_fp8, t_end=n)
+        total += time.perf_counter() - t
+    value = sample_bytes * args.steps / total / 1e9
+    sample = f"first {n} of {wl.num_tokens} tokens per step, one thread, plain C oracle"
+    line = {
+        "impl": "reference", "metric": QK_METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": dict(wk.describe_qk(wl), sample_tokens=n),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def run_reference(args):
     ws, rank, _ = dist_env()
     if rank != 0:
         return 0
+    if args.config in wk.QK_WORKLOADS_BY_NAME:
+        return run_reference_qk(args)
     wl = select_workload(args)
     inp = wk.generate(wl)
     budget = 90.0  # seconds of oracle work for the whole run
@@ -481,10 +526,149 @@ def run_ours(args):
     return 0
 
 
+def run_qk(args):
+    """The draft-token fused QK-norm / RoPE / KV insert: one launch per step
+    over one draft batch, replayed from a CUDA graph (a launch-bound few-MB
+    call) over rotated input sets whose footprint exceeds L2."""
+    import speculative_decoding_draft_ctx_gb300 as dk
+
+    ws, rank, local = dist_env()
+    if not torch.cuda.is_available():
+        raise RuntimeError("bench.py needs a CUDA device")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    pg = None
+    if ws > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl", device_id=dev)
+        pg = dist
+    dk.lib()
+    wl = wk.QK_WORKLOADS_BY_NAME[args.config]
+    base = wk.generate_qk(wl, seed=wl.seed + 1000 * rank)
+    step_bytes = wk.qk_compulsory_bytes(wl, base.num_valid_tokens)
+    foot = step_bytes
+    n_sets = max(1, math.ceil(3 * l2_bytes() / foot))
+    sets = [(base if i == 0 else wk.generate_qk(wl, seed=wl.seed + 1000 * rank + i)).to(dev) for i in range(n_sets)]
+    caches = [wk.make_qk_cache(wl, device=dev, fill=0) for _ in range(n_sets)]
+    qf = [torch.empty((wl.num_tokens, wl.num_heads * 128), dtype=torch.uint8, device=dev) if wl.q_fp8 else None
+          for _ in range(n_sets)]
+    ks = torch.tensor([base.k_scale], dtype=torch.float32, device=dev)
+    vs = torch.tensor([base.v_scale], dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step(i):
+        j = i % n_sets
+        d = sets[j]
+        dk.qknorm_rope_kv_insert(d.qkv, d.q_norm_w, d.k_norm_w, d.cos_sin, d.positions, wl.num_heads,
+                                 wl.num_kv_heads, wl.rotary_dim, d.eps, slot_mapping=d.slot_mapping,
+                                 kv_cache=caches[j], k_scale=ks, v_scale=vs, q_fp8_out=qf[j],
+                                 q_fp8_scale=d.q_scale)
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+    side = torch.cuda.Stream()
+    side.wait_stream(stream)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=side):
+        for i in range(args.steps):
+            step(i)
+    stream.wait_stream(side)
+    graph.replay()
+    torch.cuda.synchronize()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if pg:
+        pg.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        t0.record(stream)
+        graph.replay()
+        t1.record(stream)
+        torch.cuda.synchronize()
+    if pg:
+        pg.barrier()
+    total_ms = max_over_ranks(t0.elapsed_time(t1), pg, dev)
+    launch_ms = total_ms / args.steps
+    value = whole_job_rate(step_bytes, args.steps, ws, total_ms) / 1e9
+    peak, peak_kind = measured_peaks()
+    achieved = step_bytes / (launch_ms * 1e-3) / 1e9
+
+    e2e = None
+    if not args.no_e2e:
+        host = wk.generate_qk(wl, seed=wl.seed + 1000 * rank)
+        h_qkv, h_pos, h_slot = host.qkv.pin_memory(), host.positions.pin_memory(), host.slot_mapping.pin_memory()
+        d = sets[0]
+        flags = torch.zeros(1, dtype=torch.int32, device=dev)
+        h_flags = torch.zeros(1, dtype=torch.int32).pin_memory()
+        h_q = torch.empty_like(d.qkv, device="cpu").pin_memory()
+        ne = max(1, args.e2e_steps)
+
+        def e2e_step():
+            d.qkv.copy_(h_qkv, non_blocking=True)
+            d.positions.copy_(h_pos, non_blocking=True)
+            d.slot_mapping.copy_(h_slot, non_blocking=True)
+            dk.qknorm_rope_kv_insert(d.qkv, d.q_norm_w, d.k_norm_w, d.cos_sin, d.positions, wl.num_heads,
+                                     wl.num_kv_heads, wl.rotary_dim, d.eps, slot_mapping=d.slot_mapping,
+                                     kv_cache=caches[0], k_scale=ks, v_scale=vs, q_fp8_out=qf[0],
+                                     q_fp8_scale=d.q_scale, error_flags=flags)
+            h_q.copy_(d.qkv, non_blocking=True)
+            h_flags.copy_(flags, non_blocking=True)
+
+        for _ in range(3):
+            e2e_step()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(ne):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        e_ms = max_over_ranks(e0.elapsed_time(e1), pg, dev)
+        if int(h_flags.item()) != 0:
+            raise RuntimeError(f"insert reported error flags {int(h_flags.item())}")
+        e2e = {"value": whole_job_rate(step_bytes, ne, ws, e_ms) / 1e9, "unit": UNIT,
+               "h2d_bytes_per_step": h_qkv.numel() * 2 + h_pos.numel() * 8 + h_slot.numel() * 8,
+               "d2h_bytes_per_step": h_q.numel() * 2 + 4, "steps": ne, "ms_per_step": e_ms / ne}
+
+    cpu = None
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        import oracle
+
+        p = oracle.qk_problem_from_inputs(base)
+        cache = p.new_cache()
+        t = time.perf_counter()
+        p.run(cache=cache, q_fp8=wl.q_fp8)
+        dt = time.perf_counter() - t
+        cpu = {"value": step_bytes / dt / 1e9, "unit": UNIT, "cores": 1, "kind": "oracle", "seconds": dt,
+               "sample": f"the whole call ({wl.num_tokens} tokens), one thread, plain C oracle"}
+    if rank == 0:
+        line = {
+            "metric": QK_METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": dict(wk.describe_qk(wl), parallelism=f"replicas{ws}", input_sets=n_sets,
+                           timing="one CUDA graph of all steps",
+                           l2=f"{n_sets} input sets rotated, footprint > 3x L2"),
+            "bytes_per_step": step_bytes,
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                         "frac": achieved / peak, "traffic": None, "peak_source": peak_kind,
+                         "frac_of_8tbs": achieved / 8000.0},
+            "cpu_baseline": cpu, "e2e": e2e, "clocks": clk.summary(), "gpu_launches": args.steps,
+            "kernel_avg_us": launch_ms * 1e3,
+        }
+        print(json.dumps(line), flush=True)
+    if pg:
+        pg.destroy_process_group()
+    return 0
+
+
 def main(argv=None):
     args = parse_args(argv)
     if args.impl == "reference":
         return run_reference(args)
+    if args.config in wk.QK_WORKLOADS_BY_NAME:
+        return run_qk(args)
     return run_ours(args)
 
 

@@ -115,6 +115,52 @@ int dspark_ctx_kv_write_ex(const void *all_kv, const void *knorm_w, const int64_
                            int rotary_dim, float eps, int kv_dtype, unsigned int *error_flags,
                            cudaStream_t stream);
 
+/*
+ * dspark_qknorm_rope_kv_insert -- the draft tokens' fused QK-norm / RoPE,
+ * also storing their K/V (DSpark draft model page,
+ * dspark_qknorm_rope_kv_insert; norm, RoPE, cache layout and fp8 rule as in
+ * the context-KV writer page).  One launch.
+ *
+ *  qkv           device, bf16 [num_tokens, (num_heads + 2 num_kv_heads) * 128]
+ *                contiguous, 16-byte aligned: per token the query heads, then
+ *                the key heads, then the value heads.  Updated in place: every
+ *                query and key head of every token (padding included) becomes
+ *                RoPE(GemmaRMSNorm(x)) in bf16; value heads are not changed.
+ *  q_norm_w,     device, bf16 [128] each, 16-byte aligned: the Gemma weights
+ *  k_norm_w      w of the query and key norms (applied as 1 + w to every head).
+ *  cos_sin       device, bf16 [max_pos, rotary_dim], 16-byte aligned (cos | sin).
+ *  positions     device, int64 [num_tokens].  A token whose position lies
+ *                outside [0, max_pos) is left untouched (not inserted either)
+ *                and DSPARK_FLAG_POS_RANGE is raised.
+ *  num_heads, num_kv_heads   query heads and KV heads (>= 1); head_dim 128.
+ *  rotary_dim    16, 32 or 64.   eps: finite, >= 0.
+ *  slot_mapping  device, int64 [num_tokens], or NULL: no insert.  Tokens with
+ *                slot >= 0 have each KV head's K'|V row stored at block
+ *                slot / block_size, offset slot % block_size; valid slots
+ *                must be distinct (duplicates race); a slot beyond the cache
+ *                is not inserted and raises DSPARK_FLAG_SLOT_RANGE.
+ *  kv_cache      device, [num_blocks, num_kv_heads, block_size, 256] of bf16
+ *                (kv_dtype DSPARK_KV_BF16) or uint8 e4m3 codes
+ *                (DSPARK_KV_FP8_E4M3), 16-byte aligned; NULL exactly when
+ *                slot_mapping is NULL.
+ *  k_scale,      device fp32 scalars read when the kernel runs: an fp8 cache
+ *  v_scale       stores e4m3(x / scale) (IEEE fp32 division, RNE, saturating
+ *                at +-448); NULL means 1.  Ignored for a bf16 cache.
+ *  q_fp8_out     device, uint8 [num_tokens, num_heads * 128], 16-byte aligned,
+ *                or NULL: receives e4m3(q' / q_fp8_scale) of every query head.
+ *  q_fp8_scale   host fp32, positive and finite when q_fp8_out is given.
+ *  error_flags   device word the kernel ORs DSPARK_FLAG_* bits into, or NULL.
+ *  stream        the CUDA stream the kernel is enqueued on.
+ * num_tokens == 0 returns DSPARK_OK without a launch.  Allocates, copies and
+ * synchronises nothing.
+ */
+int dspark_qknorm_rope_kv_insert(void *qkv, const void *q_norm_w, const void *k_norm_w, const void *cos_sin,
+                                 int64_t max_pos, const int64_t *positions, int64_t num_tokens, int num_heads,
+                                 int num_kv_heads, int rotary_dim, float eps, const int64_t *slot_mapping,
+                                 void *kv_cache, int64_t num_blocks, int block_size, int kv_dtype,
+                                 const float *k_scale, const float *v_scale, void *q_fp8_out, float q_fp8_scale,
+                                 unsigned int *error_flags, cudaStream_t stream);
+
 /* 1 when the kernel handles this head (writer page, rotary_dims_supported:
  * head_dim 128 and rotary_dim 16, 32 or 64), else 0. */
 int dspark_ctx_kv_rotary_dims_supported(int rotary_dim, int head_dim);

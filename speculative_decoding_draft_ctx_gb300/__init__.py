@@ -2,7 +2,8 @@
 
 One kernel launch norms (Gemma RMSNorm), ropes (partial NeoX) and stores the
 context K/V of every draft layer into its paged KV cache, as bf16 or fp8
-e4m3.  The compute runs in ``libdspark_ctx_kv.so`` (C ABI declared in
+e4m3; a second launch does the draft tokens' fused QK-norm / RoPE with their
+K/V insert.  The compute runs in ``libdspark_ctx_kv.so`` (C ABI declared in
 ``include/dspark_ctx_kv.h``); this package is its ctypes binding.
 """
 
@@ -10,6 +11,6 @@ from ._binding import (  # noqa: F401
     CACHE_ROW, EXPORTS, FLAG_POS_RANGE, FLAG_SLOT_RANGE, FLAG_TIMEOUT, HEAD_DIM, KV_BF16, KV_FP8_E4M3, STATUS,
     STATUS_CODE, CacheDesc, DSparkError, Tables, cache_desc, check, dspark_ctx_kv_last_error,
     dspark_ctx_kv_rotary_dims_supported, dspark_ctx_kv_status_string, dspark_ctx_kv_validate_layers,
-    dspark_ctx_kv_write, dspark_ctx_kv_write_ex, kv_dtype_code, lib, library_path,
+    dspark_ctx_kv_write, dspark_ctx_kv_write_ex, dspark_qknorm_rope_kv_insert, kv_dtype_code, lib, library_path,
 )
-from .writer import ContextKVWriter, rotary_dims_supported  # noqa: F401
+from .writer import ContextKVWriter, qknorm_rope_kv_insert, rotary_dims_supported  # noqa: F401

@@ -36,7 +36,7 @@ EXPORTS = (
     "dspark_ctx_kv_validate_layers", "dspark_ctx_kv_tables_create", "dspark_ctx_kv_tables_update",
     "dspark_ctx_kv_tables_cache_offsets", "dspark_ctx_kv_tables_k_scales",
     "dspark_ctx_kv_tables_v_scales", "dspark_ctx_kv_tables_builds", "dspark_ctx_kv_tables_destroy",
-    "dspark_ctx_kv_last_error", "dspark_ctx_kv_status_string",
+    "dspark_ctx_kv_last_error", "dspark_ctx_kv_status_string", "dspark_qknorm_rope_kv_insert",
 )
 
 
@@ -102,6 +102,9 @@ def lib() -> ctypes.CDLL:
         L.dspark_ctx_kv_last_error.restype = ctypes.c_char_p
         L.dspark_ctx_kv_status_string.argtypes = [I]
         L.dspark_ctx_kv_status_string.restype = ctypes.c_char_p
+        L.dspark_qknorm_rope_kv_insert.argtypes = [P, P, P, P, I64, P, I64, I, I, I, ctypes.c_float, P, P, I64,
+                                                   I, I, P, P, P, ctypes.c_float, P, P]
+        L.dspark_qknorm_rope_kv_insert.restype = I
         _lib = L
         return L
 
@@ -160,6 +163,20 @@ def dspark_ctx_kv_write_ex(all_kv, knorm_w, positions, slot_mapping, num_ctx, co
         _addr(cos_sin), int(max_pos), _addr(layer0_cache), int(num_blocks), _addr(cache_offsets),
         _addr(k_scales), _addr(v_scales), int(L), int(nkv), int(block_size), int(rotary_dim),
         float(eps), kv_dtype_code(kv_dtype), _addr(error_flags), _stream(stream)))
+
+
+def dspark_qknorm_rope_kv_insert(qkv, q_norm_w, k_norm_w, cos_sin, max_pos, positions, num_tokens,
+                                 num_heads, num_kv_heads, rotary_dim, eps, slot_mapping, kv_cache,
+                                 num_blocks, block_size, kv_dtype, k_scale, v_scale, q_fp8_out,
+                                 q_fp8_scale, error_flags=None, stream=None):
+    """``dspark_qknorm_rope_kv_insert`` of the C ABI: tensors (or int
+    addresses, None = NULL) in, DSparkError on a non-OK status."""
+    check(lib().dspark_qknorm_rope_kv_insert(
+        _addr(qkv), _addr(q_norm_w), _addr(k_norm_w), _addr(cos_sin), int(max_pos), _addr(positions),
+        int(num_tokens), int(num_heads), int(num_kv_heads), int(rotary_dim), float(eps),
+        _addr(slot_mapping), _addr(kv_cache), int(num_blocks), int(block_size), kv_dtype_code(kv_dtype),
+        _addr(k_scale), _addr(v_scale), _addr(q_fp8_out), float(q_fp8_scale), _addr(error_flags),
+        _stream(stream)))
 
 
 def dspark_ctx_kv_rotary_dims_supported(rotary_dim: int, head_dim: int) -> bool:

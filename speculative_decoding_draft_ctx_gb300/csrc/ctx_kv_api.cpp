@@ -6,7 +6,9 @@
 // (per-layer cache element offsets and scale addresses, rebuilt only when the
 // data_ptrs change so CUDA-graph replays keep addressing the same memory),
 // __call__ (num_ctx == 0 launches nothing), rotary_dims_supported (head_dim
-// 128, rotary_dim 16/32/64).
+// 128, rotary_dim 16/32/64); DSpark draft model page --
+// dspark_qknorm_rope_kv_insert (the draft tokens' fused QK-norm/RoPE and K/V
+// insert, its insert skipped without a slot mapping).
 #include "../../include/dspark_ctx_kv.h"
 
 #include <cmath>
@@ -167,6 +169,86 @@ int dspark_ctx_kv_write(const void *all_kv, const void *knorm_w, const int64_t *
     return dspark_ctx_kv_write_ex(all_kv, knorm_w, positions, slot_mapping, num_ctx, cos_sin, max_pos,
                                   layer0_cache, num_blocks, cache_offsets, k_scales, v_scales, L, nkv,
                                   block_size, rotary_dim, eps, kv_dtype, nullptr, stream);
+}
+
+int dspark_qknorm_rope_kv_insert(void *qkv, const void *q_norm_w, const void *k_norm_w, const void *cos_sin,
+                                 int64_t max_pos, const int64_t *positions, int64_t num_tokens, int num_heads,
+                                 int num_kv_heads, int rotary_dim, float eps, const int64_t *slot_mapping,
+                                 void *kv_cache, int64_t num_blocks, int block_size, int kv_dtype,
+                                 const float *k_scale, const float *v_scale, void *q_fp8_out, float q_fp8_scale,
+                                 unsigned int *error_flags, cudaStream_t stream)
+{
+    if (num_tokens < 0)
+        return fail(DSPARK_ERR_INVALID_ARG, "num_tokens %lld < 0", (long long)num_tokens);
+    if (num_heads <= 0 || num_kv_heads <= 0)
+        return fail(DSPARK_ERR_INVALID_ARG, "num_heads=%d num_kv_heads=%d must be >= 1", num_heads, num_kv_heads);
+    if (max_pos <= 0)
+        return fail(DSPARK_ERR_INVALID_ARG, "max_pos %lld must be >= 1", (long long)max_pos);
+    if (!dspark_ctx_kv_rotary_dims_supported(rotary_dim, DSPARK_HEAD_DIM))
+        return fail(DSPARK_ERR_UNSUPPORTED_ROTARY_DIM, "rotary_dim %d not in {16, 32, 64}", rotary_dim);
+    if (!(eps >= 0.0f) || std::isinf(eps))
+        return fail(DSPARK_ERR_INVALID_ARG, "eps must be finite and >= 0");
+    const int64_t width = (int64_t)num_heads + 2 * (int64_t)num_kv_heads;
+    if (width > (int64_t)1 << 24 || num_tokens > (INT64_MAX / width) / (2 * DSPARK_HEAD_DIM))
+        return fail(DSPARK_ERR_INVALID_ARG, "num_tokens %lld too large", (long long)num_tokens);
+    const bool insert = slot_mapping != nullptr && kv_cache != nullptr;
+    if ((slot_mapping != nullptr) != (kv_cache != nullptr))
+        return fail(DSPARK_ERR_INVALID_ARG, "slot_mapping and kv_cache go together (both or neither)");
+    int64_t capacity = 0;
+    int bsl = 0;
+    if (insert) {
+        if (!pow2(block_size))
+            return fail(DSPARK_ERR_BLOCK_SIZE, "block size %d is not a power of two", block_size);
+        if (kv_dtype != DSPARK_KV_BF16 && kv_dtype != DSPARK_KV_FP8_E4M3)
+            return fail(DSPARK_ERR_DTYPE, "kv dtype %d unknown", kv_dtype);
+        if (num_blocks <= 0 || num_blocks > (INT64_MAX / num_kv_heads) / block_size / DSPARK_CACHE_ROW)
+            return fail(DSPARK_ERR_INVALID_ARG, "cache of %lld blocks invalid", (long long)num_blocks);
+        capacity = num_blocks * (int64_t)block_size;
+        bsl = log2_exact(block_size);
+        if (!aligned(kv_cache, 16))
+            return fail(DSPARK_ERR_ALIGNMENT, "kv_cache must be 16-byte aligned");
+        if (!aligned(slot_mapping, 8) || (k_scale && !aligned(k_scale, 4)) || (v_scale && !aligned(v_scale, 4)))
+            return fail(DSPARK_ERR_ALIGNMENT, "slot_mapping must be 8-byte and scales 4-byte aligned");
+    }
+    if (q_fp8_out && (!(q_fp8_scale > 0.0f) || std::isinf(q_fp8_scale)))
+        return fail(DSPARK_ERR_INVALID_ARG, "q_fp8_scale must be positive and finite");
+    if (num_tokens == 0)
+        return ok();  // nothing to rotate or insert, and no launch
+    if (!qkv || !q_norm_w || !k_norm_w || !cos_sin || !positions)
+        return fail(DSPARK_ERR_INVALID_ARG, "null buffer pointer");
+    if (!aligned(qkv, 16) || !aligned(q_norm_w, 16) || !aligned(k_norm_w, 16) || !aligned(cos_sin, 16) ||
+        (q_fp8_out && !aligned(q_fp8_out, 16)))
+        return fail(DSPARK_ERR_ALIGNMENT, "qkv, the norm weights, cos_sin and q_fp8_out must be 16-byte aligned");
+    if (!aligned(positions, 8))
+        return fail(DSPARK_ERR_ALIGNMENT, "positions must be 8-byte aligned");
+    if (error_flags && !aligned(error_flags, 4))
+        return fail(DSPARK_ERR_ALIGNMENT, "error_flags must be 4-byte aligned");
+
+    dspark::QkInsertParams p{};
+    p.qkv = static_cast<uint16_t *>(qkv);
+    p.q_norm_w = static_cast<const uint16_t *>(q_norm_w);
+    p.k_norm_w = static_cast<const uint16_t *>(k_norm_w);
+    p.cos_sin = static_cast<const uint16_t *>(cos_sin);
+    p.positions = positions;
+    p.slot_mapping = insert ? slot_mapping : nullptr;
+    p.cache = insert ? static_cast<unsigned char *>(kv_cache) : nullptr;
+    p.k_scale = k_scale;
+    p.v_scale = v_scale;
+    p.q_fp8 = static_cast<unsigned char *>(q_fp8_out);
+    p.error_flags = error_flags;
+    p.num_tokens = num_tokens;
+    p.max_pos = max_pos;
+    p.capacity = capacity;
+    p.num_heads = num_heads;
+    p.num_kv_heads = num_kv_heads;
+    p.block_size_log2 = bsl;
+    p.eps = eps;
+    p.q_scale = q_fp8_out ? q_fp8_scale : 1.0f;
+    const bool fp8 = insert && kv_dtype == DSPARK_KV_FP8_E4M3;
+    cudaError_t e = dspark::launch_qk_insert(p, rotary_dim, fp8, stream);
+    if (e != cudaSuccess)
+        return fail(DSPARK_ERR_CUDA, "launch failed: %s", cudaGetErrorString(e));
+    return ok();
 }
 
 int dspark_ctx_kv_validate_layers(int L, const dspark_cache_desc *layers)

@@ -44,4 +44,29 @@ cudaError_t launch_ctx_kv_write(const CtxKvParams &p, int rotary_dim, bool fp8, 
 bool tma_path_supported(const CtxKvParams &p);
 cudaError_t launch_ctx_kv_write_tma(const CtxKvParams &p, int rotary_dim, bool fp8, cudaStream_t stream);
 
+// Draft-token fused QK-norm / RoPE / KV insert (qk_insert_kernel.cu).
+struct QkInsertParams {
+    uint16_t *qkv;               // bf16 bits [T, (Hq + 2 Hkv) * 128], updated in place
+    const uint16_t *q_norm_w;    // bf16 bits [128]
+    const uint16_t *k_norm_w;    // bf16 bits [128]
+    const uint16_t *cos_sin;     // bf16 bits [max_pos, rotary_dim]
+    const int64_t *positions;    // [T]
+    const int64_t *slot_mapping; // [T] or null (no insert)
+    unsigned char *cache;        // [num_blocks, Hkv, block_size, 256] or null (no insert)
+    const float *k_scale;        // fp8 cache: device fp32 scalars (null = 1)
+    const float *v_scale;
+    unsigned char *q_fp8;        // [T, Hq * 128] e4m3 codes, or null
+    unsigned int *error_flags;   // may be null
+    int64_t num_tokens;
+    int64_t max_pos;
+    int64_t capacity;            // num_blocks * block_size
+    int32_t num_heads;
+    int32_t num_kv_heads;
+    int32_t block_size_log2;
+    float eps;
+    float q_scale;
+};
+
+cudaError_t launch_qk_insert(const QkInsertParams &p, int rotary_dim, bool fp8_cache, cudaStream_t stream);
+
 }  // namespace dspark

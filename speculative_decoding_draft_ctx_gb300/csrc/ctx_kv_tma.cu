@@ -40,6 +40,7 @@
 #include <algorithm>
 #include <mutex>
 
+#include "ctx_kv_device.cuh"
 #include "ctx_kv_internal.h"
 
 namespace dspark {
@@ -180,49 +181,6 @@ __device__ __forceinline__ void st_stream_v2(void *p, uint2 v)
     asm volatile("st.global.cs.v2.u32 [%0], {%1, %2};" ::"l"(p), "r"(v.x), "r"(v.y) : "memory");
 }
 
-__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
-{
-    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
-    return *reinterpret_cast<uint32_t *>(&v);
-}
-
-// ------------------------------------------------------------------ packed fp32 pairs
-// Blackwell's paired fp32 FMA / multiply / add (fma.rn.f32x2 and friends)
-// process two values per instruction; a pair lives in a 64-bit register.
-
-__device__ __forceinline__ uint64_t pr(float lo, float hi)
-{
-    uint64_t r;
-    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
-    return r;
-}
-
-__device__ __forceinline__ void unpr(uint64_t v, float &lo, float &hi)
-{
-    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
-}
-
-__device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c)
-{
-    uint64_t d;
-    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
-    return d;
-}
-
-__device__ __forceinline__ uint64_t mul2(uint64_t a, uint64_t b)
-{
-    uint64_t d;
-    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
-    return d;
-}
-
-__device__ __forceinline__ uint64_t add2(uint64_t a, uint64_t b)
-{
-    uint64_t d;
-    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
-    return d;
-}
-
 // RoPE on a bf16 pair: for each half, y * c + yp * sn with a single rounding
 // (the product yp * sn of two bf16 values is exact in fp32, formed as an FMA
 // with -0 so that a zero product keeps its sign).  The operands stay bf16:
@@ -240,66 +198,6 @@ __device__ __forceinline__ uint64_t rope_bf2(uint32_t y, uint32_t c, uint32_t yp
         : "=f"(lo), "=f"(hi)
         : "r"(y), "r"(c), "r"(yp), "r"(sn));
     return pr(lo, hi);
-}
-
-// bf16 pair (element 2j in the low half) -> fp32 pair, exactly
-__device__ __forceinline__ uint64_t bf2_to_f2(uint32_t w) { return pr(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u)); }
-
-// fp32 pair -> bf16 pair, round to nearest even
-__device__ __forceinline__ uint32_t f2_to_bf2(uint64_t v)
-{
-    float lo, hi;
-    unpr(v, lo, hi);
-    return pack_bf16x2(lo, hi);
-}
-
-// |w| clamped to the bf16 pair `bound` per half, sign and NaN kept
-__device__ __forceinline__ uint32_t clamp_bf2(uint32_t w, uint32_t bound)
-{
-    uint32_t d;
-    asm("min.NaN.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(w), "r"(bound));
-    return d;
-}
-
-// e4m3 codes of x / s for the 8 bf16 values in `v` (two 4-code words).
-// x is first clamped in magnitude to `bound` (a bf16 value >= 448 s, just
-// above 512 s: every clamped quotient still saturates, and x * n cannot
-// overflow).  With n = -RN(1/s), Markstein's FMA correction
-//   p0 = x n,  e = p0 s + x (exact),  p = p0 + e n
-// gives p = -RN(x / s) whenever |x| and |x / s| are at least 2^-90 (below,
-// the residual underflows, and such quotients encode to a signed zero either
-// way).  The saturating RNE pack of p, with every sign bit flipped, is the
-// code of the IEEE quotient x / s; NaN inputs come out as the NaN code 0xFF.
-// Four e4m3 codes in one word, element order a b c d from the low byte up,
-// RNE with saturation, every sign bit flipped.
-__device__ __forceinline__ uint32_t neg_e4m3x4(uint64_t ab, uint64_t cd)
-{
-    float a, b, c, d;
-    unpr(ab, a, b);
-    unpr(cd, c, d);
-    uint32_t w;
-    asm("{\n\t.reg .b16 lo, hi;\n\t"
-        "cvt.rn.satfinite.e4m3x2.f32 lo, %2, %1;\n\t"
-        "cvt.rn.satfinite.e4m3x2.f32 hi, %4, %3;\n\t"
-        "mov.b32 %0, {lo, hi};\n\t}"
-        : "=r"(w)
-        : "f"(a), "f"(b), "f"(c), "f"(d));
-    return w ^ 0x80808080u;
-}
-
-__device__ __forceinline__ uint2 quantise8(const uint4 &v, uint32_t bound, uint64_t s2, uint64_t n2)
-{
-    const uint32_t w[4] = {clamp_bf2(v.x, bound), clamp_bf2(v.y, bound), clamp_bf2(v.z, bound),
-                           clamp_bf2(v.w, bound)};
-    uint64_t p[4];
-#pragma unroll
-    for (int j = 0; j < 4; j++) {
-        const uint64_t x = bf2_to_f2(w[j]);
-        const uint64_t p0 = mul2(x, n2);
-        const uint64_t e = fma2(p0, s2, x);
-        p[j] = fma2(e, n2, p0);
-    }
-    return make_uint2(neg_e4m3x4(p[0], p[1]), neg_e4m3x4(p[2], p[3]));
 }
 
 // Shared-memory layout (dynamic): barriers and headers, per-layer tables,
@@ -555,21 +453,14 @@ __global__ void __launch_bounds__(kThreads, 2) ctx_kv_tma_kernel(const TmaParams
                 vs = __ldg(reinterpret_cast<const float *>(
                     __ldg(reinterpret_cast<const unsigned long long *>(p.v_scales) + l)));
             }
-            // bound: the smallest bf16 >= 512 s, as a bf16 pair
-            auto bound = [](float sc) {
-                uint32_t u = __float_as_uint(512.0f * sc);
-                if (u & 0xffffu)
-                    u = (u & 0xffff0000u) + 0x10000u;
-                return (u >> 16) * 0x10001u;
-            };
             const float kn = -__frcp_rn(ks), vn = -__frcp_rn(vs);
             uint32_t *e = scl + 12 * l;
             e[0] = e[1] = __float_as_uint(ks);
             e[2] = e[3] = __float_as_uint(vs);
             e[4] = e[5] = __float_as_uint(kn);
             e[6] = e[7] = __float_as_uint(vn);
-            e[8] = bound(ks);
-            e[9] = bound(vs);
+            e[8] = fp8_bound_pair(ks);
+            e[9] = fp8_bound_pair(vs);
         }
         asm volatile("bar.sync 1, %0;" ::"n"(32 * kConsumerWarps) : "memory");
 

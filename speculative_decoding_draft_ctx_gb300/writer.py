@@ -13,7 +13,8 @@ from __future__ import annotations
 
 from ._binding import (
     HEAD_DIM, DSparkError, Tables, cache_desc, dspark_ctx_kv_rotary_dims_supported,
-    dspark_ctx_kv_validate_layers, dspark_ctx_kv_write, dspark_ctx_kv_write_ex, kv_dtype_code,
+    dspark_ctx_kv_validate_layers, dspark_ctx_kv_write, dspark_ctx_kv_write_ex, dspark_qknorm_rope_kv_insert,
+    kv_dtype_code,
 )
 
 
@@ -79,3 +80,38 @@ class ContextKVWriter:
             dspark_ctx_kv_write(*args, stream=stream)
         else:
             dspark_ctx_kv_write_ex(*args, error_flags, stream=stream)
+
+
+def qknorm_rope_kv_insert(qkv, q_norm_weight, k_norm_weight, cos_sin_cache, positions, num_heads,
+                          num_kv_heads, rotary_dim, eps, slot_mapping=None, kv_cache=None,
+                          k_scale=None, v_scale=None, q_fp8_out=None, q_fp8_scale=1.0,
+                          error_flags=None, stream=None):
+    """The draft tokens' fused QK-norm / RoPE on ``qkv`` (in place), also
+    storing their K/V (DSpark draft model page, dspark_qknorm_rope_kv_insert).
+
+    ``qkv``: bf16 ``[T, (num_heads + 2 num_kv_heads) * 128]``.  With
+    ``slot_mapping`` and ``kv_cache`` (``[num_blocks, num_kv_heads,
+    block_size, 256]``, bf16 or uint8 for fp8 e4m3 with the fp32 CUDA scalars
+    ``k_scale`` / ``v_scale``) every token with a slot has its K'|V rows
+    inserted; ``q_fp8_out`` (uint8 ``[T, num_heads * 128]``) receives
+    e4m3(q' / q_fp8_scale).  The block size and the cache dtype are read from
+    ``kv_cache``.
+    """
+    import torch
+
+    T = qkv.shape[0]
+    if qkv.dim() != 2 or qkv.shape[1] != (num_heads + 2 * num_kv_heads) * HEAD_DIM:
+        raise DSparkError(1, f"qkv shape {tuple(qkv.shape)} does not match {num_heads}+2x{num_kv_heads} heads")
+    if (slot_mapping is None) != (kv_cache is None):
+        raise DSparkError(1, "slot_mapping and kv_cache go together")
+    num_blocks = block_size = 0
+    dtype = "auto"
+    if kv_cache is not None:
+        num_blocks, nkv, block_size = (int(x) for x in kv_cache.shape[:3])
+        if nkv != num_kv_heads or kv_cache.shape[3] != 2 * HEAD_DIM:
+            raise DSparkError(1, f"kv_cache shape {tuple(kv_cache.shape)} does not match {num_kv_heads} KV heads")
+        dtype = "fp8" if kv_cache.dtype == torch.uint8 else "auto"
+    dspark_qknorm_rope_kv_insert(qkv, q_norm_weight, k_norm_weight, cos_sin_cache, cos_sin_cache.shape[0],
+                                 positions, T, num_heads, num_kv_heads, rotary_dim, eps, slot_mapping,
+                                 kv_cache, num_blocks, block_size, dtype, k_scale, v_scale, q_fp8_out,
+                                 q_fp8_scale, error_flags, stream)

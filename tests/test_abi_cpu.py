@@ -156,3 +156,53 @@ def test_tables_reject_bad_arguments_without_device(L):
     assert L.dspark_ctx_kv_tables_update(None, None, 2, None, None, None) == dk.STATUS_CODE["DSPARK_ERR_INVALID_ARG"]
     assert L.dspark_ctx_kv_tables_builds(None) == 0
     L.dspark_ctx_kv_tables_destroy(None)
+
+
+# ------------------------------------------------------------ draft-token QK insert
+# (DSpark draft model page, dspark_qknorm_rope_kv_insert; layout and fp8 rules
+# of the context-KV writer page)
+
+def qk_call(expect_ok=False, **over):
+    a = dict(qkv=FAKE, q_norm_w=FAKE, k_norm_w=FAKE, cos_sin=FAKE, max_pos=64, positions=FAKE, num_tokens=7,
+             num_heads=4, num_kv_heads=1, rotary_dim=64, eps=1e-6, slot_mapping=FAKE, kv_cache=FAKE,
+             num_blocks=4, block_size=16, kv_dtype=0, k_scale=None, v_scale=None, q_fp8_out=None,
+             q_fp8_scale=1.0)
+    a.update(over)
+    if expect_ok:
+        dk.dspark_qknorm_rope_kv_insert(**a, stream=0)
+        return "DSPARK_OK"
+    with pytest.raises(dk.DSparkError) as ei:
+        dk.dspark_qknorm_rope_kv_insert(**a, stream=0)
+    return ei.value.name
+
+
+def test_qk_insert_argument_checks(L):
+    assert qk_call(rotary_dim=48) == "DSPARK_ERR_UNSUPPORTED_ROTARY_DIM"
+    assert qk_call(num_tokens=-1) == "DSPARK_ERR_INVALID_ARG"
+    assert qk_call(num_heads=0) == "DSPARK_ERR_INVALID_ARG"
+    assert qk_call(num_kv_heads=0) == "DSPARK_ERR_INVALID_ARG"
+    assert qk_call(max_pos=0) == "DSPARK_ERR_INVALID_ARG"
+    assert qk_call(eps=float("nan")) == "DSPARK_ERR_INVALID_ARG"
+    assert qk_call(eps=-1.0) == "DSPARK_ERR_INVALID_ARG"
+    assert qk_call(block_size=24) == "DSPARK_ERR_BLOCK_SIZE"
+    assert qk_call(kv_dtype=7) == "DSPARK_ERR_DTYPE"
+    assert qk_call(num_blocks=0) == "DSPARK_ERR_INVALID_ARG"
+    # the insert needs both a slot mapping and a cache
+    assert qk_call(kv_cache=None) == "DSPARK_ERR_INVALID_ARG"
+    assert qk_call(slot_mapping=None) == "DSPARK_ERR_INVALID_ARG"
+    assert qk_call(q_fp8_out=FAKE, q_fp8_scale=0.0) == "DSPARK_ERR_INVALID_ARG"
+    assert qk_call(q_fp8_out=FAKE, q_fp8_scale=float("inf")) == "DSPARK_ERR_INVALID_ARG"
+    assert qk_call(qkv=None) == "DSPARK_ERR_INVALID_ARG"
+    assert qk_call(positions=None) == "DSPARK_ERR_INVALID_ARG"
+    assert qk_call(qkv=FAKE + 8) == "DSPARK_ERR_ALIGNMENT"
+    assert qk_call(kv_cache=FAKE + 8) == "DSPARK_ERR_ALIGNMENT"
+    assert qk_call(q_fp8_out=FAKE + 8) == "DSPARK_ERR_ALIGNMENT"
+    assert qk_call(positions=FAKE + 4) == "DSPARK_ERR_ALIGNMENT"
+    assert qk_call(error_flags=FAKE + 2) == "DSPARK_ERR_ALIGNMENT"
+    # without an insert the cache arguments are not looked at
+    assert qk_call(slot_mapping=None, kv_cache=None, block_size=24, kv_dtype=7, num_tokens=0,
+                   expect_ok=True) == "DSPARK_OK"
+    # no tokens: OK without a launch
+    assert qk_call(num_tokens=0, expect_ok=True) == "DSPARK_OK"
+    assert qk_call(rotary_dim=48) == "DSPARK_ERR_UNSUPPORTED_ROTARY_DIM"
+    assert "not in {16, 32, 64}" in dk.dspark_ctx_kv_last_error()

@@ -175,11 +175,13 @@ def make_qk_cache(wl: QkWorkload, device="cpu", fill: int | None = PREFILL_BYTE)
     return c
 
 
-def qk_compulsory_bytes(wl: QkWorkload, num_valid_tokens: int) -> int:
-    """Bytes one call must move at least: qkv read once; query and key heads
-    written back; the K|V cache rows of valid tokens; the fp8 query output;
-    per token its position, slot and cos|sin row; the two norm weights."""
-    T, Hq, Hkv = wl.num_tokens, wl.num_heads, wl.num_kv_heads
+def qk_compulsory_bytes(wl: QkWorkload, num_valid_tokens: int, num_tokens: int | None = None) -> int:
+    """Bytes one call (or its first ``num_tokens`` tokens) must move at least:
+    qkv read once; query and key heads written back; the K|V cache rows of
+    valid tokens; the fp8 query output; per token its position, slot and
+    cos|sin row; the two norm weights."""
+    T = wl.num_tokens if num_tokens is None else num_tokens
+    Hq, Hkv = wl.num_heads, wl.num_kv_heads
     read = T * wl.width * 2
     back = T * (Hq + Hkv) * HEAD_DIM * 2
     cache = num_valid_tokens * Hkv * ROW_ELEMS * wl.elem_size

@@ -101,6 +101,8 @@ def lib():
         L.dspark_oracle_write.restype = ctypes.c_int
         L.dspark_oracle_rows.argtypes = [P, P, ctypes.c_int64, P, P, P, P, ctypes.c_int64, P]
         L.dspark_oracle_rows.restype = ctypes.c_int
+        L.dspark_oracle_bf16_rne_array.argtypes = [P, P, ctypes.c_int64]
+        L.dspark_oracle_bf16_rne_array.restype = None
         L.dspark_oracle_qk_check.argtypes = [P, ctypes.c_int, ctypes.c_int]
         L.dspark_oracle_qk_check.restype = ctypes.c_int
         L.dspark_oracle_qk_insert.argtypes = [P, ctypes.c_int64, ctypes.c_int64, P, P, P, P, P, P,
@@ -144,6 +146,29 @@ def e4m3_rne_sat(x: float) -> int:
 
 
 # ---------------------------------------------------------------- steps
+
+def bf16_rne_array(x: np.ndarray) -> np.ndarray:
+    """bf16 codes (RNE) of fp64 values, elementwise."""
+    a = np.ascontiguousarray(x, dtype=np.float64)
+    out = np.empty(a.shape, np.uint16)
+    lib().dspark_oracle_bf16_rne_array(_ptr(a), _ptr(out), a.size)
+    return out
+
+
+def bf16_values(bits: np.ndarray) -> np.ndarray:
+    """Exact fp64 values of bf16 codes (a bf16 code is the top half of an fp32)."""
+    b = np.ascontiguousarray(bits, dtype=np.uint16)
+    return (b.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+def project_context_kv(x_bits: np.ndarray, w_bits: np.ndarray) -> np.ndarray:
+    """The fused context-KV projection: all_kv[t, n] = bf16(sum_k x[t, k] w[n, k]),
+    the sum exact up to fp64 rounding (an fp64 matmul), one rounding to bf16.
+    x_bits: [T, hidden], w_bits: [N, hidden] (bf16 codes); returns [T, N] codes."""
+    x = bf16_values(x_bits)
+    w = bf16_values(w_bits)
+    return bf16_rne_array(x @ w.T)
+
 
 def gemma_knorm(k_bits: np.ndarray, w_bits: np.ndarray, eps: float):
     """Step 2 on one 128-element K row (bf16 bits) -> (y, y_alt, n_ambiguous)."""

@@ -464,3 +464,16 @@ int dspark_oracle_rows(const dspark_oracle_inputs *in, const int64_t *row_ids, i
         *n_alt = total_alt;
     return total_alt > alt_cap ? ORACLE_ERR_ALT_CAP : ORACLE_OK;
 }
+
+/* ------------------------------------------------------------------ */
+/* The fused context-KV projection's output (DSpark draft model page,
+ * precompute_and_store_context_kv: all_kv = _project_context_kv_token_major
+ * (context_states, ...), "the fused projection output all_kv [num_ctx, L, 2,
+ * nkv, 128]" of the context-KV writer page): every element is the exact dot
+ * product of a context-state row and a weight row (computed by the caller in
+ * fp64), rounded once to bf16.  n values in, n bf16 codes out. */
+void dspark_oracle_bf16_rne_array(const double *x, uint16_t *out, int64_t n)
+{
+    for (int64_t i = 0; i < n; i++)
+        out[i] = dspark_oracle_bf16_rne(x[i]);
+}

@@ -10,3 +10,6 @@ from .qk_insert import (  # noqa: F401
     QUERY_ROWS_PER_REQUEST, QkWorkload, QK_WORKLOADS, QK_WORKLOADS_BY_NAME, QkInputs, generate_qk,
     make_qk_cache, qk_compulsory_bytes, describe_qk,
 )
+from .proj import (  # noqa: F401
+    ProjWorkload, PROJ_WORKLOADS, PROJ_WORKLOADS_BY_NAME, ProjInputs, generate_proj, proj_flops, with_all_kv,
+)

@@ -208,19 +208,24 @@ def _positions_and_slots(wl: Workload, g: torch.Generator):
     return pos.contiguous(), slots.contiguous()
 
 
-def generate(wl: Workload, seed: int | None = None) -> Inputs:
+def generate(wl: Workload, seed: int | None = None, with_all_kv: bool = True) -> Inputs:
     """Draw the inputs of ``wl`` from a seeded torch CPU generator (fp32
-    samples rounded to bf16 with round-to-nearest-even)."""
+    samples rounded to bf16 with round-to-nearest-even).  ``with_all_kv=False``
+    skips the K/V draw (``all_kv`` is then an empty tensor): the caller
+    computes it, e.g. from a projection."""
     g = torch.Generator().manual_seed(wl.seed if seed is None else seed)
     T, L, H = wl.num_ctx, wl.num_layers, wl.num_kv_heads
-    kv = torch.randn((T, L, 2, H, HEAD_DIM), generator=g, dtype=torch.float32)
-    if wl.kv_std != 1.0:
-        kv.mul_(wl.kv_std)
-    if wl.outlier_frac > 0:
-        hit = torch.rand(kv.shape, generator=g) < wl.outlier_frac
-        kv = torch.where(hit, kv * wl.outlier_mult, kv)
-    all_kv = kv.to(torch.bfloat16).contiguous()
-    del kv
+    if with_all_kv:
+        kv = torch.randn((T, L, 2, H, HEAD_DIM), generator=g, dtype=torch.float32)
+        if wl.kv_std != 1.0:
+            kv.mul_(wl.kv_std)
+        if wl.outlier_frac > 0:
+            hit = torch.rand(kv.shape, generator=g) < wl.outlier_frac
+            kv = torch.where(hit, kv * wl.outlier_mult, kv)
+        all_kv = kv.to(torch.bfloat16).contiguous()
+        del kv
+    else:
+        all_kv = torch.empty((0,), dtype=torch.bfloat16)
     knorm_w = (torch.randn((L, HEAD_DIM), generator=g) * wl.w_std).to(torch.bfloat16).contiguous()
     pos, slots = _positions_and_slots(wl, g)
     cos_sin = rope_cos_sin_cache(wl.max_pos, wl.rotary_dim, wl.rope_theta)

@@ -46,6 +46,7 @@ KERNEL_SRCS = [os.path.join(ROOT, "speculative_decoding_draft_ctx_gb300", "csrc"
                for f in ("ctx_kv_tma.cu", "ctx_kv_kernel.cu", "ctx_kv_api.cpp", "ctx_kv_internal.h",
                          "ctx_kv_device.cuh")]
 QK_METRIC = "draft-token QK-norm/RoPE/KV-insert GB/s on 1 GB300; % of HBM roofline"
+PROJ_METRIC = "fused context-KV projection + write TFLOP/s on 1 GB300; % of bf16 tensor roofline"
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "ncu_traffic.json")
 FALLBACK_HBM_GBS = 6800.0
 
@@ -57,8 +58,10 @@ def parse_args(argv=None):
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--config", default="long_context",
-                    choices=[w.name for w in wk.WORKLOADS] + [w.name for w in wk.QK_WORKLOADS],
-                    help="a context-KV write workload, or a qk_* workload of the draft-token QK insert")
+                    choices=[w.name for w in wk.WORKLOADS] + [w.name for w in wk.QK_WORKLOADS] +
+                    [w.name for w in wk.PROJ_WORKLOADS],
+                    help="a context-KV write workload, a qk_* workload of the draft-token QK insert, or a "
+                         "proj_* workload of the projection with the write fused into it")
     ap.add_argument("--e2e-steps", type=int, default=30)
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="oracle sample budget")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -119,14 +122,14 @@ def replica_seed(wl: wk.Workload, rank: int, index: int = 0) -> int:
     return wl.seed + 1000 * rank + index
 
 
-def measured_peaks():
+def measured_peaks(key: str = "hbm_gbs"):
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
         with open(path) as f:
             d = json.load(f)
-        return float(d["hbm_gbs"]), "measured"
+        return float(d[key]), "measured"
     except (OSError, KeyError, ValueError):
-        return FALLBACK_HBM_GBS, "fallback"
+        return {"hbm_gbs": FALLBACK_HBM_GBS, "bf16_tflops": 1900.0}[key], "fallback"
 
 
 def kernel_sha() -> str:
@@ -333,6 +336,8 @@ def run_reference(args):
         return 0
     if args.config in wk.QK_WORKLOADS_BY_NAME:
         return run_reference_qk(args)
+    if args.config in wk.PROJ_WORKLOADS_BY_NAME:
+        return run_reference_proj(args)
     wl = select_workload(args)
     inp = wk.generate(wl)
     budget = 90.0  # seconds of oracle work for the whole run
@@ -663,12 +668,215 @@ def run_qk(args):
     return 0
 
 
+def run_proj(args):
+    """The context-KV projection with the write fused into its epilogue: one
+    tensor-core launch per step (all_kv never reaches HBM), input sets
+    rotated so that each step's operands miss L2.  Beside it, timed the same
+    way: the library's projection alone, PyTorch's (cuBLAS) matmul alone, and
+    the unfused path a user would otherwise run (cuBLAS projection, then the
+    library's write kernel)."""
+    import speculative_decoding_draft_ctx_gb300 as dk
+
+    ws, rank, local = dist_env()
+    if not torch.cuda.is_available():
+        raise RuntimeError("bench.py needs a CUDA device")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    pg = None
+    if ws > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl", device_id=dev)
+        pg = dist
+    dk.lib()
+    wl = wk.PROJ_WORKLOADS_BY_NAME[args.config]
+    b = wl.base
+    flops = wk.proj_flops(wl)
+    foot = (b.num_ctx + wl.n_out) * wl.hidden * 2
+    n_sets = max(1, math.ceil(3 * l2_bytes() / foot))
+    sets = [wk.generate_proj(wl, seed=b.seed + 500 + 1000 * rank + i).to(dev) for i in range(n_sets)]
+    d0 = device_inputs_ctx(sets[0].ctx)
+    fp8 = b.kv_dtype == wk.KV_FP8
+    caches = wk.make_caches(b, device=dev, fill=None)
+    writer = dk.ContextKVWriter(caches, d0["k_scales"], d0["v_scales"], "fp8" if fp8 else "auto")
+    stream = torch.cuda.current_stream()
+    all_kv = torch.empty((b.num_ctx, b.num_layers, 2, b.num_kv_heads, 128), dtype=torch.bfloat16, device=dev)
+
+    def fused(i):
+        s_ = sets[i % n_sets]
+        c = s_.ctx
+        writer.project_and_write(s_.x, s_.w_kv, c.knorm_w, c.eps, c.positions, c.cos_sin, b.rotary_dim,
+                                 c.slot_mapping)
+
+    def project_only(i):
+        s_ = sets[i % n_sets]
+        dk.project_context_kv(s_.x, s_.w_kv, b.num_layers, b.num_kv_heads, out=all_kv)
+
+    def cublas_only(i):
+        s_ = sets[i % n_sets]
+        torch.matmul(s_.x, s_.w_kv.t(), out=all_kv.view(b.num_ctx, -1))
+
+    def unfused(i):
+        s_ = sets[i % n_sets]
+        c = s_.ctx
+        torch.matmul(s_.x, s_.w_kv.t(), out=all_kv.view(b.num_ctx, -1))
+        writer(all_kv, c.knorm_w, c.eps, c.positions, c.cos_sin, b.rotary_dim, c.slot_mapping)
+
+    def timed(fn, steps):
+        for i in range(args.warmup):
+            fn(i)
+        torch.cuda.synchronize()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        if pg:
+            pg.barrier()
+        torch.cuda.synchronize()
+        t0.record(stream)
+        for i, (a, z) in enumerate(ev):
+            a.record(stream)
+            fn(i)
+            z.record(stream)
+        t1.record(stream)
+        torch.cuda.synchronize()
+        if pg:
+            pg.barrier()
+        per = sum(a.elapsed_time(z) for a, z in ev) / steps
+        return max_over_ranks(t0.elapsed_time(t1), pg, dev), per
+
+    with ClockSampler(local) as clk:
+        total_ms, fused_ms = timed(fused, args.steps)
+    side_steps = max(10, min(args.steps, 200))
+    _, proj_ms = timed(project_only, side_steps)
+    _, cublas_ms = timed(cublas_only, side_steps)
+    _, unfused_ms = timed(unfused, side_steps)
+    value = whole_job_rate(flops, args.steps, ws, total_ms) / 1e12
+    peak, peak_kind = measured_peaks("bf16_tflops")
+    achieved = flops / (fused_ms * 1e-3) / 1e12
+
+    e2e = None
+    if not args.no_e2e:
+        h_x = sets[0].x.cpu().pin_memory()
+        d = sets[0]
+        flags = torch.zeros(1, dtype=torch.int32, device=dev)
+        h_flags = torch.zeros(1, dtype=torch.int32).pin_memory()
+        ne = max(1, args.e2e_steps)
+
+        def e2e_step():
+            d.x.copy_(h_x, non_blocking=True)
+            c = d.ctx
+            writer.project_and_write(d.x, d.w_kv, c.knorm_w, c.eps, c.positions, c.cos_sin, b.rotary_dim,
+                                     c.slot_mapping, error_flags=flags)
+            h_flags.copy_(flags, non_blocking=True)
+
+        for _ in range(3):
+            e2e_step()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(ne):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        e_ms = max_over_ranks(e0.elapsed_time(e1), pg, dev)
+        if int(h_flags.item()) != 0:
+            raise RuntimeError(f"projection write reported error flags {int(h_flags.item())}")
+        e2e = {"value": whole_job_rate(flops, ne, ws, e_ms) / 1e12, "unit": "TFLOP/s",
+               "h2d_bytes_per_step": h_x.numel() * 2, "d2h_bytes_per_step": 4, "steps": ne,
+               "ms_per_step": e_ms / ne}
+
+    cpu = None
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        n = min(b.num_ctx, 16)
+        dt = proj_oracle_sample(wl, n)
+        cpu = {"value": 2 * n * wl.n_out * wl.hidden / dt / 1e12, "unit": "TFLOP/s", "cores": os.cpu_count(),
+               "kind": "oracle", "seconds": dt,
+               "sample": f"first {n} of {b.num_ctx} tokens: fp64 numpy matmul (BLAS threads) + C write oracle"}
+    if rank == 0:
+        line = {
+            "metric": PROJ_METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": ws, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": dict(wk.describe(b), workload=wl.name, hidden=wl.hidden, n_out=wl.n_out,
+                           parallelism=f"replicas{ws}", input_sets=n_sets, timing="CUDA events per launch",
+                           l2=("inputs larger than L2" if n_sets == 1 else
+                               f"{n_sets} input sets rotated, footprint > 3x L2")),
+            "flops_per_step": flops,
+            "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                         "frac": achieved / peak, "traffic": None, "peak_source": peak_kind},
+            "compare_ms_per_step": {"fused_projection_write": fused_ms, "projection_alone": proj_ms,
+                                    "cublas_matmul_alone": cublas_ms,
+                                    "unfused_cublas_matmul_then_write": unfused_ms},
+            "cpu_baseline": cpu, "e2e": e2e, "clocks": clk.summary(), "gpu_launches": args.steps,
+            "kernel_avg_us": fused_ms * 1e3,
+        }
+        print(json.dumps(line), flush=True)
+    if pg:
+        pg.destroy_process_group()
+    return 0
+
+
+def proj_oracle_sample(wl, n: int) -> float:
+    """Seconds the oracle takes for the projection and write of the first
+    ``n`` tokens of a projection workload (fp64 BLAS matmul + C write)."""
+    import oracle
+
+    b = wl.base
+    inp = wk.generate_proj(wl)
+    bits = lambda t: t.contiguous().view(torch.int16).numpy().view(np.uint16)  # noqa: E731
+    c = inp.ctx
+    sub_ctx = wk.Inputs(b.with_(num_ctx=n), c.all_kv, c.knorm_w, c.positions[:n].contiguous(),
+                        c.slot_mapping[:n].contiguous(), c.cos_sin, c.k_scale, c.v_scale, c.eps)
+    sub = wk.ProjInputs(wl.with_(base=b.with_(num_ctx=n)), inp.x[:n], inp.w_kv, sub_ctx)
+    t = time.perf_counter()
+    kv = oracle.project_context_kv(bits(sub.x), bits(sub.w_kv))
+    pr = oracle.problem_from_inputs(wk.with_all_kv(sub, kv))
+    pr.write(pr.new_caches())
+    return time.perf_counter() - t
+
+
+def run_reference_proj(args):
+    """The reference arm of a projection workload: the oracle on the first
+    tokens of the call per step (fp64 BLAS matmul + the C write oracle)."""
+    wl = wk.PROJ_WORKLOADS_BY_NAME[args.config]
+    b = wl.base
+    per_step = 90.0 / max(1, args.steps + args.warmup)
+    probe = proj_oracle_sample(wl, min(b.num_ctx, 4)) / min(b.num_ctx, 4)
+    n = int(max(1, min(b.num_ctx, per_step / max(probe, 1e-7))))
+    for _ in range(args.warmup):
+        proj_oracle_sample(wl, n)
+    total = sum(proj_oracle_sample(wl, n) for _ in range(args.steps))
+    value = 2 * n * wl.n_out * wl.hidden * args.steps / total / 1e12
+    sample = f"first {n} of {b.num_ctx} tokens per step: fp64 numpy matmul (BLAS threads) + C write oracle"
+    line = {
+        "impl": "reference", "metric": PROJ_METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": dict(wk.describe(b), workload=wl.name, hidden=wl.hidden, sample_tokens=n),
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": os.cpu_count(), "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def device_inputs_ctx(ctx):
+    """Per-layer fp32 scale tensors (one element each) of a device-side
+    context-write input set, like the attention layers' k/v scales."""
+    L = ctx.knorm_w.shape[0]
+    return {"k_scales": [ctx.k_scale[l:l + 1].clone() for l in range(L)],
+            "v_scales": [ctx.v_scale[l:l + 1].clone() for l in range(L)]}
+
+
 def main(argv=None):
     args = parse_args(argv)
     if args.impl == "reference":
         return run_reference(args)
     if args.config in wk.QK_WORKLOADS_BY_NAME:
         return run_qk(args)
+    if args.config in wk.PROJ_WORKLOADS_BY_NAME:
+        return run_proj(args)
     return run_ours(args)
 
 

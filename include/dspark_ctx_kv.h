@@ -116,6 +116,40 @@ int dspark_ctx_kv_write_ex(const void *all_kv, const void *knorm_w, const int64_
                            cudaStream_t stream);
 
 /*
+ * dspark_ctx_kv_project -- the context-KV projection on the tensor cores
+ * (DSpark draft model page, precompute_and_store_context_kv:
+ * all_kv = _project_context_kv_token_major(context_states, ...)):
+ * all_kv_out[t, n] = bf16(sum_k x[t, k] * w_kv[n, k]) with an fp32
+ * accumulator, n = ((l * 2 + kv) * nkv + h) * 128 + d.
+ *
+ *  x           device, bf16 [num_ctx, hidden] contiguous, 16-byte aligned
+ *              (the normed context states).
+ *  w_kv        device, bf16 [L * 2 * nkv * 128, hidden] contiguous, 16-byte
+ *              aligned: the K and V projection rows of every layer.
+ *  all_kv_out  device, bf16 [num_ctx, L, 2, nkv, 128], 16-byte aligned.
+ *  hidden      a positive multiple of 8; 1 <= L * nkv <= 65535;
+ *              num_ctx <= 8,388,480 (0 returns DSPARK_OK without a launch).
+ * One launch; allocates, copies and synchronises nothing (the tensor maps
+ * travel as kernel parameters).
+ */
+int dspark_ctx_kv_project(const void *x, const void *w_kv, void *all_kv_out, int64_t num_ctx, int hidden, int L,
+                          int nkv, cudaStream_t stream);
+
+/*
+ * dspark_ctx_kv_project_write -- the projection with the context-KV write in
+ * its epilogue: the same result as dspark_ctx_kv_project followed by
+ * dspark_ctx_kv_write_ex on its output, in one launch, without all_kv in
+ * device memory.  x, w_kv, num_ctx and hidden as for dspark_ctx_kv_project;
+ * every other argument as for dspark_ctx_kv_write_ex.
+ */
+int dspark_ctx_kv_project_write(const void *x, const void *w_kv, int64_t num_ctx, int hidden, const void *knorm_w,
+                                const int64_t *positions, const int64_t *slot_mapping, const void *cos_sin,
+                                int64_t max_pos, void *layer0_cache, int64_t num_blocks,
+                                const int64_t *cache_offsets, const float *const *k_scales,
+                                const float *const *v_scales, int L, int nkv, int block_size, int rotary_dim,
+                                float eps, int kv_dtype, unsigned int *error_flags, cudaStream_t stream);
+
+/*
  * dspark_qknorm_rope_kv_insert -- the draft tokens' fused QK-norm / RoPE,
  * also storing their K/V (DSpark draft model page,
  * dspark_qknorm_rope_kv_insert; norm, RoPE, cache layout and fp8 rule as in

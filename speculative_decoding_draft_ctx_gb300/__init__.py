@@ -11,6 +11,9 @@ from ._binding import (  # noqa: F401
     CACHE_ROW, EXPORTS, FLAG_POS_RANGE, FLAG_SLOT_RANGE, FLAG_TIMEOUT, HEAD_DIM, KV_BF16, KV_FP8_E4M3, STATUS,
     STATUS_CODE, CacheDesc, DSparkError, Tables, cache_desc, check, dspark_ctx_kv_last_error,
     dspark_ctx_kv_rotary_dims_supported, dspark_ctx_kv_status_string, dspark_ctx_kv_validate_layers,
-    dspark_ctx_kv_write, dspark_ctx_kv_write_ex, dspark_qknorm_rope_kv_insert, kv_dtype_code, lib, library_path,
+    dspark_ctx_kv_write, dspark_ctx_kv_write_ex, dspark_qknorm_rope_kv_insert, dspark_ctx_kv_project,
+    dspark_ctx_kv_project_write, kv_dtype_code, lib, library_path,
 )
-from .writer import ContextKVWriter, qknorm_rope_kv_insert, rotary_dims_supported  # noqa: F401
+from .writer import (  # noqa: F401
+    ContextKVWriter, project_context_kv, qknorm_rope_kv_insert, rotary_dims_supported,
+)

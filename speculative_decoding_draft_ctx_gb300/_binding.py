@@ -37,6 +37,7 @@ EXPORTS = (
     "dspark_ctx_kv_tables_cache_offsets", "dspark_ctx_kv_tables_k_scales",
     "dspark_ctx_kv_tables_v_scales", "dspark_ctx_kv_tables_builds", "dspark_ctx_kv_tables_destroy",
     "dspark_ctx_kv_last_error", "dspark_ctx_kv_status_string", "dspark_qknorm_rope_kv_insert",
+    "dspark_ctx_kv_project", "dspark_ctx_kv_project_write",
 )
 
 
@@ -105,6 +106,11 @@ def lib() -> ctypes.CDLL:
         L.dspark_qknorm_rope_kv_insert.argtypes = [P, P, P, P, I64, P, I64, I, I, I, ctypes.c_float, P, P, I64,
                                                    I, I, P, P, P, ctypes.c_float, P, P]
         L.dspark_qknorm_rope_kv_insert.restype = I
+        L.dspark_ctx_kv_project.argtypes = [P, P, P, I64, I, I, I, P]
+        L.dspark_ctx_kv_project.restype = I
+        L.dspark_ctx_kv_project_write.argtypes = [P, P, I64, I, P, P, P, P, I64, P, I64, P, P, P, I, I, I, I,
+                                                  ctypes.c_float, I, P, P]
+        L.dspark_ctx_kv_project_write.restype = I
         _lib = L
         return L
 
@@ -177,6 +183,23 @@ def dspark_qknorm_rope_kv_insert(qkv, q_norm_w, k_norm_w, cos_sin, max_pos, posi
         _addr(slot_mapping), _addr(kv_cache), int(num_blocks), int(block_size), kv_dtype_code(kv_dtype),
         _addr(k_scale), _addr(v_scale), _addr(q_fp8_out), float(q_fp8_scale), _addr(error_flags),
         _stream(stream)))
+
+
+def dspark_ctx_kv_project(x, w_kv, all_kv_out, num_ctx, hidden, L, nkv, stream=None):
+    """``dspark_ctx_kv_project`` of the C ABI."""
+    check(lib().dspark_ctx_kv_project(_addr(x), _addr(w_kv), _addr(all_kv_out), int(num_ctx), int(hidden),
+                                      int(L), int(nkv), _stream(stream)))
+
+
+def dspark_ctx_kv_project_write(x, w_kv, num_ctx, hidden, knorm_w, positions, slot_mapping, cos_sin, max_pos,
+                                layer0_cache, num_blocks, cache_offsets, k_scales, v_scales, L, nkv, block_size,
+                                rotary_dim, eps, kv_dtype, error_flags=None, stream=None):
+    """``dspark_ctx_kv_project_write`` of the C ABI."""
+    check(lib().dspark_ctx_kv_project_write(
+        _addr(x), _addr(w_kv), int(num_ctx), int(hidden), _addr(knorm_w), _addr(positions), _addr(slot_mapping),
+        _addr(cos_sin), int(max_pos), _addr(layer0_cache), int(num_blocks), _addr(cache_offsets), _addr(k_scales),
+        _addr(v_scales), int(L), int(nkv), int(block_size), int(rotary_dim), float(eps), kv_dtype_code(kv_dtype),
+        _addr(error_flags), _stream(stream)))
 
 
 def dspark_ctx_kv_rotary_dims_supported(rotary_dim: int, head_dim: int) -> bool:

@@ -8,7 +8,9 @@
 // __call__ (num_ctx == 0 launches nothing), rotary_dims_supported (head_dim
 // 128, rotary_dim 16/32/64); DSpark draft model page --
 // dspark_qknorm_rope_kv_insert (the draft tokens' fused QK-norm/RoPE and K/V
-// insert, its insert skipped without a slot mapping).
+// insert, its insert skipped without a slot mapping); precompute_and_store_
+// context_kv (the context states' projection into all_kv, on its own or with
+// the write fused into it).
 #include "../../include/dspark_ctx_kv.h"
 
 #include <cmath>
@@ -248,6 +250,119 @@ int dspark_qknorm_rope_kv_insert(void *qkv, const void *q_norm_w, const void *k_
     cudaError_t e = dspark::launch_qk_insert(p, rotary_dim, fp8, stream);
     if (e != cudaSuccess)
         return fail(DSPARK_ERR_CUDA, "launch failed: %s", cudaGetErrorString(e));
+    return ok();
+}
+
+namespace {
+
+// Shape rules of the tensor-core projection: TMA needs 16-byte aligned bases
+// and rows (hidden a multiple of 8 bf16); the grid holds L * nkv column tiles
+// by ceil(T / 128) row tiles.
+int check_projection(const void *x, const void *w_kv, int64_t num_ctx, int hidden, int L, int nkv)
+{
+    if (num_ctx < 0)
+        return fail(DSPARK_ERR_INVALID_ARG, "num_ctx %lld < 0", (long long)num_ctx);
+    if (L <= 0 || nkv <= 0 || (int64_t)L * nkv > 65535)
+        return fail(DSPARK_ERR_INVALID_ARG, "L=%d nkv=%d: need 1 <= L * nkv <= 65535", L, nkv);
+    if (hidden <= 0 || hidden % 8 != 0)
+        return fail(DSPARK_ERR_ALIGNMENT, "hidden %d must be a positive multiple of 8", hidden);
+    if (num_ctx > (int64_t)65535 * 128)
+        return fail(DSPARK_ERR_INVALID_ARG, "num_ctx %lld above %d", (long long)num_ctx, 65535 * 128);
+    if (num_ctx > 0 && (!x || !w_kv))
+        return fail(DSPARK_ERR_INVALID_ARG, "null x or w_kv");
+    if (num_ctx > 0 && (!aligned(x, 16) || !aligned(w_kv, 16)))
+        return fail(DSPARK_ERR_ALIGNMENT, "x and w_kv must be 16-byte aligned");
+    return DSPARK_OK;
+}
+
+}  // namespace
+
+int dspark_ctx_kv_project(const void *x, const void *w_kv, void *all_kv_out, int64_t num_ctx, int hidden, int L,
+                          int nkv, cudaStream_t stream)
+{
+    int st = check_projection(x, w_kv, num_ctx, hidden, L, nkv);
+    if (st != DSPARK_OK)
+        return st;
+    if (num_ctx == 0)
+        return ok();
+    if (!all_kv_out || !aligned(all_kv_out, 16))
+        return fail(DSPARK_ERR_ALIGNMENT, "all_kv_out must be a 16-byte aligned device buffer");
+    dspark::ProjArgs a{};
+    a.x = static_cast<const uint16_t *>(x);
+    a.w_kv = static_cast<const uint16_t *>(w_kv);
+    a.all_kv_out = static_cast<uint16_t *>(all_kv_out);
+    a.T = num_ctx;
+    a.hidden = hidden;
+    a.L = L;
+    a.nkv = nkv;
+    cudaError_t e = dspark::launch_proj(a, stream);
+    if (e != cudaSuccess)
+        return fail(DSPARK_ERR_CUDA, "projection launch failed: %s", cudaGetErrorString(e));
+    return ok();
+}
+
+int dspark_ctx_kv_project_write(const void *x, const void *w_kv, int64_t num_ctx, int hidden, const void *knorm_w,
+                                const int64_t *positions, const int64_t *slot_mapping, const void *cos_sin,
+                                int64_t max_pos, void *layer0_cache, int64_t num_blocks,
+                                const int64_t *cache_offsets, const float *const *k_scales,
+                                const float *const *v_scales, int L, int nkv, int block_size, int rotary_dim,
+                                float eps, int kv_dtype, unsigned int *error_flags, cudaStream_t stream)
+{
+    int st = check_projection(x, w_kv, num_ctx, hidden, L, nkv);
+    if (st != DSPARK_OK)
+        return st;
+    if (num_blocks <= 0 || max_pos <= 0)
+        return fail(DSPARK_ERR_INVALID_ARG, "num_blocks=%lld max_pos=%lld must be >= 1", (long long)num_blocks,
+                    (long long)max_pos);
+    if (!dspark_ctx_kv_rotary_dims_supported(rotary_dim, DSPARK_HEAD_DIM))
+        return fail(DSPARK_ERR_UNSUPPORTED_ROTARY_DIM, "rotary_dim %d not in {16, 32, 64}", rotary_dim);
+    if (!pow2(block_size))
+        return fail(DSPARK_ERR_BLOCK_SIZE, "block size %d is not a power of two", block_size);
+    if (kv_dtype != DSPARK_KV_BF16 && kv_dtype != DSPARK_KV_FP8_E4M3)
+        return fail(DSPARK_ERR_DTYPE, "kv dtype %d unknown", kv_dtype);
+    if (!(eps >= 0.0f) || std::isinf(eps))
+        return fail(DSPARK_ERR_INVALID_ARG, "eps must be finite and >= 0");
+    const int64_t capacity = num_blocks * (int64_t)block_size;
+    if (capacity / block_size != num_blocks || num_blocks > (INT64_MAX / nkv) / block_size / DSPARK_CACHE_ROW)
+        return fail(DSPARK_ERR_INVALID_ARG, "cache of %lld blocks too large", (long long)num_blocks);
+    if (num_ctx == 0)
+        return ok();
+    if (!knorm_w || !positions || !slot_mapping || !cos_sin || !layer0_cache || !cache_offsets)
+        return fail(DSPARK_ERR_INVALID_ARG, "null buffer pointer");
+    if (kv_dtype == DSPARK_KV_FP8_E4M3 && (!k_scales || !v_scales))
+        return fail(DSPARK_ERR_INVALID_ARG, "fp8 cache needs k_scales and v_scales");
+    if (!aligned(knorm_w, 16) || !aligned(cos_sin, 16) || !aligned(layer0_cache, 16))
+        return fail(DSPARK_ERR_ALIGNMENT, "knorm_w, cos_sin and layer0_cache must be 16-byte aligned");
+    if (!aligned(positions, 8) || !aligned(slot_mapping, 8) || !aligned(cache_offsets, 8) ||
+        (k_scales && !aligned(k_scales, 8)) || (v_scales && !aligned(v_scales, 8)))
+        return fail(DSPARK_ERR_ALIGNMENT, "int64 and pointer tables must be 8-byte aligned");
+    if (error_flags && !aligned(error_flags, 4))
+        return fail(DSPARK_ERR_ALIGNMENT, "error_flags must be 4-byte aligned");
+    dspark::ProjArgs a{};
+    a.x = static_cast<const uint16_t *>(x);
+    a.w_kv = static_cast<const uint16_t *>(w_kv);
+    a.knorm_w = static_cast<const uint16_t *>(knorm_w);
+    a.positions = positions;
+    a.slot_mapping = slot_mapping;
+    a.cos_sin = static_cast<const uint16_t *>(cos_sin);
+    a.cache0 = static_cast<unsigned char *>(layer0_cache);
+    a.cache_offsets = cache_offsets;
+    a.k_scales = k_scales;
+    a.v_scales = v_scales;
+    a.error_flags = error_flags;
+    a.T = num_ctx;
+    a.max_pos = max_pos;
+    a.capacity = capacity;
+    a.hidden = hidden;
+    a.L = L;
+    a.nkv = nkv;
+    a.block_size_log2 = log2_exact(block_size);
+    a.rotary_dim = rotary_dim;
+    a.fp8 = kv_dtype == DSPARK_KV_FP8_E4M3;
+    a.eps = eps;
+    cudaError_t e = dspark::launch_proj(a, stream);
+    if (e != cudaSuccess)
+        return fail(DSPARK_ERR_CUDA, "projection launch failed: %s", cudaGetErrorString(e));
     return ok();
 }
 

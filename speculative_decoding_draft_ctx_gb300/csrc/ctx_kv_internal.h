@@ -69,4 +69,34 @@ struct QkInsertParams {
 
 cudaError_t launch_qk_insert(const QkInsertParams &p, int rotary_dim, bool fp8_cache, cudaStream_t stream);
 
+// Fused context-KV projection (proj_gemm.cu): all_kv = bf16(x w^T) on the
+// tensor cores, stored to all_kv_out, or (all_kv_out null) written straight
+// into the caches by the context-KV write in the GEMM's epilogue.
+struct ProjArgs {
+    const uint16_t *x;           // bf16 [T, hidden]
+    const uint16_t *w_kv;        // bf16 [L * 2 * nkv * 128, hidden]
+    uint16_t *all_kv_out;        // bf16 [T, L * 2 * nkv * 128], or null: write
+    const uint16_t *knorm_w;     // write: bf16 [L, 128]
+    const int64_t *positions;
+    const int64_t *slot_mapping;
+    const uint16_t *cos_sin;
+    unsigned char *cache0;
+    const int64_t *cache_offsets;
+    const float *const *k_scales;
+    const float *const *v_scales;
+    unsigned int *error_flags;
+    int64_t T;
+    int64_t max_pos;
+    int64_t capacity;
+    int32_t hidden;
+    int32_t L;
+    int32_t nkv;
+    int32_t block_size_log2;
+    int32_t rotary_dim;
+    bool fp8;
+    float eps;
+};
+
+cudaError_t launch_proj(const ProjArgs &a, cudaStream_t stream);
+
 }  // namespace dspark

@@ -13,8 +13,8 @@ from __future__ import annotations
 
 from ._binding import (
     HEAD_DIM, DSparkError, Tables, cache_desc, dspark_ctx_kv_rotary_dims_supported,
-    dspark_ctx_kv_validate_layers, dspark_ctx_kv_write, dspark_ctx_kv_write_ex, dspark_qknorm_rope_kv_insert,
-    kv_dtype_code,
+    dspark_ctx_kv_project, dspark_ctx_kv_project_write, dspark_ctx_kv_validate_layers, dspark_ctx_kv_write,
+    dspark_ctx_kv_write_ex, dspark_qknorm_rope_kv_insert, kv_dtype_code,
 )
 
 
@@ -81,6 +81,23 @@ class ContextKVWriter:
         else:
             dspark_ctx_kv_write_ex(*args, error_flags, stream=stream)
 
+    def project_and_write(self, context_states, w_kv, k_norm_weight, eps, positions, cos_sin_cache, rotary_dim,
+                          slot_mapping, stream=None, error_flags=None):
+        """Project the (normed) context states with the stacked K/V weights
+        ``w_kv`` ``[L * 2 * nkv * 128, hidden]`` and write every layer's
+        context K/V in the same launch: all_kv never reaches device memory."""
+        num_ctx, hidden = context_states.shape
+        if w_kv.shape[0] != self.num_layers * 2 * self.num_kv_heads * HEAD_DIM or w_kv.shape[1] != hidden:
+            raise DSparkError(1, f"w_kv shape {tuple(w_kv.shape)} does not match the layers and hidden {hidden}")
+        if num_ctx == 0:
+            return
+        self.ensure_tables(stream)
+        t = self._tables
+        dspark_ctx_kv_project_write(context_states, w_kv, num_ctx, hidden, k_norm_weight, positions, slot_mapping,
+                                    cos_sin_cache, cos_sin_cache.shape[0], self.kv_caches[0], self.num_blocks,
+                                    t.cache_offsets, t.k_scales, t.v_scales, self.num_layers, self.num_kv_heads,
+                                    self.block_size, rotary_dim, eps, self._dtype, error_flags, stream)
+
 
 def qknorm_rope_kv_insert(qkv, q_norm_weight, k_norm_weight, cos_sin_cache, positions, num_heads,
                           num_kv_heads, rotary_dim, eps, slot_mapping=None, kv_cache=None,
@@ -115,3 +132,16 @@ def qknorm_rope_kv_insert(qkv, q_norm_weight, k_norm_weight, cos_sin_cache, posi
                                  positions, T, num_heads, num_kv_heads, rotary_dim, eps, slot_mapping,
                                  kv_cache, num_blocks, block_size, dtype, k_scale, v_scale, q_fp8_out,
                                  q_fp8_scale, error_flags, stream)
+
+
+def project_context_kv(context_states, w_kv, num_layers, num_kv_heads, out=None, stream=None):
+    """all_kv = bf16(context_states @ w_kv^T) as ``[num_ctx, L, 2, nkv, 128]``
+    on the tensor cores (the fused projection the context-KV writer reads)."""
+    import torch
+
+    num_ctx, hidden = context_states.shape
+    if out is None:
+        out = torch.empty((num_ctx, num_layers, 2, num_kv_heads, HEAD_DIM), dtype=torch.bfloat16,
+                          device=context_states.device)
+    dspark_ctx_kv_project(context_states, w_kv, out, num_ctx, hidden, num_layers, num_kv_heads, stream)
+    return out

@@ -1,0 +1,221 @@
+"""GPU parity of the tensor-core context-KV projection and of the projection
+with the write fused into its epilogue (DSpark draft model page,
+precompute_and_store_context_kv: all_kv = the projection of the context
+states, then the fused writer), through the C ABI.
+
+* Exact-integer inputs (x in {-8..8}/8, w in {-8..8}/32): every fp32 partial
+  sum is exact whatever the order of the tensor cores' accumulation, so the
+  bf16 projection is unique -- the projection must equal the oracle's bit
+  for bit, and the fused write must match the oracle's write of the oracle's
+  projection within the write's own tolerance (tests/parity.py).
+* Gaussian inputs: each projected element within |sum of fp32 rounding
+  errors| <= hidden * 2^-24 * sum_k |x_k w_k| (any summation order) plus one
+  bf16 rounding of the exact dot product; and the fused write against the
+  library's own unfused composition (projection, then the write kernel).
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import workloads as wk
+from parity import compare_caches, device_inputs, gpu_write, to_numpy_caches
+
+pytestmark = pytest.mark.gpu
+
+
+def bits(x: torch.Tensor) -> np.ndarray:
+    return x.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
+
+
+def proj_workload(name, recipe="int", **base_over):
+    wl = wk.PROJ_WORKLOADS_BY_NAME[name].with_(recipe=recipe)
+    if base_over:
+        wl = wl.with_(base=wl.base.with_(**base_over))
+    return wl
+
+
+def gpu_project(inp: wk.ProjInputs):
+    import speculative_decoding_draft_ctx_gb300 as dk
+
+    b = inp.workload.base
+    x, w = inp.x.cuda(), inp.w_kv.cuda()
+    out = dk.project_context_kv(x, w, b.num_layers, b.num_kv_heads)
+    torch.cuda.synchronize()
+    return out
+
+
+def gpu_project_write(inp: wk.ProjInputs, flags=None):
+    import speculative_decoding_draft_ctx_gb300 as dk
+
+    b = inp.workload.base
+    d = device_inputs(inp.ctx)
+    caches = wk.make_caches(b, device="cuda")
+    w = dk.ContextKVWriter(caches, d.extra["k_scales"], d.extra["v_scales"],
+                           "fp8" if b.kv_dtype == wk.KV_FP8 else "auto")
+    w.project_and_write(inp.x.cuda(), inp.w_kv.cuda(), d.knorm_w, d.eps, d.positions, d.cos_sin, b.rotary_dim,
+                        d.slot_mapping, error_flags=flags)
+    torch.cuda.synchronize()
+    return caches
+
+
+PROJ_SHAPES = [
+    # (base workload, overrides, hidden)
+    ("proj_tiny", {}, 256),
+    ("proj_draft_step", {}, 4096),
+    ("proj_draft_step", {"num_ctx": 200, "pad_count": 9}, 136),       # a ragged row tile and a ragged k-block
+    ("proj_draft_step", {"num_ctx": 129, "num_layers": 2, "num_kv_heads": 3, "pad_count": 4}, 72),
+    ("proj_prefill_fp8", {}, 512),
+]
+
+
+@pytest.mark.parametrize("name,over,hidden", PROJ_SHAPES)
+def test_projection_bit_exact_on_exact_inputs(oracle_lib, name, over, hidden):
+    wl = proj_workload(name, **over).with_(hidden=hidden)
+    inp = wk.generate_proj(wl)
+    got = bits(gpu_project(inp)).reshape(wl.base.num_ctx, -1)
+    ref = oracle_lib.project_context_kv(bits(inp.x), bits(inp.w_kv))
+    bad = np.argwhere(got != ref)
+    assert len(bad) == 0, (len(bad), bad[:5].tolist())
+
+
+def test_projection_gaussian_within_the_fp32_bound(oracle_lib):
+    wl = proj_workload("proj_draft_step", recipe="gauss", num_ctx=256, pad_count=5)
+    inp = wk.generate_proj(wl)
+    got = oracle_lib.bf16_values(bits(gpu_project(inp)).reshape(wl.base.num_ctx, -1))
+    x = oracle_lib.bf16_values(bits(inp.x))
+    w = oracle_lib.bf16_values(bits(inp.w_kv))
+    exact = x @ w.T
+    bound = wl.hidden * 2.0**-24 / (1 - wl.hidden * 2.0**-24) * (np.abs(x) @ np.abs(w).T)
+    # one bf16 rounding: half a bf16 ulp of the value (2^-8 relative), doubled for slack at binade edges
+    ulp = np.abs(exact) * 2.0**-7 + 2.0**-133
+    err = np.abs(got - exact)
+    assert (err <= bound + ulp).all(), float((err - bound - ulp).max())
+    # and most elements are the correctly rounded bf16 of the exact dot product
+    ref = oracle_lib.bf16_values(oracle_lib.bf16_rne_array(exact))
+    assert (got == ref).mean() > 0.995
+
+
+FUSED = [
+    ("proj_tiny", {}, 256),
+    ("proj_draft_step", {}, 4096),
+    ("proj_draft_step_fp8", {}, 4096),
+    ("proj_draft_step", {"num_ctx": 200, "pad_count": 9, "rotary_dim": 16}, 136),
+    ("proj_draft_step_fp8", {"num_ctx": 333, "num_layers": 3, "num_kv_heads": 5, "rotary_dim": 32,
+                             "block_size": 4, "num_blocks": 2048, "pad_count": 20}, 264),
+]
+
+
+@pytest.mark.parametrize("name,over,hidden", FUSED)
+def test_fused_write_matches_the_oracle_on_exact_inputs(oracle_lib, name, over, hidden):
+    wl = proj_workload(name, **over).with_(hidden=hidden)
+    inp = wk.generate_proj(wl)
+    b = wl.base
+    fp8 = b.kv_dtype == wk.KV_FP8
+    caches = gpu_project_write(inp)
+    all_kv = oracle_lib.project_context_kv(bits(inp.x), bits(inp.w_kv))
+    ctx = wk.with_all_kv(inp, all_kv)
+    p = oracle_lib.problem_from_inputs(ctx)
+    ora = p.new_caches()
+    alts = p.write(ora)
+    problems = compare_caches(to_numpy_caches(caches, fp8), ora, alts, fp8)
+    assert not problems, problems
+
+
+def test_fused_write_full_prefill_sampled(oracle_lib):
+    """Prefill fp8 at full size (8192 tokens, hidden 4096): every written row
+    of 512 sampled tokens against the oracle, and nothing else written."""
+    wl = proj_workload("proj_prefill_fp8")
+    inp = wk.generate_proj(wl)
+    b = wl.base
+    caches = gpu_project_write(inp)
+    g = to_numpy_caches(caches, True)
+    rng = np.random.default_rng(7)
+    toks = np.sort(rng.choice(b.num_ctx, 512, replace=False))
+    all_kv = oracle_lib.project_context_kv(bits(inp.x[toks]), bits(inp.w_kv))
+    sub = wk.Inputs(b.with_(num_ctx=len(toks)),
+                    torch.from_numpy(all_kv.view(np.int16)).view(torch.bfloat16).reshape(
+                        len(toks), b.num_layers, 2, b.num_kv_heads, 128),
+                    inp.ctx.knorm_w, inp.ctx.positions[toks].contiguous(), inp.ctx.slot_mapping[toks].contiguous(),
+                    inp.ctx.cos_sin, inp.ctx.k_scale, inp.ctx.v_scale, inp.ctx.eps)
+    p = oracle_lib.problem_from_inputs(sub)
+    ids = np.arange(len(toks) * b.num_layers * b.num_kv_heads, dtype=np.int64)
+    rows, (ar, ad, av) = p.rows(ids)
+    dest = p.dest_rows(ids)
+    keep = dest >= 0
+    from parity import compare_rows
+
+    for l in range(b.num_layers):
+        sel = keep & ((ids // b.num_kv_heads) % b.num_layers == l)
+        idx = {}
+        pos_of = {int(i): k for k, i in enumerate(np.nonzero(sel)[0])}
+        for r, dm, v in zip(ar.tolist(), ad.tolist(), av.tolist()):
+            if r in pos_of:
+                idx.setdefault((pos_of[r], dm), []).append(v)
+        gl = g[l].reshape(-1, 256)[dest[sel]]
+        bad = compare_rows(gl, rows[sel], idx, True)
+        assert not bad, (l, len(bad), bad[:5])
+    # exactly the valid tokens' rows were written
+    valid = int((inp.ctx.slot_mapping >= 0).sum())
+    for l in range(b.num_layers):
+        written = (~(g[l].reshape(-1, 256) == 0xFF).all(axis=1)).sum()
+        assert written == valid * b.num_kv_heads
+
+
+@pytest.mark.parametrize("name", ["proj_draft_step", "proj_draft_step_fp8"])
+def test_fused_write_gaussian_equals_unfused_composition(oracle_lib, name):
+    """Gaussian inputs: the fused launch against the library's projection
+    followed by its write kernel (the same bf16 all_kv).  The two sum the
+    squares of a row in different fp32 orders, so a normed value may differ
+    by one bf16 ulp, and a rotated output where y c and y' s nearly cancel
+    then differs by several of its own ulps; the bound is therefore taken at
+    the row's scale: V exact (bf16) or within one code (fp8); K equal in all
+    but a few elements, every difference below 2^-6 of the row's largest
+    magnitude (or, in an fp8 cache, one code)."""
+    wl = proj_workload(name, recipe="gauss")
+    inp = wk.generate_proj(wl)
+    b = wl.base
+    fp8 = b.kv_dtype == wk.KV_FP8
+    fused = to_numpy_caches(gpu_project_write(inp), fp8)
+    all_kv = gpu_project(inp).cpu()
+    ctx = wk.Inputs(b, all_kv.reshape(b.num_ctx, b.num_layers, 2, b.num_kv_heads, 128), inp.ctx.knorm_w,
+                    inp.ctx.positions, inp.ctx.slot_mapping, inp.ctx.cos_sin, inp.ctx.k_scale, inp.ctx.v_scale,
+                    inp.ctx.eps)
+    unfused, _, _ = gpu_write(ctx)
+    unfused = to_numpy_caches(unfused, fp8)
+    sign = 0x80 if fp8 else 0x8000
+    for f, u in zip(fused, unfused):
+        f, u = f.reshape(-1, 256), u.reshape(-1, 256)
+        fo = np.where(f & sign, -(f & (sign - 1)).astype(np.int64), (f & (sign - 1)).astype(np.int64))
+        uo = np.where(u & sign, -(u & (sign - 1)).astype(np.int64), (u & (sign - 1)).astype(np.int64))
+        d = np.abs(fo - uo)
+        if fp8:
+            assert d[:, 128:].max() <= 1
+            fv = np.array([oracle_lib.e4m3_decode(c) for c in range(256)])[f[:, :128]]
+            uv = np.array([oracle_lib.e4m3_decode(c) for c in range(256)])[u[:, :128]]
+        else:
+            assert d[:, 128:].max() == 0
+            fv, uv = oracle_lib.bf16_values(f[:, :128]), oracle_lib.bf16_values(u[:, :128])
+        written = ~(u == (0xFF if fp8 else 0xFFFF)).all(axis=1)
+        scale = np.abs(uv[written]).max(axis=1, keepdims=True)
+        near = np.abs(fv[written] - uv[written]) <= scale * 2.0**-6
+        if fp8:  # a bf16 ulp of K' may also move an e4m3 code across its rounding boundary
+            near |= d[written, :128] <= 1
+        assert near.all()
+        assert (d[written, :128] == 0).mean() > 0.999
+
+
+def test_fused_write_flags_out_of_range_rows(oracle_lib):
+    import speculative_decoding_draft_ctx_gb300 as dk
+
+    wl = proj_workload("proj_draft_step", num_ctx=130, pad_count=0)
+    inp = wk.generate_proj(wl)
+    inp.ctx.slot_mapping[3] = wl.base.capacity
+    inp.ctx.positions[129] = wl.base.max_pos
+    flags = torch.zeros(1, dtype=torch.int32, device="cuda")
+    caches = gpu_project_write(inp, flags=flags)
+    assert int(flags.item()) == dk.FLAG_SLOT_RANGE | dk.FLAG_POS_RANGE
+    g = to_numpy_caches(caches, False)
+    for c in g:
+        written = (~(c.reshape(-1, 256) == 0xFFFF).all(axis=1)).sum()
+        assert written == (130 - 2) * wl.base.num_kv_heads

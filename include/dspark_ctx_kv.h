@@ -140,7 +140,7 @@ int dspark_ctx_kv_project(const void *x, const void *w_kv, void *all_kv_out, int
  * its epilogue: the same result as dspark_ctx_kv_project followed by
  * dspark_ctx_kv_write_ex on its output, in one launch, without all_kv in
  * device memory.  x, w_kv, num_ctx and hidden as for dspark_ctx_kv_project;
- * every other argument as for dspark_ctx_kv_write_ex.
+ * every other argument as for dspark_ctx_kv_write_ex; L <= 32.
  */
 int dspark_ctx_kv_project_write(const void *x, const void *w_kv, int64_t num_ctx, int hidden, const void *knorm_w,
                                 const int64_t *positions, const int64_t *slot_mapping, const void *cos_sin,

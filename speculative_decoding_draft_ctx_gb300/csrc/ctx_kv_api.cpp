@@ -322,6 +322,8 @@ int dspark_ctx_kv_project_write(const void *x, const void *w_kv, int64_t num_ctx
         return fail(DSPARK_ERR_DTYPE, "kv dtype %d unknown", kv_dtype);
     if (!(eps >= 0.0f) || std::isinf(eps))
         return fail(DSPARK_ERR_INVALID_ARG, "eps must be finite and >= 0");
+    if (L > 32)
+        return fail(DSPARK_ERR_INVALID_ARG, "the fused projection write handles at most 32 layers (L=%d)", L);
     const int64_t capacity = num_blocks * (int64_t)block_size;
     if (capacity / block_size != num_blocks || num_blocks > (INT64_MAX / nkv) / block_size / DSPARK_CACHE_ROW)
         return fail(DSPARK_ERR_INVALID_ARG, "cache of %lld blocks too large", (long long)num_blocks);

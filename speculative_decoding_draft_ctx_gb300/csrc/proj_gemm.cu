@@ -11,9 +11,13 @@
 // states) and w [N, hidden] (N = L * 2 * nkv * 128, row ((l*2 + kv)*nkv + h)
 // * 128 + d), both bf16 and K-major: a TN GEMM with an fp32 accumulator.
 //
-// Tiling.  A CTA computes a 128-token x 256-column tile: the K rows and the V
-// rows of one (layer, head), i.e. exactly the two 128-element halves of the
-// head's cache rows, so the write needs no other tile.  Per 64-wide k-block a
+// Tiling.  A tile is 128 tokens x 256 columns: the K rows and the V rows of
+// one (layer, head), i.e. exactly the two 128-element halves of the head's
+// cache rows, so the write needs no other tile.  One persistent CTA per SM
+// walks the tiles (groups of 16 column tiles, all row tiles of a group
+// before the next, so the running CTAs share their weights and x rows in
+// L2) with two tensor-memory accumulators: the epilogue of one tile runs
+// while the MMAs of the next fill the other accumulator.  Per 64-wide k-block a
 // TMA producer warp loads the x tile (128 x 64) and the two weight boxes
 // (128 x 64 each) into a 4-stage shared-memory ring with 128-byte swizzle;
 // one thread of an MMA warp issues four tcgen05.mma (M 128, N 256, K 16,
@@ -47,8 +51,11 @@ constexpr int kThreadsG = 192;                             // warp 0 TMA, warp 1
 constexpr uint32_t kABytes = BM * BK * 2;                  // 16 KB
 constexpr uint32_t kBoxBytes = 128 * BK * 2;               // one 128-row weight box, 16 KB
 constexpr uint32_t kStageBytes = kABytes + 2 * kBoxBytes;  // 48 KB
-constexpr uint32_t kTmemCols = 256;
-constexpr uint32_t kSmemBytes = kStages * kStageBytes + 1024 /* alignment pad */ + 1024 /* barriers, tables */;
+constexpr uint32_t kTmemCols = 512;  // two 256-column accumulators: the epilogue of one tile overlaps the next
+constexpr int kMaxLayersProj = 32;   // the (1 + w) table of every layer lives in shared memory
+constexpr int kGroupN = 16;          // column tiles per rasterisation group
+constexpr uint32_t kSmemBytes = kStages * kStageBytes + 1024 /* alignment pad */ + 256 /* barriers */ +
+                                kMaxLayersProj * 128 * 4 /* (1 + w) table */;
 constexpr unsigned kFlagSlot = 0x1u, kFlagPos = 0x2u, kFlagTimeout = 0x4u;
 constexpr unsigned long long kTimeoutNs = 4000000000ull;
 constexpr uint32_t kSuspendNs = 200000;
@@ -212,6 +219,19 @@ __device__ __forceinline__ void st16(void *p, uint32_t a, uint32_t b, uint32_t c
     *reinterpret_cast<uint4 *>(p) = make_uint4(a, b, c, d);
 }
 
+// Tile order: groups of kGroupN column tiles (one (layer, head) each), all
+// row tiles of a group before the next group, so that the CTAs running at
+// any one time share a few MB of weights and x rows (both stay in L2).
+__device__ __forceinline__ void tile_coords(int tile, int num_m, int num_n, int &m, int &n)
+{
+    const int per_group = kGroupN * num_m;
+    const int g = tile / per_group;
+    const int r = tile - g * per_group;
+    const int gn = min(kGroupN, num_n - g * kGroupN);
+    m = r / gn;
+    n = g * kGroupN + (r - m * gn);
+}
+
 template <int MODE, int ROT, bool FP8>
 __global__ void __launch_bounds__(kThreadsG, 1)
     proj_gemm_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant__ CUtensorMap tmw,
@@ -221,24 +241,27 @@ __global__ void __launch_bounds__(kThreadsG, 1)
     unsigned char *smem = smem_raw + ((1024u - (saddr(smem_raw) & 1023u)) & 1023u);  // 1024-aligned for the swizzle
     unsigned char *stages = smem;
     unsigned char *ctl = smem + kStages * kStageBytes;
-    uint64_t *full = reinterpret_cast<uint64_t *>(ctl);  // TMA -> MMA
-    uint64_t *empty = full + kStages;                      // MMA -> TMA
-    uint64_t *done = empty + kStages;                      // MMA -> epilogue
+    uint64_t *full = reinterpret_cast<uint64_t *>(ctl);  // TMA -> MMA, per stage
+    uint64_t *empty = full + kStages;                      // MMA -> TMA, per stage
+    uint64_t *acc_full = empty + kStages;                  // MMA -> epilogue, per accumulator
+    uint64_t *acc_empty = acc_full + 2;                    // epilogue -> MMA, per accumulator
+    uint64_t *done = acc_empty + 2;                        // every MMA of the CTA has completed
     volatile uint32_t *tmem_slot = reinterpret_cast<volatile uint32_t *>(done + 1);
     volatile int *abort = reinterpret_cast<volatile int *>(tmem_slot + 1);
-    float *w1 = reinterpret_cast<float *>(ctl + 256);      // (1 + w) of the layer, 128 floats
+    float *w1 = reinterpret_cast<float *>(ctl + 256);      // (1 + w) of every layer, [L][128]
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int jt = blockIdx.x;  // (layer, head) of this tile
-    const int l = jt / p.nkv, h = jt - l * p.nkv;
-    const int64_t m0 = (int64_t)blockIdx.y * BM;
-    const int nk = ((l * 2 + 0) * p.nkv + h) * 128;  // first weight row of K(l, h)
-    const int nv = ((l * 2 + 1) * p.nkv + h) * 128;  // and of V(l, h)
+    const int num_m = (int)((p.T + BM - 1) / BM), num_n = p.L * p.nkv;
+    const int num_tiles = num_m * num_n;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; s++) {
             mbar_init(full + s, 1);
             mbar_init(empty + s, 1);
+        }
+        for (int b = 0; b < 2; b++) {
+            mbar_init(acc_full + b, 1);
+            mbar_init(acc_empty + b, 4);  // one arrive per epilogue warp
         }
         mbar_init(done, 1);
         *abort = 0;
@@ -254,8 +277,8 @@ __global__ void __launch_bounds__(kThreadsG, 1)
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
     }
     if (MODE == kModeWrite && warp >= 2) {
-        const int d = threadIdx.x - 64;  // the 128 epilogue threads: one weight each
-        w1[d] = 1.0f + bfl((uint32_t)__ldg(p.knorm_w + l * 128 + d));
+        for (int i = threadIdx.x - 64; i < p.L * 128; i += 128)
+            w1[i] = 1.0f + bfl((uint32_t)__ldg(p.knorm_w + i));
     }
     tc_fence_before();
     __syncthreads();
@@ -266,22 +289,31 @@ __global__ void __launch_bounds__(kThreadsG, 1)
     if (warp == 0) {
         // ------------------------------------------------------------ TMA producer
         if (lane == 0) {
-            int issued = 0;
-            for (int kb = 0, s = 0; kb < p.num_kb; kb++, s = (s + 1 == kStages) ? 0 : s + 1) {
-                const uint32_t ph = (uint32_t)(kb / kStages) & 1u;
-                if (!mbar_wait(empty + s, ph ^ 1u, abort))
-                    break;
-                unsigned char *st = stages + s * kStageBytes;
-                mbar_expect_arrive(full + s, kStageBytes);
-                tma_load(st, &tmx, kb * BK, (int32_t)m0, full + s);
-                tma_load(st + kABytes, &tmw, kb * BK, nk, full + s);
-                tma_load(st + kABytes + kBoxBytes, &tmw, kb * BK, nv, full + s);
-                issued++;
+            int issued = 0;  // k-blocks issued over all tiles
+            bool ok = true;
+            for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
+                int m, n;
+                tile_coords(tile, num_m, num_n, m, n);
+                const int l = n / p.nkv, h = n - l * p.nkv;
+                const int nk = ((l * 2 + 0) * p.nkv + h) * 128, nv = ((l * 2 + 1) * p.nkv + h) * 128;
+                for (int kb = 0; kb < p.num_kb; kb++) {
+                    const int s = issued % kStages;
+                    if (!mbar_wait(empty + s, ((uint32_t)(issued / kStages) & 1u) ^ 1u, abort)) {
+                        ok = false;
+                        break;
+                    }
+                    unsigned char *st = stages + s * kStageBytes;
+                    mbar_expect_arrive(full + s, kStageBytes);
+                    tma_load(st, &tmx, kb * BK, m * BM, full + s);
+                    tma_load(st + kABytes, &tmw, kb * BK, nk, full + s);
+                    tma_load(st + kABytes + kBoxBytes, &tmw, kb * BK, nv, full + s);
+                    issued++;
+                }
             }
             // the copies of the last rounds may still be landing: wait (bounded)
-            for (int kb = issued > kStages ? issued - kStages : 0; kb < issued; kb++) {
+            for (int it = issued > kStages ? issued - kStages : 0; it < issued; it++) {
                 const unsigned long long t0 = gtimer();
-                while (!mbar_try(full + kb % kStages, (uint32_t)(kb / kStages) & 1u) && gtimer() - t0 < kTimeoutNs) {
+                while (!mbar_try(full + it % kStages, (uint32_t)(it / kStages) & 1u) && gtimer() - t0 < kTimeoutNs) {
                 }
             }
         }
@@ -289,16 +321,31 @@ __global__ void __launch_bounds__(kThreadsG, 1)
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
-            for (int kb = 0, s = 0; kb < p.num_kb; kb++, s = (s + 1 == kStages) ? 0 : s + 1) {
-                if (!mbar_wait(full + s, (uint32_t)(kb / kStages) & 1u, abort))
+            int it = 0;  // k-blocks consumed over all tiles
+            bool ok = true;
+            for (int tile = blockIdx.x, i = 0; tile < num_tiles && ok; tile += gridDim.x, i++) {
+                const int b = i & 1;
+                // the epilogue has drained this accumulator (its previous use)
+                if (!mbar_wait(acc_empty + b, ((uint32_t)(i >> 1) & 1u) ^ 1u, abort))
                     break;
                 tc_fence_after();
-                const uint32_t a = saddr(stages + s * kStageBytes);
-                const uint32_t b = a + kABytes;
+                const uint32_t d = tmem + (uint32_t)(b * BN);
+                for (int kb = 0; kb < p.num_kb; kb++, it++) {
+                    const int s = it % kStages;
+                    if (!mbar_wait(full + s, (uint32_t)(it / kStages) & 1u, abort)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t a = saddr(stages + s * kStageBytes);
+                    const uint32_t bb = a + kABytes;
 #pragma unroll
-                for (int k = 0; k < BK / 16; k++)  // 16 bf16 = 32 bytes per step along K
-                    mma_bf16(tmem, sw128_desc(a + 32 * k), sw128_desc(b + 32 * k), (kb | k) != 0);
-                mma_commit(empty + s);
+                    for (int k = 0; k < BK / 16; k++)  // 16 bf16 = 32 bytes per step along K
+                        mma_bf16(d, sw128_desc(a + 32 * k), sw128_desc(bb + 32 * k), (kb | k) != 0);
+                    mma_commit(empty + s);
+                }
+                if (ok)
+                    mma_commit(acc_full + b);
             }
             mma_commit(done);  // fires once every MMA issued above has completed
         }
@@ -307,43 +354,61 @@ __global__ void __launch_bounds__(kThreadsG, 1)
         // ------------------------------------------------------------ epilogue
         const int q4 = warp & 3;  // the TMEM lane quarter this warp may access
         const int row = q4 * 32 + lane;
-        const int64_t t = m0 + row;
-        const uint32_t trow = tmem + ((uint32_t)(q4 * 32) << 16);
-        int64_t slot = -1, pos = 0;
-        if (MODE == kModeWrite && t < p.T) {
-            slot = __ldg(p.slot_mapping + t);
-            if (slot >= 0) {
-                pos = __ldg(p.positions + t);
-                if (slot >= p.capacity) {
-                    flags |= kFlagSlot;
-                    slot = -1;
-                } else if (pos < 0 || pos >= p.max_pos) {
-                    flags |= kFlagPos;
-                    slot = -1;
+        for (int tile = blockIdx.x, i = 0; tile < num_tiles; tile += gridDim.x, i++) {
+            const int b = i & 1;
+            int m, n;
+            tile_coords(tile, num_m, num_n, m, n);
+            const int l = n / p.nkv, h = n - l * p.nkv;
+            const int64_t t = (int64_t)m * BM + row;
+            int64_t slot = -1, pos = 0;
+            if (MODE == kModeWrite && t < p.T) {
+                slot = __ldg(p.slot_mapping + t);
+                if (slot >= 0) {
+                    pos = __ldg(p.positions + t);
+                    if (slot >= p.capacity) {
+                        if (n == 0)
+                            flags |= kFlagSlot;
+                        slot = -1;
+                    } else if (pos < 0 || pos >= p.max_pos) {
+                        if (n == 0)
+                            flags |= kFlagPos;
+                        slot = -1;
+                    }
                 }
             }
-        }
-        bool ok = mbar_wait(done, 0, abort);
-        ok = __all_sync(0xffffffffu, ok) && !*abort;
-        tc_fence_after();
-        if (ok && MODE == kModeProject) {
-            const int64_t N = (int64_t)p.L * 2 * p.nkv * 128;
+            bool ok = mbar_wait(acc_full + b, (uint32_t)(i >> 1) & 1u, abort);
+            ok = __all_sync(0xffffffffu, ok) && !*abort;
+            if (!ok)
+                break;
+            tc_fence_after();
+            const uint32_t trow = tmem + (uint32_t)(b * BN) + ((uint32_t)(q4 * 32) << 16);
+            if (MODE == kModeProject) {
+                const int64_t N = (int64_t)p.L * 2 * p.nkv * 128;
+                const int nk = ((l * 2 + 0) * p.nkv + h) * 128, nv = ((l * 2 + 1) * p.nkv + h) * 128;
 #pragma unroll 1
-            for (int c = 0; c < 8; c++) {
-                uint32_t r[32];
-                tmem_ld32(trow + 32 * c, r);  // every lane: the load is warp-wide
-                if (t < p.T) {
-                    uint32_t pk[16];
+                for (int c = 0; c < 8; c++) {
+                    uint32_t r[32];
+                    tmem_ld32(trow + 32 * c, r);  // every lane: the load is warp-wide
+                    if (c == 7) {                 // the accumulator is read: hand it back
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0)
+                            asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(saddr(acc_empty + b))
+                                         : "memory");
+                    }
+                    if (t < p.T) {
+                        uint32_t pk[16];
 #pragma unroll
-                    for (int i = 0; i < 16; i++)
-                        pk[i] = pack_bf16x2(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1]));
-                    uint16_t *dst = p.all_kv_out + t * N + (c < 4 ? nk + 32 * c : nv + 32 * (c - 4));
+                        for (int j = 0; j < 16; j++)
+                            pk[j] = pack_bf16x2(__uint_as_float(r[2 * j]), __uint_as_float(r[2 * j + 1]));
+                        uint16_t *dst = p.all_kv_out + t * N + (c < 4 ? nk + 32 * c : nv + 32 * (c - 4));
 #pragma unroll
-                    for (int k = 0; k < 4; k++)
-                        st16(dst + 8 * k, pk[4 * k], pk[4 * k + 1], pk[4 * k + 2], pk[4 * k + 3]);
+                        for (int k = 0; k < 4; k++)
+                            st16(dst + 8 * k, pk[4 * k], pk[4 * k + 1], pk[4 * k + 2], pk[4 * k + 3]);
+                    }
                 }
+                continue;
             }
-        } else if (ok) {
             // K: bf16 as the projection materialises it, then the Gemma norm in fp32
             uint32_t kw[64];
             float ss = 0.0f;
@@ -352,21 +417,23 @@ __global__ void __launch_bounds__(kThreadsG, 1)
                 uint32_t r[32];
                 tmem_ld32(trow + 32 * c, r);
 #pragma unroll
-                for (int i = 0; i < 16; i++) {
-                    const uint32_t pk = pack_bf16x2(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1]));
-                    kw[16 * c + i] = pk;
+                for (int j = 0; j < 16; j++) {
+                    const uint32_t pk = pack_bf16x2(__uint_as_float(r[2 * j]), __uint_as_float(r[2 * j + 1]));
+                    kw[16 * c + j] = pk;
                     ss = fmaf(bfl(pk), bfl(pk), ss);
                     ss = fmaf(bfh(pk), bfh(pk), ss);
                 }
             }
             float inv;  // ss/128 + eps >= eps > 0 (hardware reciprocal square root)
             asm("rsqrt.approx.ftz.f32 %0, %1;" : "=f"(inv) : "f"(fmaf(ss, 1.0f / kHeadDim, p.eps)));
+            const float *wl = w1 + l * 128;
 #pragma unroll
-            for (int i = 0; i < 64; i++)
-                kw[i] = pack_bf16x2((bfl(kw[i]) * inv) * w1[2 * i], (bfh(kw[i]) * inv) * w1[2 * i + 1]);
+            for (int j = 0; j < 64; j++)
+                kw[j] = pack_bf16x2((bfl(kw[j]) * inv) * wl[2 * j], (bfh(kw[j]) * inv) * wl[2 * j + 1]);
             unsigned char *dst = nullptr;
+            Fp8Scale vq;
             if (slot >= 0) {
-                // RoPE: dims i and i + r/2 (both in this thread), cos|sin of the token's position
+                // RoPE: dims j and j + r/2 (both in this thread), cos|sin of the token's position
                 uint32_t cs[ROT / 2];
                 const uint4 *src = reinterpret_cast<const uint4 *>(p.cos_sin + pos * ROT);
 #pragma unroll
@@ -375,21 +442,23 @@ __global__ void __launch_bounds__(kThreadsG, 1)
                     cs[4 * k] = v.x, cs[4 * k + 1] = v.y, cs[4 * k + 2] = v.z, cs[4 * k + 3] = v.w;
                 }
 #pragma unroll
-                for (int i = 0; i < ROT / 4; i++) {
-                    const uint32_t a = kw[i], b = kw[i + ROT / 4], c = cs[i], s = cs[ROT / 4 + i];
-                    kw[i] = rope_pair(a, c, b, s ^ 0x80008000u);  // a c - b s
-                    kw[i + ROT / 4] = rope_pair(b, c, a, s);      // b c + a s
+                for (int j = 0; j < ROT / 4; j++) {
+                    const uint32_t a = kw[j], bb = kw[j + ROT / 4], c = cs[j], s = cs[ROT / 4 + j];
+                    kw[j] = rope_pair(a, c, bb, s ^ 0x80008000u);  // a c - b s
+                    kw[j + ROT / 4] = rope_pair(bb, c, a, s);      // b c + a s
                 }
                 const int64_t rowel =
                     ((((slot >> p.bsl) * p.nkv + h) << p.bsl) + (slot & ((int64_t(1) << p.bsl) - 1))) * kRowElems;
                 dst = p.cache0 + (__ldg(p.cache_offsets + l) + rowel) * (FP8 ? 1 : 2);
                 if (FP8) {
-                    const float ks = __ldg(reinterpret_cast<const float *>(
-                        __ldg(reinterpret_cast<const unsigned long long *>(p.k_scales) + l)));
-                    const Fp8Scale kq = fp8_scale(ks);
+                    const Fp8Scale kq = fp8_scale(__ldg(reinterpret_cast<const float *>(
+                        __ldg(reinterpret_cast<const unsigned long long *>(p.k_scales) + l))));
+                    vq = fp8_scale(__ldg(reinterpret_cast<const float *>(
+                        __ldg(reinterpret_cast<const unsigned long long *>(p.v_scales) + l))));
 #pragma unroll
                     for (int k = 0; k < 8; k++) {
-                        const uint2 lo = quantise8(make_uint4(kw[8 * k], kw[8 * k + 1], kw[8 * k + 2], kw[8 * k + 3]), kq);
+                        const uint2 lo =
+                            quantise8(make_uint4(kw[8 * k], kw[8 * k + 1], kw[8 * k + 2], kw[8 * k + 3]), kq);
                         const uint2 hi =
                             quantise8(make_uint4(kw[8 * k + 4], kw[8 * k + 5], kw[8 * k + 6], kw[8 * k + 7]), kq);
                         st16(dst + 16 * k, lo.x, lo.y, hi.x, hi.y);
@@ -400,24 +469,28 @@ __global__ void __launch_bounds__(kThreadsG, 1)
                         st16(dst + 16 * k, kw[4 * k], kw[4 * k + 1], kw[4 * k + 2], kw[4 * k + 3]);
                 }
             }
-            // V: bf16 as materialised, stored as it is (or encoded)
-            Fp8Scale vq;
-            if (FP8 && slot >= 0)
-                vq = fp8_scale(__ldg(reinterpret_cast<const float *>(
-                    __ldg(reinterpret_cast<const unsigned long long *>(p.v_scales) + l))));
-#pragma unroll 1
+            // V: bf16 as materialised, stored as it is (or encoded); after its
+            // last read the accumulator is handed back to the MMA warp
+#pragma unroll
             for (int c = 0; c < 4; c++) {
                 uint32_t r[32];
                 tmem_ld32(trow + 128 + 32 * c, r);
+                if (c == 3) {
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0)
+                        asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(saddr(acc_empty + b)) : "memory");
+                }
                 if (slot >= 0) {
                     uint32_t pk[16];
 #pragma unroll
-                    for (int i = 0; i < 16; i++)
-                        pk[i] = pack_bf16x2(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1]));
+                    for (int j = 0; j < 16; j++)
+                        pk[j] = pack_bf16x2(__uint_as_float(r[2 * j]), __uint_as_float(r[2 * j + 1]));
                     if (FP8) {
 #pragma unroll
                         for (int k = 0; k < 2; k++) {
-                            const uint2 lo = quantise8(make_uint4(pk[8 * k], pk[8 * k + 1], pk[8 * k + 2], pk[8 * k + 3]), vq);
+                            const uint2 lo =
+                                quantise8(make_uint4(pk[8 * k], pk[8 * k + 1], pk[8 * k + 2], pk[8 * k + 3]), vq);
                             const uint2 hi =
                                 quantise8(make_uint4(pk[8 * k + 4], pk[8 * k + 5], pk[8 * k + 6], pk[8 * k + 7]), vq);
                             st16(dst + 128 + 32 * c + 16 * k, lo.x, lo.y, hi.x, hi.y);
@@ -435,7 +508,7 @@ __global__ void __launch_bounds__(kThreadsG, 1)
     __syncthreads();
     tc_fence_after();
     if (warp == 1) {
-        // every MMA has completed before the accumulator is freed (the
+        // every MMA has completed before the accumulators are freed (the
         // epilogue may have stopped waiting after an abort)
         if (lane == 0) {
             const unsigned long long t0 = gtimer();
@@ -487,12 +560,14 @@ cudaError_t launch_gemm(const CUtensorMap &tx, const CUtensorMap &tw, const Gemm
 {
     static std::mutex mu;
     static bool attr_set[64];
+    static int sms_cache[64];
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess)
         return e;
     if (dev < 0 || dev >= 64)
         return cudaErrorInvalidDevice;
+    int sms;
     {
         std::lock_guard<std::mutex> lock(mu);
         if (!attr_set[dev]) {
@@ -502,8 +577,17 @@ cudaError_t launch_gemm(const CUtensorMap &tx, const CUtensorMap &tw, const Gemm
                 return e;
             attr_set[dev] = true;
         }
+        if (sms_cache[dev] == 0) {
+            e = cudaDeviceGetAttribute(&sms_cache[dev], cudaDevAttrMultiProcessorCount, dev);
+            if (e != cudaSuccess)
+                return e;
+        }
+        sms = sms_cache[dev];
     }
-    const dim3 grid((unsigned)(p.L * p.nkv), (unsigned)((p.T + BM - 1) / BM));
+    // persistent: one CTA per SM (the shared-memory ring holds one), each
+    // walking the tile order with a stride of the grid
+    const int64_t tiles = (int64_t)p.L * p.nkv * ((p.T + BM - 1) / BM);
+    const int grid = (int)(tiles < sms ? tiles : sms);
     proj_gemm_kernel<MODE, ROT, FP8><<<grid, kThreadsG, kSmemBytes, stream>>>(tx, tw, p);
     return cudaGetLastError();
 }
@@ -539,6 +623,8 @@ cudaError_t launch_proj(const ProjArgs &a, cudaStream_t stream)
     p.eps = a.eps;
     if (a.all_kv_out)
         return launch_gemm<kModeProject, 16, false>(tx, tw, p, stream);
+    if (a.L > kMaxLayersProj)
+        return cudaErrorInvalidValue;
     switch (a.rotary_dim) {
     case 16:
         return a.fp8 ? launch_gemm<kModeWrite, 16, true>(tx, tw, p, stream)

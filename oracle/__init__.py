@@ -101,6 +101,8 @@ def lib():
         L.dspark_oracle_write.restype = ctypes.c_int
         L.dspark_oracle_rows.argtypes = [P, P, ctypes.c_int64, P, P, P, P, ctypes.c_int64, P]
         L.dspark_oracle_rows.restype = ctypes.c_int
+        L.dspark_oracle_gemma_norm_rows.argtypes = [P, P, ctypes.c_int64, ctypes.c_int64, ctypes.c_float, P, P]
+        L.dspark_oracle_gemma_norm_rows.restype = ctypes.c_int64
         L.dspark_oracle_bf16_rne_array.argtypes = [P, P, ctypes.c_int64]
         L.dspark_oracle_bf16_rne_array.restype = None
         L.dspark_oracle_qk_check.argtypes = [P, ctypes.c_int, ctypes.c_int]
@@ -146,6 +148,19 @@ def e4m3_rne_sat(x: float) -> int:
 
 
 # ---------------------------------------------------------------- steps
+
+def gemma_norm_rows(x_bits: np.ndarray, w_bits: np.ndarray, eps: float):
+    """The hidden-state Gemma RMSNorm of every row of x ([rows, n] bf16 codes)
+    with weight w ([n]): (y, y_alt) bf16 codes, y_alt the admissible other
+    neighbour where the exact value is within 2^-18 of a midpoint."""
+    x = np.ascontiguousarray(x_bits, dtype=np.uint16)
+    rows, n = x.shape
+    w = np.ascontiguousarray(w_bits, dtype=np.uint16).reshape(n)
+    y = np.empty_like(x)
+    ya = np.empty_like(x)
+    lib().dspark_oracle_gemma_norm_rows(_ptr(x), _ptr(w), rows, n, ctypes.c_float(eps), _ptr(y), _ptr(ya))
+    return y, ya
+
 
 def bf16_rne_array(x: np.ndarray) -> np.ndarray:
     """bf16 codes (RNE) of fp64 values, elementwise."""

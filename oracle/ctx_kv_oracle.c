@@ -477,3 +477,39 @@ void dspark_oracle_bf16_rne_array(const double *x, uint16_t *out, int64_t n)
     for (int64_t i = 0; i < n; i++)
         out[i] = dspark_oracle_bf16_rne(x[i]);
 }
+
+/* ------------------------------------------------------------------ */
+/* The hidden-state Gemma RMSNorm (DSpark draft model page: hidden_norm =
+ * _gemma_rms_norm(hidden_size, eps), applied to the context states by
+ * _normalize_context_states; "an fp32 1 + w weight"): for each of `rows`
+ * rows of n bf16 values, y = x * rsqrt(mean(x^2) + eps) * (1 + w) rounded
+ * to bf16, evaluated here in fp64.  y_alt as for the K norm: the other bf16
+ * neighbour where the exact value lies within 2^-18 of a rounding midpoint
+ * (else y).  Returns the number of such elements. */
+int64_t dspark_oracle_gemma_norm_rows(const uint16_t *x, const uint16_t *w, int64_t rows, int64_t n, float eps,
+                                      uint16_t *y, uint16_t *y_alt)
+{
+    int64_t amb = 0;
+    for (int64_t r = 0; r < rows; r++) {
+        const uint16_t *xr = x + r * n;
+        double ss = 0.0;
+        for (int64_t d = 0; d < n; d++) {
+            double v = dspark_oracle_bf16_decode(xr[d]);
+            ss += v * v;
+        }
+        double inv = 1.0 / sqrt(ss / (double)n + (double)eps);
+        for (int64_t d = 0; d < n; d++) {
+            double v = dspark_oracle_bf16_decode(xr[d]) * inv * (1.0 + dspark_oracle_bf16_decode(w[d]));
+            uint16_t dn = dspark_oracle_bf16_rne(v * (1.0 - ORACLE_TIE_REL));
+            uint16_t up = dspark_oracle_bf16_rne(v * (1.0 + ORACLE_TIE_REL));
+            uint16_t yy = dspark_oracle_bf16_rne(v);
+            y[r * n + d] = yy;
+            y_alt[r * n + d] = yy;
+            if (dn != up) {
+                y_alt[r * n + d] = yy == dn ? up : dn;
+                amb++;
+            }
+        }
+    }
+    return amb;
+}

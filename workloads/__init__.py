@@ -13,3 +13,6 @@ from .qk_insert import (  # noqa: F401
 from .proj import (  # noqa: F401
     ProjWorkload, PROJ_WORKLOADS, PROJ_WORKLOADS_BY_NAME, ProjInputs, generate_proj, proj_flops, with_all_kv,
 )
+from .hidden_norm import (  # noqa: F401
+    NormWorkload, NORM_WORKLOADS, NORM_WORKLOADS_BY_NAME, generate_norm, norm_bytes,
+)

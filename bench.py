@@ -47,6 +47,7 @@ KERNEL_SRCS = [os.path.join(ROOT, "speculative_decoding_draft_ctx_gb300", "csrc"
                          "ctx_kv_device.cuh")]
 QK_METRIC = "draft-token QK-norm/RoPE/KV-insert GB/s on 1 GB300; % of HBM roofline"
 PROJ_METRIC = "fused context-KV projection + write TFLOP/s on 1 GB300; % of bf16 tensor roofline"
+NORM_METRIC = "context-state Gemma RMSNorm GB/s on 1 GB300; % of HBM roofline"
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "ncu_traffic.json")
 FALLBACK_HBM_GBS = 6800.0
 
@@ -59,7 +60,7 @@ def parse_args(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--config", default="long_context",
                     choices=[w.name for w in wk.WORKLOADS] + [w.name for w in wk.QK_WORKLOADS] +
-                    [w.name for w in wk.PROJ_WORKLOADS],
+                    [w.name for w in wk.PROJ_WORKLOADS] + [w.name for w in wk.NORM_WORKLOADS],
                     help="a context-KV write workload, a qk_* workload of the draft-token QK insert, or a "
                          "proj_* workload of the projection with the write fused into it")
     ap.add_argument("--e2e-steps", type=int, default=30)
@@ -338,6 +339,8 @@ def run_reference(args):
         return run_reference_qk(args)
     if args.config in wk.PROJ_WORKLOADS_BY_NAME:
         return run_reference_proj(args)
+    if args.config in wk.NORM_WORKLOADS_BY_NAME:
+        return run_reference_norm(args)
     wl = select_workload(args)
     inp = wk.generate(wl)
     budget = 90.0  # seconds of oracle work for the whole run
@@ -815,6 +818,138 @@ def run_proj(args):
     return 0
 
 
+def run_norm(args):
+    """The hidden-state Gemma RMSNorm of the context states: one launch per
+    step, CUDA events per launch, input sets rotated past L2; beside it the
+    unfused PyTorch composition (fp32 ops) timed the same way."""
+    import speculative_decoding_draft_ctx_gb300 as dk
+
+    ws, rank, local = dist_env()
+    if not torch.cuda.is_available():
+        raise RuntimeError("bench.py needs a CUDA device")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    pg = None
+    if ws > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl", device_id=dev)
+        pg = dist
+    dk.lib()
+    wl = wk.NORM_WORKLOADS_BY_NAME[args.config]
+    step_bytes = wk.norm_bytes(wl)
+    n_sets = max(1, math.ceil(3 * l2_bytes() / step_bytes))
+    sets = []
+    for i in range(n_sets):
+        x, w, eps = wk.generate_norm(wl, seed=wl.seed + 1000 * rank + i)
+        sets.append((x.to(dev), w.to(dev), torch.empty_like(x, device=dev)))
+    stream = torch.cuda.current_stream()
+
+    def ours(i):
+        x, w, o = sets[i % n_sets]
+        dk.gemma_rms_norm(x, w, wl.eps, out=o)
+
+    def unfused(i):
+        x, w, o = sets[i % n_sets]
+        xf = x.float()
+        o.copy_((xf * torch.rsqrt(xf.pow(2).mean(-1, keepdim=True) + wl.eps) * (1.0 + w.float())).to(torch.bfloat16))
+
+    def timed(fn, steps):
+        """The steps replayed from one CUDA graph (no host launch gaps:
+        a 10 us launch is shorter than the host's launch path)."""
+        for i in range(args.warmup):
+            fn(i)
+        torch.cuda.synchronize()
+        side = torch.cuda.Stream()
+        side.wait_stream(stream)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=side):
+            for i in range(steps):
+                fn(i)
+        stream.wait_stream(side)
+        graph.replay()
+        torch.cuda.synchronize()
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        if pg:
+            pg.barrier()
+        torch.cuda.synchronize()
+        t0.record(stream)
+        graph.replay()
+        t1.record(stream)
+        torch.cuda.synchronize()
+        if pg:
+            pg.barrier()
+        ms = t0.elapsed_time(t1)
+        del graph
+        return max_over_ranks(ms, pg, dev), ms / steps
+
+    with ClockSampler(local) as clk:
+        total_ms, ours_ms = timed(ours, args.steps)
+    _, unfused_ms = timed(unfused, max(10, min(args.steps, 200)))
+    value = whole_job_rate(step_bytes, args.steps, ws, total_ms) / 1e9
+    peak, peak_kind = measured_peaks()
+    achieved = step_bytes / (ours_ms * 1e-3) / 1e9
+
+    e2e = None
+    if not args.no_e2e:
+        hx = sets[0][0].cpu().pin_memory()
+        ho = torch.empty_like(hx).pin_memory()
+        x, w, o = sets[0]
+        ne = max(1, args.e2e_steps)
+
+        def e2e_step():
+            x.copy_(hx, non_blocking=True)
+            dk.gemma_rms_norm(x, w, wl.eps, out=o)
+            ho.copy_(o, non_blocking=True)
+
+        for _ in range(3):
+            e2e_step()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(ne):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        e_ms = max_over_ranks(e0.elapsed_time(e1), pg, dev)
+        e2e = {"value": whole_job_rate(step_bytes, ne, ws, e_ms) / 1e9, "unit": UNIT,
+               "h2d_bytes_per_step": hx.numel() * 2, "d2h_bytes_per_step": ho.numel() * 2, "steps": ne,
+               "ms_per_step": e_ms / ne}
+
+    cpu = None
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        import oracle
+
+        x, w, eps = wk.generate_norm(wl)
+        n = min(wl.rows, 256)
+        xb = x[:n].contiguous().view(torch.int16).numpy().view(np.uint16)
+        t = time.perf_counter()
+        oracle.gemma_norm_rows(xb, w.view(torch.int16).numpy().view(np.uint16), eps)
+        dt = time.perf_counter() - t
+        cpu = {"value": 4 * n * wl.hidden / dt / 1e9, "unit": UNIT, "cores": 1, "kind": "oracle", "seconds": dt,
+               "sample": f"first {n} of {wl.rows} rows, one thread, plain C oracle"}
+    if rank == 0:
+        line = {
+            "metric": NORM_METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": wl.name, "rows": wl.rows, "hidden": wl.hidden, "parallelism": f"replicas{ws}",
+                       "input_sets": n_sets, "timing": "one CUDA graph of all steps",
+                       "l2": ("inputs larger than L2" if n_sets == 1 else
+                              f"{n_sets} input sets rotated, footprint > 3x L2")},
+            "bytes_per_step": step_bytes,
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                         "frac": achieved / peak, "traffic": None, "peak_source": peak_kind},
+            "compare_ms_per_step": {"fused_norm": ours_ms, "unfused_torch_fp32": unfused_ms},
+            "cpu_baseline": cpu, "e2e": e2e, "clocks": clk.summary(), "gpu_launches": args.steps,
+            "kernel_avg_us": ours_ms * 1e3,
+        }
+        print(json.dumps(line), flush=True)
+    if pg:
+        pg.destroy_process_group()
+    return 0
+
+
 def proj_oracle_sample(wl, n: int) -> float:
     """Seconds the oracle takes for the projection and write of the first
     ``n`` tokens of a projection workload (fp64 BLAS matmul + C write)."""
@@ -861,6 +996,42 @@ def run_reference_proj(args):
     return 0
 
 
+def run_reference_norm(args):
+    """The reference arm of a norm workload: the C oracle on the first rows
+    of the call per step."""
+    import oracle
+
+    wl = wk.NORM_WORKLOADS_BY_NAME[args.config]
+    x, w, eps = wk.generate_norm(wl)
+    wb = w.view(torch.int16).numpy().view(np.uint16)
+    per_step = 90.0 / max(1, args.steps + args.warmup)
+    t = time.perf_counter()
+    oracle.gemma_norm_rows(x[:8].contiguous().view(torch.int16).numpy().view(np.uint16), wb, eps)
+    per_row = max((time.perf_counter() - t) / 8, 1e-7)
+    n = int(max(1, min(wl.rows, per_step / per_row)))
+    xb = x[:n].contiguous().view(torch.int16).numpy().view(np.uint16)
+    for _ in range(args.warmup):
+        oracle.gemma_norm_rows(xb, wb, eps)
+    total = 0.0
+    for _ in range(args.steps):
+        t = time.perf_counter()
+        oracle.gemma_norm_rows(xb, wb, eps)
+        total += time.perf_counter() - t
+    value = 4 * n * wl.hidden * args.steps / total / 1e9
+    line = {
+        "impl": "reference", "metric": NORM_METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": wl.name, "rows": wl.rows, "hidden": wl.hidden, "sample_rows": n},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": f"first {n} of {wl.rows} rows per step, one thread, plain C oracle"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def device_inputs_ctx(ctx):
     """Per-layer fp32 scale tensors (one element each) of a device-side
     context-write input set, like the attention layers' k/v scales."""
@@ -877,6 +1048,8 @@ def main(argv=None):
         return run_qk(args)
     if args.config in wk.PROJ_WORKLOADS_BY_NAME:
         return run_proj(args)
+    if args.config in wk.NORM_WORKLOADS_BY_NAME:
+        return run_norm(args)
     return run_ours(args)
 
 

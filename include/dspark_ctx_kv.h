@@ -116,6 +116,23 @@ int dspark_ctx_kv_write_ex(const void *all_kv, const void *knorm_w, const int64_
                            cudaStream_t stream);
 
 /*
+ * dspark_gemma_rms_norm -- the hidden-state Gemma RMSNorm of the context
+ * states (DSpark draft model page: hidden_norm = _gemma_rms_norm(hidden_size,
+ * eps), _normalize_context_states): for every row,
+ * out = bf16(x * rsqrt(mean(x^2) + eps) * (1 + w)), evaluated in fp32.
+ *
+ *  x      device, bf16 [rows, hidden] contiguous, 16-byte aligned.
+ *  w      device, bf16 [hidden], 16-byte aligned (applied as 1 + w).
+ *  out    device, bf16 [rows, hidden], 16-byte aligned; may be x itself
+ *         (in place), must not overlap it otherwise.
+ *  hidden a positive multiple of 8, at most 8192.   eps: finite, >= 0.
+ * rows == 0 returns DSPARK_OK without a launch.  One launch; allocates,
+ * copies and synchronises nothing.
+ */
+int dspark_gemma_rms_norm(const void *x, const void *w, void *out, int64_t rows, int hidden, float eps,
+                          cudaStream_t stream);
+
+/*
  * dspark_ctx_kv_project -- the context-KV projection on the tensor cores
  * (DSpark draft model page, precompute_and_store_context_kv:
  * all_kv = _project_context_kv_token_major(context_states, ...)):

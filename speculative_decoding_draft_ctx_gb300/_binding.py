@@ -37,7 +37,7 @@ EXPORTS = (
     "dspark_ctx_kv_tables_cache_offsets", "dspark_ctx_kv_tables_k_scales",
     "dspark_ctx_kv_tables_v_scales", "dspark_ctx_kv_tables_builds", "dspark_ctx_kv_tables_destroy",
     "dspark_ctx_kv_last_error", "dspark_ctx_kv_status_string", "dspark_qknorm_rope_kv_insert",
-    "dspark_ctx_kv_project", "dspark_ctx_kv_project_write",
+    "dspark_ctx_kv_project", "dspark_ctx_kv_project_write", "dspark_gemma_rms_norm",
 )
 
 
@@ -111,6 +111,8 @@ def lib() -> ctypes.CDLL:
         L.dspark_ctx_kv_project_write.argtypes = [P, P, I64, I, P, P, P, P, I64, P, I64, P, P, P, I, I, I, I,
                                                   ctypes.c_float, I, P, P]
         L.dspark_ctx_kv_project_write.restype = I
+        L.dspark_gemma_rms_norm.argtypes = [P, P, P, I64, I, ctypes.c_float, P]
+        L.dspark_gemma_rms_norm.restype = I
         _lib = L
         return L
 
@@ -183,6 +185,12 @@ def dspark_qknorm_rope_kv_insert(qkv, q_norm_w, k_norm_w, cos_sin, max_pos, posi
         _addr(slot_mapping), _addr(kv_cache), int(num_blocks), int(block_size), kv_dtype_code(kv_dtype),
         _addr(k_scale), _addr(v_scale), _addr(q_fp8_out), float(q_fp8_scale), _addr(error_flags),
         _stream(stream)))
+
+
+def dspark_gemma_rms_norm(x, w, out, rows, hidden, eps, stream=None):
+    """``dspark_gemma_rms_norm`` of the C ABI."""
+    check(lib().dspark_gemma_rms_norm(_addr(x), _addr(w), _addr(out), int(rows), int(hidden), float(eps),
+                                      _stream(stream)))
 
 
 def dspark_ctx_kv_project(x, w_kv, all_kv_out, num_ctx, hidden, L, nkv, stream=None):

@@ -24,6 +24,7 @@ KERNEL_SRC = os.path.join(CSRC, "ctx_kv_kernel.cu")
 TMA_SRC = os.path.join(CSRC, "ctx_kv_tma.cu")
 QK_SRC = os.path.join(CSRC, "qk_insert_kernel.cu")
 PROJ_SRC = os.path.join(CSRC, "proj_gemm.cu")
+NORM_SRC = os.path.join(CSRC, "hidden_norm.cu")
 API_SRC = os.path.join(CSRC, "ctx_kv_api.cpp")
 HEADERS = [os.path.join(CSRC, "ctx_kv_internal.h"), os.path.join(CSRC, "ctx_kv_device.cuh"),
            os.path.join(INCLUDE, "dspark_ctx_kv.h")]
@@ -45,7 +46,7 @@ def _stale() -> bool:
     if not os.path.exists(LIB_PATH):
         return True
     t = os.path.getmtime(LIB_PATH)
-    return any(os.path.getmtime(s) > t for s in [KERNEL_SRC, TMA_SRC, QK_SRC, PROJ_SRC, API_SRC, *HEADERS])
+    return any(os.path.getmtime(s) > t for s in [KERNEL_SRC, TMA_SRC, QK_SRC, PROJ_SRC, NORM_SRC, API_SRC, *HEADERS])
 
 
 def _run(cmd):
@@ -64,7 +65,7 @@ def build(force: bool = False, verbose: bool = False) -> str:
         home = cuda_home()
         nvcc = os.path.join(home, "bin", "nvcc")
         objs, cmds = [], []
-        for src in (KERNEL_SRC, TMA_SRC, QK_SRC, PROJ_SRC):
+        for src in (KERNEL_SRC, TMA_SRC, QK_SRC, PROJ_SRC, NORM_SRC):
             obj = os.path.join(BUILD_DIR, os.path.basename(src)[:-3] + ".o")
             cmd = [nvcc, *ARCH, "-lineinfo", "-O3", "-std=c++17", "-Xcompiler", "-fPIC",
                    "-I", INCLUDE, "-c", src, "-o", obj]
@@ -79,7 +80,7 @@ def build(force: bool = False, verbose: bool = False) -> str:
         with ThreadPoolExecutor(len(cmds)) as ex:
             outs = list(ex.map(_run, cmds))
         if verbose:
-            sys.stderr.write("".join(outs[:4]))
+            sys.stderr.write("".join(outs[:5]))
         tmp = LIB_PATH + f".tmp{os.getpid()}"
         _run([nvcc, *ARCH, "-shared", "-o", tmp, *objs, "-lpthread", "-ldl", "-lrt"])
         os.replace(tmp, LIB_PATH)

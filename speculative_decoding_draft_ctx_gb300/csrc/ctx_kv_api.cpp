@@ -368,6 +368,34 @@ int dspark_ctx_kv_project_write(const void *x, const void *w_kv, int64_t num_ctx
     return ok();
 }
 
+int dspark_gemma_rms_norm(const void *x, const void *w, void *out, int64_t rows, int hidden, float eps,
+                          cudaStream_t stream)
+{
+    if (rows < 0)
+        return fail(DSPARK_ERR_INVALID_ARG, "rows %lld < 0", (long long)rows);
+    if (hidden <= 0 || hidden % 8 != 0 || hidden > 8192)
+        return fail(DSPARK_ERR_INVALID_ARG, "hidden %d must be a positive multiple of 8, at most 8192", hidden);
+    if (!(eps >= 0.0f) || std::isinf(eps))
+        return fail(DSPARK_ERR_INVALID_ARG, "eps must be finite and >= 0");
+    if (rows > INT64_MAX / hidden / 2)
+        return fail(DSPARK_ERR_INVALID_ARG, "rows %lld too large", (long long)rows);
+    if (rows == 0)
+        return ok();
+    if (!x || !w || !out)
+        return fail(DSPARK_ERR_INVALID_ARG, "null buffer pointer");
+    if (!aligned(x, 16) || !aligned(w, 16) || !aligned(out, 16))
+        return fail(DSPARK_ERR_ALIGNMENT, "x, w and out must be 16-byte aligned");
+    const uintptr_t xb = reinterpret_cast<uintptr_t>(x), ob = reinterpret_cast<uintptr_t>(out);
+    const uintptr_t span = (uintptr_t)rows * (uintptr_t)hidden * 2;
+    if (xb != ob && xb < ob + span && ob < xb + span)
+        return fail(DSPARK_ERR_INVALID_ARG, "out overlaps x without being x");
+    cudaError_t e = dspark::launch_gemma_norm(static_cast<const uint16_t *>(x), static_cast<const uint16_t *>(w),
+                                              static_cast<uint16_t *>(out), rows, hidden, eps, stream);
+    if (e != cudaSuccess)
+        return fail(DSPARK_ERR_CUDA, "norm launch failed: %s", cudaGetErrorString(e));
+    return ok();
+}
+
 int dspark_ctx_kv_validate_layers(int L, const dspark_cache_desc *layers)
 {
     if (L <= 0 || !layers)

@@ -99,4 +99,9 @@ struct ProjArgs {
 
 cudaError_t launch_proj(const ProjArgs &a, cudaStream_t stream);
 
+// Hidden-state Gemma RMSNorm (hidden_norm.cu): rows of hidden bf16 values,
+// hidden a multiple of 8 and at most 8192; out may equal x.
+cudaError_t launch_gemma_norm(const uint16_t *x, const uint16_t *w, uint16_t *out, int64_t rows, int hidden,
+                              float eps, cudaStream_t stream);
+
 }  // namespace dspark

@@ -14,7 +14,7 @@ from __future__ import annotations
 from ._binding import (
     HEAD_DIM, DSparkError, Tables, cache_desc, dspark_ctx_kv_rotary_dims_supported,
     dspark_ctx_kv_project, dspark_ctx_kv_project_write, dspark_ctx_kv_validate_layers, dspark_ctx_kv_write,
-    dspark_ctx_kv_write_ex, dspark_qknorm_rope_kv_insert, kv_dtype_code,
+    dspark_ctx_kv_write_ex, dspark_gemma_rms_norm, dspark_qknorm_rope_kv_insert, kv_dtype_code,
 )
 
 
@@ -144,4 +144,17 @@ def project_context_kv(context_states, w_kv, num_layers, num_kv_heads, out=None,
         out = torch.empty((num_ctx, num_layers, 2, num_kv_heads, HEAD_DIM), dtype=torch.bfloat16,
                           device=context_states.device)
     dspark_ctx_kv_project(context_states, w_kv, out, num_ctx, hidden, num_layers, num_kv_heads, stream)
+    return out
+
+
+def gemma_rms_norm(x, weight, eps, out=None, stream=None):
+    """The hidden-state Gemma RMSNorm of the context states (the draft model's
+    hidden_norm): ``bf16(x * rsqrt(mean(x^2) + eps) * (1 + weight))`` per row
+    of ``x`` (bf16 ``[rows, hidden]``); ``out=x`` works in place."""
+    import torch
+
+    rows, hidden = x.shape
+    if out is None:
+        out = torch.empty_like(x)
+    dspark_gemma_rms_norm(x, weight, out, rows, hidden, eps, stream)
     return out

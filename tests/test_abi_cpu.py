@@ -206,3 +206,45 @@ def test_qk_insert_argument_checks(L):
     assert qk_call(num_tokens=0, expect_ok=True) == "DSPARK_OK"
     assert qk_call(rotary_dim=48) == "DSPARK_ERR_UNSUPPORTED_ROTARY_DIM"
     assert "not in {16, 32, 64}" in dk.dspark_ctx_kv_last_error()
+
+
+def test_norm_argument_checks(L):
+    def norm(**over):
+        a = dict(x=FAKE, w=FAKE, out=FAKE, rows=4, hidden=4096, eps=1e-6)
+        a.update(over)
+        with pytest.raises(dk.DSparkError) as ei:
+            dk.dspark_gemma_rms_norm(**a, stream=0)
+        return ei.value.name
+    assert norm(hidden=100) == "DSPARK_ERR_INVALID_ARG"
+    assert norm(hidden=8200) == "DSPARK_ERR_INVALID_ARG"
+    assert norm(rows=-1) == "DSPARK_ERR_INVALID_ARG"
+    assert norm(eps=float("inf")) == "DSPARK_ERR_INVALID_ARG"
+    assert norm(x=None) == "DSPARK_ERR_INVALID_ARG"
+    assert norm(x=FAKE + 8) == "DSPARK_ERR_ALIGNMENT"
+    assert norm(out=FAKE + 16) == "DSPARK_ERR_INVALID_ARG"  # overlaps x without being x
+    dk.dspark_gemma_rms_norm(FAKE, FAKE, FAKE, 0, 4096, 1e-6, stream=0)  # no rows: no launch
+
+
+def test_projection_argument_checks(L):
+    def proj(**over):
+        a = dict(x=FAKE, w_kv=FAKE, all_kv_out=FAKE, num_ctx=4, hidden=4096, L=2, nkv=2)
+        a.update(over)
+        with pytest.raises(dk.DSparkError) as ei:
+            dk.dspark_ctx_kv_project(**a, stream=0)
+        return ei.value.name
+    assert proj(hidden=100) == "DSPARK_ERR_ALIGNMENT"
+    assert proj(L=0) == "DSPARK_ERR_INVALID_ARG"
+    assert proj(nkv=40000) == "DSPARK_ERR_INVALID_ARG"
+    assert proj(num_ctx=-1) == "DSPARK_ERR_INVALID_ARG"
+    assert proj(num_ctx=65535 * 128 + 1) == "DSPARK_ERR_INVALID_ARG"
+    assert proj(x=FAKE + 8) == "DSPARK_ERR_ALIGNMENT"
+    assert proj(all_kv_out=None) == "DSPARK_ERR_ALIGNMENT"
+    dk.dspark_ctx_kv_project(FAKE, FAKE, FAKE, 0, 4096, 2, 2, stream=0)  # no tokens: no launch
+    with pytest.raises(dk.DSparkError) as ei:
+        dk.dspark_ctx_kv_project_write(FAKE, FAKE, 4, 4096, FAKE, FAKE, FAKE, FAKE, 64, FAKE, 4, FAKE, FAKE, FAKE,
+                                       33, 1, 16, 32, 1e-6, 0, stream=0)
+    assert ei.value.name == "DSPARK_ERR_INVALID_ARG"  # more than 32 layers
+    with pytest.raises(dk.DSparkError) as ei:
+        dk.dspark_ctx_kv_project_write(FAKE, FAKE, 4, 4096, FAKE, FAKE, FAKE, FAKE, 64, FAKE, 4, FAKE, FAKE, FAKE,
+                                       2, 1, 16, 48, 1e-6, 0, stream=0)
+    assert ei.value.name == "DSPARK_ERR_UNSUPPORTED_ROTARY_DIM"

@@ -67,7 +67,7 @@ class OracleInputs(ctypes.Structure):
         ("num_ctx", ctypes.c_int64), ("max_pos", ctypes.c_int64), ("num_blocks", ctypes.c_int64),
         ("num_layers", ctypes.c_int32), ("num_kv_heads", ctypes.c_int32),
         ("block_size", ctypes.c_int32), ("rotary_dim", ctypes.c_int32),
-        ("kv_dtype", ctypes.c_int32), ("eps", ctypes.c_float),
+        ("kv_dtype", ctypes.c_int32), ("eps", ctypes.c_float), ("layer_slots", ctypes.c_void_p),
     ]
 
 
@@ -217,7 +217,8 @@ class Problem:
     slot_mapping int64, k_scale / v_scale float32 ``[L]``."""
 
     def __init__(self, all_kv, knorm_w, positions, slot_mapping, cos_sin, k_scale, v_scale,
-                 *, num_blocks: int, block_size: int, rotary_dim: int, kv_dtype: int, eps: float):
+                 *, num_blocks: int, block_size: int, rotary_dim: int, kv_dtype: int, eps: float,
+                 layer_slots=None):
         self.all_kv = np.ascontiguousarray(all_kv, dtype=np.uint16)
         T, L, two, H, D = self.all_kv.shape
         assert two == 2 and D == HEAD_DIM
@@ -231,11 +232,15 @@ class Problem:
         self.T, self.L, self.H = T, L, H
         self.num_blocks, self.block_size = int(num_blocks), int(block_size)
         self.rotary_dim, self.kv_dtype, self.eps = int(rotary_dim), int(kv_dtype), float(eps)
+        # [L, T] one slot mapping per layer, or None (slot_mapping shared)
+        self.layer_slots = None if layer_slots is None else \
+            np.ascontiguousarray(layer_slots, dtype=np.int64).reshape(L, T)
         self.c = OracleInputs(
             _ptr(self.all_kv), _ptr(self.knorm_w), _ptr(self.positions), _ptr(self.slot_mapping),
             _ptr(self.cos_sin), _ptr(self.k_scale), _ptr(self.v_scale),
             T, self.cos_sin.shape[0], self.num_blocks, L, H, self.block_size, self.rotary_dim,
             self.kv_dtype, ctypes.c_float(self.eps).value,
+            _ptr(self.layer_slots) if self.layer_slots is not None else None,
         )
 
     @property
@@ -294,13 +299,16 @@ class Problem:
         -1 for padding."""
         ids = np.asarray(row_ids, dtype=np.int64).reshape(-1)
         t = ids // (self.L * self.H)
+        l = (ids // self.H) % self.L
         h = ids % self.H
-        return np.array([dest_row(int(self.slot_mapping[ti]), int(hi), self.H, self.block_size,
-                                  self.num_blocks) for ti, hi in zip(t, h)], dtype=np.int64)
+        slot = self.slot_mapping[t] if self.layer_slots is None else self.layer_slots[l, t]
+        return np.array([dest_row(int(s), int(hi), self.H, self.block_size, self.num_blocks)
+                         for s, hi in zip(slot, h)], dtype=np.int64)
 
 
-def problem_from_inputs(inp) -> Problem:
-    """A Problem from a ``workloads.Inputs`` (CPU torch tensors)."""
+def problem_from_inputs(inp, layer_slots=None) -> Problem:
+    """A Problem from a ``workloads.Inputs`` (CPU torch tensors); layer_slots
+    ([L, T] int64) gives every layer its own slot mapping."""
     import torch  # local: the oracle's arithmetic does not use torch
 
     def bits(x):
@@ -312,6 +320,7 @@ def problem_from_inputs(inp) -> Problem:
         bits(inp.cos_sin), inp.k_scale.cpu().numpy(), inp.v_scale.cpu().numpy(),
         num_blocks=wl.num_blocks, block_size=wl.block_size, rotary_dim=wl.rotary_dim,
         kv_dtype=KV_FP8_E4M3 if wl.kv_dtype == "fp8_e4m3" else KV_BF16, eps=inp.eps,
+        layer_slots=None if layer_slots is None else np.asarray(layer_slots),
     )
 
 

@@ -68,7 +68,17 @@ typedef struct {
     int32_t rotary_dim;
     int32_t kv_dtype;
     float eps;
+    /* [L][T] one slot mapping per layer (drafts whose layers span several
+     * KV-cache groups, DSpark draft model page, _shared_slot_mapping), or
+     * NULL: slot_mapping is shared by every layer. */
+    const int64_t *layer_slots;
 } dspark_oracle_inputs;
+
+/* The slot of token t in layer l's cache. */
+static int64_t slot_of(const dspark_oracle_inputs *in, int64_t t, int32_t l)
+{
+    return in->layer_slots ? in->layer_slots[(int64_t)l * in->num_ctx + t] : in->slot_mapping[t];
+}
 
 /* ------------------------------------------------------------------ */
 /* bf16: 1 sign, 8 exponent, 7 stored mantissa bits (the top half of an
@@ -328,9 +338,9 @@ static int cmp_i64(const void *a, const void *b)
     return (x > y) - (x < y);
 }
 
-/* Preconditions of a write: valid slots unique and inside the cache,
- * positions of valid tokens inside the cos|sin table, fp8 scales positive
- * and finite. */
+/* Preconditions of a write: within each layer's cache, valid slots unique
+ * and inside the cache; positions of tokens with a valid slot (in any
+ * layer) inside the cos|sin table; fp8 scales positive and finite. */
 int dspark_oracle_check_inputs(const dspark_oracle_inputs *in)
 {
     if (!in || in->num_ctx < 0 || in->num_layers <= 0 || in->num_kv_heads <= 0 ||
@@ -341,36 +351,44 @@ int dspark_oracle_check_inputs(const dspark_oracle_inputs *in)
     if (in->kv_dtype != ORACLE_KV_BF16 && in->kv_dtype != ORACLE_KV_FP8_E4M3)
         return ORACLE_ERR_ARG;
     const int64_t cap = in->num_blocks * in->block_size;
-    int64_t nv = 0;
+    const int L = in->num_layers;
     for (int64_t t = 0; t < in->num_ctx; t++) {
-        int64_t s = in->slot_mapping[t];
-        if (s < 0)
-            continue;
-        if (s >= cap)
-            return ORACLE_ERR_SLOT_RANGE;
-        if (in->positions[t] < 0 || in->positions[t] >= in->max_pos)
+        int any = 0;
+        for (int l = 0; l < L; l++) {
+            int64_t s = slot_of(in, t, l);
+            if (s < 0)
+                continue;
+            if (s >= cap)
+                return ORACLE_ERR_SLOT_RANGE;
+            any = 1;
+        }
+        if (any && (in->positions[t] < 0 || in->positions[t] >= in->max_pos))
             return ORACLE_ERR_POS_RANGE;
-        nv++;
     }
     if (in->kv_dtype == ORACLE_KV_FP8_E4M3)
-        for (int l = 0; l < in->num_layers; l++)
+        for (int l = 0; l < L; l++)
             if (!(in->k_scale[l] > 0.0f) || !(in->v_scale[l] > 0.0f) ||
                 isinf(in->k_scale[l]) || isinf(in->v_scale[l]))
                 return ORACLE_ERR_SCALE;
-    int64_t *sorted = (int64_t *)malloc((size_t)(nv ? nv : 1) * sizeof(int64_t));
+    int64_t *sorted = (int64_t *)malloc((size_t)(in->num_ctx ? in->num_ctx : 1) * sizeof(int64_t));
     if (!sorted)
         return ORACLE_ERR_NOMEM;
-    nv = 0;
-    for (int64_t t = 0; t < in->num_ctx; t++)
-        if (in->slot_mapping[t] >= 0)
-            sorted[nv++] = in->slot_mapping[t];
-    qsort(sorted, (size_t)nv, sizeof(int64_t), cmp_i64);
     int rc = ORACLE_OK;
-    for (int64_t i = 1; i < nv; i++)
-        if (sorted[i] == sorted[i - 1]) {
-            rc = ORACLE_ERR_SLOT_DUP;
-            break;
+    const int layers_to_check = in->layer_slots ? L : 1;
+    for (int l = 0; l < layers_to_check && rc == ORACLE_OK; l++) {
+        int64_t nv = 0;
+        for (int64_t t = 0; t < in->num_ctx; t++) {
+            int64_t s = slot_of(in, t, l);
+            if (s >= 0)
+                sorted[nv++] = s;
         }
+        qsort(sorted, (size_t)nv, sizeof(int64_t), cmp_i64);
+        for (int64_t i = 1; i < nv; i++)
+            if (sorted[i] == sorted[i - 1]) {
+                rc = ORACLE_ERR_SLOT_DUP;
+                break;
+            }
+    }
     free(sorted);
     return rc;
 }
@@ -399,10 +417,10 @@ int dspark_oracle_write(const dspark_oracle_inputs *in, void *const *caches,
     uint16_t rv[3 * ORACLE_HEAD_DIM];
     uint16_t row[ORACLE_ROW];
     for (int64_t t = t_begin; t < t_end; t++) {
-        int64_t slot = in->slot_mapping[t];
-        if (slot < 0)
-            continue; /* padding: not written */
         for (int l = 0; l < L; l++) {
+            const int64_t slot = slot_of(in, t, l);
+            if (slot < 0)
+                continue; /* padding: not written */
             for (int h = 0; h < H; h++) {
                 int32_t na = 0;
                 rc = dspark_oracle_row(in, t, l, h, row, rd, rv, &na);

@@ -278,3 +278,25 @@ def describe(wl: Workload) -> dict:
         "block_size": wl.block_size, "num_blocks": wl.num_blocks, "kv_cache_dtype": wl.kv_dtype,
         "max_pos": wl.max_pos,
     }
+
+
+def layer_slot_mappings(inp: Inputs, groups: int = 2, seed: int = 0) -> torch.Tensor:
+    """int64 ``[L, T]``: one slot mapping per layer for a draft whose layers
+    span ``groups`` KV-cache groups (DSpark draft model page,
+    ``_shared_slot_mapping``: such drafts have no shared mapping).  Layer l
+    belongs to group ``l * groups // L``; group 0 keeps the workload's own
+    mapping, every other group gets distinct random slots of the same cache
+    size, and a few tokens padded in one group are valid in another."""
+    wl = inp.workload
+    T, L = wl.num_ctx, wl.num_layers
+    g = torch.Generator().manual_seed(wl.seed * 7 + 11 + seed)
+    maps = [inp.slot_mapping.clone()]
+    for _ in range(1, groups):
+        m = torch.randperm(wl.capacity, generator=g)[:T].to(torch.int64)
+        flip = torch.rand(T, generator=g) < 0.05
+        valid = (inp.slot_mapping >= 0) ^ flip
+        maps.append(torch.where(valid, m, torch.full_like(m, -1)))
+    out = torch.empty((L, T), dtype=torch.int64)
+    for l in range(L):
+        out[l] = maps[min(groups - 1, l * groups // L)]
+    return out.contiguous()

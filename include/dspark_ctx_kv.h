@@ -212,6 +212,20 @@ int dspark_qknorm_rope_kv_insert(void *qkv, const void *q_norm_w, const void *k_
                                  const float *k_scale, const float *v_scale, void *q_fp8_out, float q_fp8_scale,
                                  unsigned int *error_flags, cudaStream_t stream);
 
+/* As dspark_ctx_kv_write_ex, for a draft whose layers do not share one slot
+ * mapping (DSpark draft model page, _shared_slot_mapping: drafts whose
+ * layers span several KV-cache groups).  layer_slot_mappings: device, [L]
+ * device pointers (8-byte aligned) to each layer's int64 [num_ctx] mapping,
+ * e.g. dspark_ctx_kv_tables_layer_slots.  Layer l's rows of token t go to
+ * layer l's slot of t (< 0: not written); valid slots must be distinct
+ * within each layer.  Positions stay shared by all layers. */
+int dspark_ctx_kv_write_layer_slots(const void *all_kv, const void *knorm_w, const int64_t *positions,
+                                    const int64_t *const *layer_slot_mappings, int64_t num_ctx,
+                                    const void *cos_sin, int64_t max_pos, void *layer0_cache, int64_t num_blocks,
+                                    const int64_t *cache_offsets, const float *const *k_scales,
+                                    const float *const *v_scales, int L, int nkv, int block_size, int rotary_dim,
+                                    float eps, int kv_dtype, unsigned int *error_flags, cudaStream_t stream);
+
 /* 1 when the kernel handles this head (writer page, rotary_dims_supported:
  * head_dim 128 and rotary_dim 16, 32 or 64), else 0. */
 int dspark_ctx_kv_rotary_dims_supported(int rotary_dim, int head_dim);
@@ -268,6 +282,13 @@ int dspark_ctx_kv_tables_update(dspark_ctx_kv_tables *tables, void *const *layer
                                 size_t elem_size, const float *const *k_scale_ptrs,
                                 const float *const *v_scale_ptrs, cudaStream_t stream);
 
+/* Per-layer slot mappings: layer_slot_ptrs is a host array [L] of device
+ * addresses of int64 [num_ctx] mappings.  Same addresses as the last call:
+ * DSPARK_OK, nothing enqueued; new ones: the device pointer table is copied
+ * on `stream`, unless it is capturing (DSPARK_ERR_CAPTURING, table kept). */
+int dspark_ctx_kv_tables_update_slots(dspark_ctx_kv_tables *tables, const int64_t *const *layer_slot_ptrs,
+                                      cudaStream_t stream);
+const int64_t *const *dspark_ctx_kv_tables_layer_slots(const dspark_ctx_kv_tables *tables);
 const int64_t *dspark_ctx_kv_tables_cache_offsets(const dspark_ctx_kv_tables *tables);
 const float *const *dspark_ctx_kv_tables_k_scales(const dspark_ctx_kv_tables *tables);
 const float *const *dspark_ctx_kv_tables_v_scales(const dspark_ctx_kv_tables *tables);

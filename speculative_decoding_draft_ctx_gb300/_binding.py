@@ -38,6 +38,7 @@ EXPORTS = (
     "dspark_ctx_kv_tables_v_scales", "dspark_ctx_kv_tables_builds", "dspark_ctx_kv_tables_destroy",
     "dspark_ctx_kv_last_error", "dspark_ctx_kv_status_string", "dspark_qknorm_rope_kv_insert",
     "dspark_ctx_kv_project", "dspark_ctx_kv_project_write", "dspark_gemma_rms_norm",
+    "dspark_ctx_kv_write_layer_slots", "dspark_ctx_kv_tables_update_slots", "dspark_ctx_kv_tables_layer_slots",
 )
 
 
@@ -113,6 +114,12 @@ def lib() -> ctypes.CDLL:
         L.dspark_ctx_kv_project_write.restype = I
         L.dspark_gemma_rms_norm.argtypes = [P, P, P, I64, I, ctypes.c_float, P]
         L.dspark_gemma_rms_norm.restype = I
+        L.dspark_ctx_kv_write_layer_slots.argtypes = write_args[:3] + [P] + write_args[4:] + [P, P]
+        L.dspark_ctx_kv_write_layer_slots.restype = I
+        L.dspark_ctx_kv_tables_update_slots.argtypes = [P, P, P]
+        L.dspark_ctx_kv_tables_update_slots.restype = I
+        L.dspark_ctx_kv_tables_layer_slots.argtypes = [P]
+        L.dspark_ctx_kv_tables_layer_slots.restype = P
         _lib = L
         return L
 
@@ -210,6 +217,18 @@ def dspark_ctx_kv_project_write(x, w_kv, num_ctx, hidden, knorm_w, positions, sl
         _addr(error_flags), _stream(stream)))
 
 
+def dspark_ctx_kv_write_layer_slots(all_kv, knorm_w, positions, layer_slot_mappings, num_ctx, cos_sin, max_pos,
+                                    layer0_cache, num_blocks, cache_offsets, k_scales, v_scales, L, nkv,
+                                    block_size, rotary_dim, eps, kv_dtype, error_flags=None, stream=None):
+    """``dspark_ctx_kv_write_layer_slots``: per-layer slot mappings given as a
+    device pointer table (an address)."""
+    check(lib().dspark_ctx_kv_write_layer_slots(
+        _addr(all_kv), _addr(knorm_w), _addr(positions), _addr(layer_slot_mappings), int(num_ctx),
+        _addr(cos_sin), int(max_pos), _addr(layer0_cache), int(num_blocks), _addr(cache_offsets),
+        _addr(k_scales), _addr(v_scales), int(L), int(nkv), int(block_size), int(rotary_dim),
+        float(eps), kv_dtype_code(kv_dtype), _addr(error_flags), _stream(stream)))
+
+
 def dspark_ctx_kv_rotary_dims_supported(rotary_dim: int, head_dim: int) -> bool:
     return bool(lib().dspark_ctx_kv_rotary_dims_supported(int(rotary_dim), int(head_dim)))
 
@@ -269,6 +288,15 @@ class Tables:
         vp = (ctypes.c_void_p * L)(*[_addr(s) for s in v_scales]) if v_scales is not None else None
         esize = caches[0].element_size() if hasattr(caches[0], "element_size") else 2
         check(lib().dspark_ctx_kv_tables_update(self._h, cp, esize, kp, vp, _stream(stream)))
+
+    def update_slots(self, slot_mappings, stream=None):
+        """Per-layer slot mappings (one int64 CUDA tensor per layer)."""
+        sp = (ctypes.c_void_p * self.L)(*[_addr(s) for s in slot_mappings])
+        check(lib().dspark_ctx_kv_tables_update_slots(self._h, sp, _stream(stream)))
+
+    @property
+    def layer_slots(self) -> int:
+        return lib().dspark_ctx_kv_tables_layer_slots(self._h) or 0
 
     @property
     def cache_offsets(self) -> int:

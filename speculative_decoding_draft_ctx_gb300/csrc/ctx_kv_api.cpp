@@ -64,6 +64,13 @@ int log2_exact(int64_t v)
     return n;
 }
 
+// The write with a shared or a per-layer slot mapping (exactly one is given).
+int write_common(const void *all_kv, const void *knorm_w, const int64_t *positions, const int64_t *slot_mapping,
+                 const int64_t *const *layer_slots, int64_t num_ctx, const void *cos_sin, int64_t max_pos,
+                 void *layer0_cache, int64_t num_blocks, const int64_t *cache_offsets, const float *const *k_scales,
+                 const float *const *v_scales, int L, int nkv, int block_size, int rotary_dim, float eps,
+                 int kv_dtype, unsigned int *error_flags, cudaStream_t stream);
+
 }  // namespace
 
 extern "C" {
@@ -98,6 +105,37 @@ int dspark_ctx_kv_write_ex(const void *all_kv, const void *knorm_w, const int64_
                            int rotary_dim, float eps, int kv_dtype, unsigned int *error_flags,
                            cudaStream_t stream)
 {
+    if (num_ctx > 0 && !slot_mapping)
+        return fail(DSPARK_ERR_INVALID_ARG, "null slot_mapping");
+    return write_common(all_kv, knorm_w, positions, slot_mapping, nullptr, num_ctx, cos_sin, max_pos, layer0_cache,
+                        num_blocks, cache_offsets, k_scales, v_scales, L, nkv, block_size, rotary_dim, eps,
+                        kv_dtype, error_flags, stream);
+}
+
+int dspark_ctx_kv_write_layer_slots(const void *all_kv, const void *knorm_w, const int64_t *positions,
+                                    const int64_t *const *layer_slot_mappings, int64_t num_ctx,
+                                    const void *cos_sin, int64_t max_pos, void *layer0_cache, int64_t num_blocks,
+                                    const int64_t *cache_offsets, const float *const *k_scales,
+                                    const float *const *v_scales, int L, int nkv, int block_size, int rotary_dim,
+                                    float eps, int kv_dtype, unsigned int *error_flags, cudaStream_t stream)
+{
+    if (num_ctx > 0 && (!layer_slot_mappings || !aligned(layer_slot_mappings, 8)))
+        return fail(DSPARK_ERR_INVALID_ARG, "layer_slot_mappings must be an 8-byte aligned device pointer table");
+    return write_common(all_kv, knorm_w, positions, nullptr, layer_slot_mappings, num_ctx, cos_sin, max_pos,
+                        layer0_cache, num_blocks, cache_offsets, k_scales, v_scales, L, nkv, block_size, rotary_dim,
+                        eps, kv_dtype, error_flags, stream);
+}
+
+}  // extern "C"
+
+namespace {
+
+int write_common(const void *all_kv, const void *knorm_w, const int64_t *positions, const int64_t *slot_mapping,
+                 const int64_t *const *layer_slots, int64_t num_ctx, const void *cos_sin, int64_t max_pos,
+                 void *layer0_cache, int64_t num_blocks, const int64_t *cache_offsets, const float *const *k_scales,
+                 const float *const *v_scales, int L, int nkv, int block_size, int rotary_dim, float eps,
+                 int kv_dtype, unsigned int *error_flags, cudaStream_t stream)
+{
     // Scalar checks first: they need no device and no pointer.
     if (num_ctx < 0)
         return fail(DSPARK_ERR_INVALID_ARG, "num_ctx %lld < 0", (long long)num_ctx);
@@ -122,13 +160,13 @@ int dspark_ctx_kv_write_ex(const void *all_kv, const void *knorm_w, const int64_
     if (num_ctx == 0)
         return ok();  // nothing to store, and no launch
 
-    if (!all_kv || !knorm_w || !positions || !slot_mapping || !cos_sin || !layer0_cache || !cache_offsets)
+    if (!all_kv || !knorm_w || !positions || !cos_sin || !layer0_cache || !cache_offsets)
         return fail(DSPARK_ERR_INVALID_ARG, "null buffer pointer");
     if (kv_dtype == DSPARK_KV_FP8_E4M3 && (!k_scales || !v_scales))
         return fail(DSPARK_ERR_INVALID_ARG, "fp8 cache needs k_scales and v_scales");
     if (!aligned(all_kv, 16) || !aligned(knorm_w, 16) || !aligned(cos_sin, 16) || !aligned(layer0_cache, 16))
         return fail(DSPARK_ERR_ALIGNMENT, "all_kv, knorm_w, cos_sin and layer0_cache must be 16-byte aligned");
-    if (!aligned(positions, 8) || !aligned(slot_mapping, 8) || !aligned(cache_offsets, 8) ||
+    if (!aligned(positions, 8) || (slot_mapping && !aligned(slot_mapping, 8)) || !aligned(cache_offsets, 8) ||
         (k_scales && !aligned(k_scales, 8)) || (v_scales && !aligned(v_scales, 8)))
         return fail(DSPARK_ERR_ALIGNMENT, "int64 and pointer tables must be 8-byte aligned");
     if (error_flags && !aligned(error_flags, 4))
@@ -139,6 +177,7 @@ int dspark_ctx_kv_write_ex(const void *all_kv, const void *knorm_w, const int64_
     p.knorm_w = static_cast<const uint16_t *>(knorm_w);
     p.positions = positions;
     p.slot_mapping = slot_mapping;
+    p.layer_slots = layer_slots;
     p.cos_sin = static_cast<const uint16_t *>(cos_sin);
     p.cache0 = static_cast<unsigned char *>(layer0_cache);
     p.cache_offsets = cache_offsets;
@@ -160,6 +199,10 @@ int dspark_ctx_kv_write_ex(const void *all_kv, const void *knorm_w, const int64_
         return fail(DSPARK_ERR_CUDA, "launch failed: %s", cudaGetErrorString(e));
     return ok();
 }
+
+}  // namespace
+
+extern "C" {
 
 int dspark_ctx_kv_write(const void *all_kv, const void *knorm_w, const int64_t *positions,
                         const int64_t *slot_mapping, int64_t num_ctx, const void *cos_sin,
@@ -335,7 +378,7 @@ int dspark_ctx_kv_project_write(const void *x, const void *w_kv, int64_t num_ctx
         return fail(DSPARK_ERR_INVALID_ARG, "fp8 cache needs k_scales and v_scales");
     if (!aligned(knorm_w, 16) || !aligned(cos_sin, 16) || !aligned(layer0_cache, 16))
         return fail(DSPARK_ERR_ALIGNMENT, "knorm_w, cos_sin and layer0_cache must be 16-byte aligned");
-    if (!aligned(positions, 8) || !aligned(slot_mapping, 8) || !aligned(cache_offsets, 8) ||
+    if (!aligned(positions, 8) || (slot_mapping && !aligned(slot_mapping, 8)) || !aligned(cache_offsets, 8) ||
         (k_scales && !aligned(k_scales, 8)) || (v_scales && !aligned(v_scales, 8)))
         return fail(DSPARK_ERR_ALIGNMENT, "int64 and pointer tables must be 8-byte aligned");
     if (error_flags && !aligned(error_flags, 4))
@@ -452,7 +495,9 @@ struct dspark_ctx_kv_tables {
     int device = -1;
     int64_t *d_offsets = nullptr;         // [L]
     const float **d_scales = nullptr;     // [2L]: k then v
+    const int64_t **d_slots = nullptr;    // [L]: per-layer slot mappings
     std::vector<uintptr_t> key;           // caches, k scales, v scales, elem size
+    std::vector<uintptr_t> slot_key;      // per-layer slot mapping addresses
     int64_t builds = 0;
 };
 
@@ -472,8 +517,11 @@ int dspark_ctx_kv_tables_create(int L, dspark_ctx_kv_tables **out)
         e = cudaMalloc(reinterpret_cast<void **>(&t->d_offsets), sizeof(int64_t) * L);
     if (e == cudaSuccess)
         e = cudaMalloc(reinterpret_cast<void **>(&t->d_scales), sizeof(float *) * 2 * L);
+    if (e == cudaSuccess)
+        e = cudaMalloc(reinterpret_cast<void **>(&t->d_slots), sizeof(int64_t *) * L);
     if (e != cudaSuccess) {
         cudaFree(t->d_offsets);
+        cudaFree(t->d_scales);
         delete t;
         return fail(DSPARK_ERR_CUDA, "tables_create: %s", cudaGetErrorString(e));
     }
@@ -530,6 +578,39 @@ int dspark_ctx_kv_tables_update(dspark_ctx_kv_tables *t, void *const *layer_cach
     return ok();
 }
 
+int dspark_ctx_kv_tables_update_slots(dspark_ctx_kv_tables *t, const int64_t *const *layer_slot_ptrs,
+                                      cudaStream_t stream)
+{
+    if (!t || !layer_slot_ptrs)
+        return fail(DSPARK_ERR_INVALID_ARG, "tables_update_slots: null argument");
+    const int L = t->L;
+    std::vector<uintptr_t> key(L);
+    for (int l = 0; l < L; l++) {
+        key[l] = reinterpret_cast<uintptr_t>(layer_slot_ptrs[l]);
+        if (!key[l] || key[l] % 8)
+            return fail(DSPARK_ERR_INVALID_ARG, "tables_update_slots: layer %d mapping null or misaligned", l);
+    }
+    if (key == t->slot_key)
+        return ok();  // the same mappings as the table already holds
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    cudaError_t e = cudaStreamIsCapturing(stream, &cap);
+    if (e != cudaSuccess)
+        return fail(DSPARK_ERR_CUDA, "tables_update_slots: %s", cudaGetErrorString(e));
+    if (cap != cudaStreamCaptureStatusNone)
+        return fail(DSPARK_ERR_CAPTURING, "tables_update_slots: the slot mappings moved while the stream is capturing");
+    e = cudaMemcpyAsync(t->d_slots, layer_slot_ptrs, sizeof(int64_t *) * L, cudaMemcpyHostToDevice, stream);
+    if (e != cudaSuccess)
+        return fail(DSPARK_ERR_CUDA, "tables_update_slots: %s", cudaGetErrorString(e));
+    t->slot_key.swap(key);
+    t->builds++;
+    return ok();
+}
+
+const int64_t *const *dspark_ctx_kv_tables_layer_slots(const dspark_ctx_kv_tables *t)
+{
+    return t ? t->d_slots : nullptr;
+}
+
 const int64_t *dspark_ctx_kv_tables_cache_offsets(const dspark_ctx_kv_tables *t)
 {
     return t ? t->d_offsets : nullptr;
@@ -556,6 +637,7 @@ void dspark_ctx_kv_tables_destroy(dspark_ctx_kv_tables *t)
                     cudaSetDevice(t->device) == cudaSuccess;
     cudaFree(t->d_offsets);
     cudaFree(t->d_scales);
+    cudaFree(t->d_slots);
     if (switched)
         cudaSetDevice(prev);
     delete t;

@@ -18,7 +18,8 @@ struct CtxKvParams {
     const uint16_t *all_kv;      // bf16 bits [T, L, 2, H, 128]
     const uint16_t *knorm_w;     // bf16 bits [L, 128]
     const int64_t *positions;    // [T]
-    const int64_t *slot_mapping; // [T]
+    const int64_t *slot_mapping; // [T], shared by every layer (unused when layer_slots is set)
+    const int64_t *const *layer_slots; // [L] device pointers to per-layer [T] slot mappings, or null
     const uint16_t *cos_sin;     // bf16 bits [max_pos, rotary_dim]
     unsigned char *cache0;       // layer 0 cache base
     const int64_t *cache_offsets;     // [L] element offsets
@@ -40,7 +41,8 @@ struct CtxKvParams {
 cudaError_t launch_ctx_kv_write(const CtxKvParams &p, int rotary_dim, bool fp8, cudaStream_t stream);
 
 // Pipelined bulk-copy kernel: handles up to 32 layers and up to 64 KV heads
-// (one layer's K|V rows of a token fit a 32 KB stage).
+// (one layer's K|V rows of a token fit a 32 KB stage); with per-layer slot
+// mappings each unit is one (token, layer).
 bool tma_path_supported(const CtxKvParams &p);
 cudaError_t launch_ctx_kv_write_tma(const CtxKvParams &p, int rotary_dim, bool fp8, cudaStream_t stream);
 

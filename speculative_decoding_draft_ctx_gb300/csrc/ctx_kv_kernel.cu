@@ -28,7 +28,9 @@
 //     y_partner*s of two bf16 values is exact in fp32);
 //   fp8: x / scale as an IEEE fp32 division, then a saturating RNE pack to
 //     e4m3 pairs (cvt.rn.satfinite.e4m3x2.f32 via cuda_fp8.h).
-// Rows whose slot or position is out of range are skipped and reported
+// With per-layer slot mappings the slot of (t, l) comes from layer l's
+// mapping (a device pointer table).  Rows whose slot or position is out of
+// range are skipped and reported
 // through the optional error word; no access leaves the caller's buffers.
 #include <cuda_bf16.h>
 #include <cuda_fp8.h>
@@ -131,7 +133,10 @@ __global__ void __launch_bounds__(kThreads) ctx_kv_write_kernel(const CtxKvParam
         const int l = rem / HC;
         const int h0 = (rem - l * HC) * kHeadsPerUnit;
         const int nh = min(kHeadsPerUnit, H - h0);
-        const int64_t slot = __ldg(p.slot_mapping + t);
+        const int64_t slot =
+            p.layer_slots ? __ldg(reinterpret_cast<const int64_t *>(__ldg(
+                                reinterpret_cast<const unsigned long long *>(p.layer_slots) + l)) + t)
+                          : __ldg(p.slot_mapping + t);
         if (slot < 0)
             continue;  // padding: neither read nor written
         const int64_t pos = __ldg(p.positions + t);

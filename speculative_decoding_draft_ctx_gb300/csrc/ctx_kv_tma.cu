@@ -7,7 +7,8 @@
 // layer's [num_blocks, nkv, block_size, 256] cache as bf16 or fp8 e4m3 of
 // x / scale, slots < 0 not written).
 //
-// Data movement.  all_kv[t, l0 : l0 + Lp] -- every K and V row of Lp layers of
+// Data movement (with per-layer slot mappings Lp is 1 and every unit reads
+// its own layer's slot).  all_kv[t, l0 : l0 + Lp] -- every K and V row of Lp layers of
 // one token -- is one contiguous block of Lp * nkv * 512 bytes.  Each CTA runs
 // a ring of shared-memory stages: a producer warp reads the slot and position
 // of its next tokens, skips padding (nothing of a padded token is read), and
@@ -301,7 +302,14 @@ __global__ void __launch_bounds__(kThreads, 2) ctx_kv_tma_kernel(const TmaParams
             pos = 0;
             if (u < u_end) {
                 const long long t = NP == 1 ? u : u / NP;
-                slot = __ldg(p.slot_mapping + t);
+                if (p.layer_slots) {  // one layer per unit, its own mapping
+                    const int l = (int)(u - t * NP);
+                    slot = __ldg(reinterpret_cast<const int64_t *>(
+                               __ldg(reinterpret_cast<const unsigned long long *>(p.layer_slots) + l)) +
+                           t);
+                } else {
+                    slot = __ldg(p.slot_mapping + t);
+                }
                 pos = __ldg(p.positions + t);
             }
         };
@@ -309,7 +317,9 @@ __global__ void __launch_bounds__(kThreads, 2) ctx_kv_tma_kernel(const TmaParams
             if (slot < 0)
                 return;
             const long long u = base + (long long)lane * step;
-            const bool first_piece = NP == 1 || u % NP == 0;
+            // a token's slot is reported once (by its first piece), a
+            // per-layer slot by its own unit
+            const bool first_piece = NP == 1 || p.layer_slots != nullptr || u % NP == 0;
             if (slot >= p.capacity) {
                 if (first_piece)
                     flags |= kFlagSlot;
@@ -591,16 +601,19 @@ bool plan_for(const CtxKvParams &p, Plan &pl)
     const int row_bytes = H * 512;
     if (row_bytes > kMaxSlabBytes || L > kMaxTmaLayers)
         return false;
-    pl.Lp = std::min(L, kMaxSlabBytes / row_bytes);
+    // per-layer slot mappings: one layer per unit (each unit has one slot)
+    pl.Lp = p.layer_slots ? 1 : std::min(L, kMaxSlabBytes / row_bytes);
     pl.NP = (L + pl.Lp - 1) / pl.Lp;
     // Three stages measured best on the bf16 long-context workload and as good
     // as four on the fp8 prefill one (a deeper ring of reads in flight slowed
     // the write-heavy bf16 workload); fewer when three would not leave room
-    // for two CTAs per SM.
+    // for two CTAs per SM.  Single-layer stages are small: up to about 48 KB
+    // of them per CTA keep as many bytes in flight.
     const Layout one = make_layout(L, 1, (uint32_t)pl.Lp * row_bytes);
     const int fixed = (int)one.stages;
+    const int cap = pl.Lp * row_bytes >= 8192 ? kStages : std::max(kStages, 49152 / (int)one.stage_bytes);
     int S = (kStageBudget - fixed) / (int)one.stage_bytes;
-    S = S < 2 ? 2 : (S > kStages ? kStages : S);
+    S = S < 2 ? 2 : (S > cap ? cap : S);
     pl.S = S;
     pl.lay = make_layout(L, S, (uint32_t)pl.Lp * row_bytes);
     return pl.lay.total <= 113 * 1024;

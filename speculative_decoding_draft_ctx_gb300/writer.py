@@ -14,7 +14,8 @@ from __future__ import annotations
 from ._binding import (
     HEAD_DIM, DSparkError, Tables, cache_desc, dspark_ctx_kv_rotary_dims_supported,
     dspark_ctx_kv_project, dspark_ctx_kv_project_write, dspark_ctx_kv_validate_layers, dspark_ctx_kv_write,
-    dspark_ctx_kv_write_ex, dspark_gemma_rms_norm, dspark_qknorm_rope_kv_insert, kv_dtype_code,
+    dspark_ctx_kv_write_ex, dspark_ctx_kv_write_layer_slots, dspark_gemma_rms_norm, dspark_qknorm_rope_kv_insert,
+    kv_dtype_code,
 )
 
 
@@ -66,13 +67,32 @@ class ContextKVWriter:
 
     def __call__(self, all_kv, k_norm_weight, eps, positions, cos_sin_cache, rotary_dim, slot_mapping,
                  stream=None, error_flags=None):
+        """``slot_mapping``: one int64 tensor shared by every layer, or a list
+        of one per layer (the same tensor everywhere counts as shared, like
+        the pages' _shared_slot_mapping; otherwise each layer's rows go to
+        its own slots)."""
         num_ctx, L, two, nkv, hd = all_kv.shape
         if L != self.num_layers or nkv != self.num_kv_heads or two != 2 or hd != HEAD_DIM:
             raise DSparkError(1, f"all_kv shape {tuple(all_kv.shape)} does not match the layers")
         if num_ctx == 0:
             return
+        per_layer = None
+        if isinstance(slot_mapping, (list, tuple)):
+            if len(slot_mapping) != L or any(s is None for s in slot_mapping):
+                raise DSparkError(1, "one slot mapping per layer expected")
+            if all(s.data_ptr() == slot_mapping[0].data_ptr() for s in slot_mapping):
+                slot_mapping = slot_mapping[0]
+            else:
+                per_layer = slot_mapping
         self.ensure_tables(stream)
         t = self._tables
+        if per_layer is not None:
+            t.update_slots(per_layer, stream)
+            dspark_ctx_kv_write_layer_slots(all_kv, k_norm_weight, positions, t.layer_slots, num_ctx,
+                                            cos_sin_cache, cos_sin_cache.shape[0], self.kv_caches[0],
+                                            self.num_blocks, t.cache_offsets, t.k_scales, t.v_scales, L, nkv,
+                                            self.block_size, rotary_dim, eps, self._dtype, error_flags, stream)
+            return
         args = (all_kv, k_norm_weight, positions, slot_mapping, num_ctx, cos_sin_cache,
                 cos_sin_cache.shape[0], self.kv_caches[0], self.num_blocks, t.cache_offsets,
                 t.k_scales, t.v_scales, L, nkv, self.block_size, rotary_dim, eps, self._dtype)

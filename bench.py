@@ -72,6 +72,8 @@ def parse_args(argv=None):
     ap.add_argument("--num-blocks", type=int, default=None, help="with --num-ctx: fewer cache blocks")
     ap.add_argument("--graph", action="store_true",
                     help="replay the timed steps from one CUDA graph (launch-bound small workloads)")
+    ap.add_argument("--layer-slots", type=int, default=0, metavar="G",
+                    help="context write: layers split over G KV-cache groups, one slot mapping per group")
     return ap.parse_args(argv)
 
 
@@ -407,11 +409,28 @@ def run_ours(args):
     writer = dk.ContextKVWriter(caches, k_scales, v_scales, "fp8" if fp8 else "auto")
     stream = torch.cuda.current_stream()
 
+    if args.layer_slots:
+        for d in sets:
+            ls = wk.layer_slot_mappings(d.to("cpu"), groups=args.layer_slots).to(dev)
+            d.extra["slots"] = [ls[l] for l in range(wl.num_layers)]
+        # every layer's rows are written at its own group's slots: the valid rows of each layer count
+        step_rows = int(sum(int((s >= 0).sum()) for s in sets[0].extra["slots"])) * wl.num_kv_heads
+        valid_layer_tokens = step_rows // wl.num_kv_heads
+        step_bytes = (valid_layer_tokens * wl.num_kv_heads * (2 * wk.ROW_ELEMS + wk.ROW_ELEMS * wl.elem_size) +
+                      wk.compulsory_bytes(wl, 0) + base.num_valid_tokens * (8 + 2 * wl.rotary_dim) +
+                      8 * wl.num_ctx * (wl.num_layers - 1))
+
+    # per-layer mappings: each input set has its own slot tensors, so its own
+    # writer (and pointer table): nothing is rebuilt while a graph captures
+    writers = ([dk.ContextKVWriter(caches, k_scales, v_scales, "fp8" if fp8 else "auto") for _ in range(n_sets)]
+               if args.layer_slots else [writer])
+
     def step(i):
         d = sets[i % n_sets]
-        writer(d.all_kv, d.knorm_w, d.eps, d.positions, d.cos_sin, wl.rotary_dim, d.slot_mapping)
+        slots = d.extra["slots"] if args.layer_slots else d.slot_mapping
+        writers[i % len(writers)](d.all_kv, d.knorm_w, d.eps, d.positions, d.cos_sin, wl.rotary_dim, slots)
 
-    for i in range(args.warmup):
+    for i in range(max(args.warmup, n_sets if args.layer_slots else 0)):
         step(i)
     torch.cuda.synchronize()
 
@@ -459,7 +478,7 @@ def run_ours(args):
 
     peak, peak_kind = measured_peaks()
     achieved = step_bytes / (avg_launch_ms * 1e-3) / 1e9
-    traffic = recorded_traffic(wl.name)
+    traffic = None if args.layer_slots else recorded_traffic(wl.name)
     copy_gbs = copy_same_bytes(step_bytes, dev, stream)
 
     # end to end through the public API: pinned host inputs copied in, the
@@ -513,6 +532,8 @@ def run_ours(args):
             "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
             "config": dict(wk.describe(wl), parallelism=f"replicas{ws}", input_sets=n_sets,
+                           slot_mappings=(f"per layer, {args.layer_slots} KV-cache groups" if args.layer_slots
+                                          else "shared"),
                            timing="one CUDA graph of all steps" if graph is not None else "CUDA events per launch",
                            l2=("inputs larger than L2" if n_sets == 1 else
                                f"{n_sets} input sets rotated, footprint > 3x L2")),

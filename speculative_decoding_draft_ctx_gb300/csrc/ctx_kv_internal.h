@@ -41,8 +41,8 @@ struct CtxKvParams {
 cudaError_t launch_ctx_kv_write(const CtxKvParams &p, int rotary_dim, bool fp8, cudaStream_t stream);
 
 // Pipelined bulk-copy kernel: handles up to 32 layers and up to 64 KV heads
-// (one layer's K|V rows of a token fit a 32 KB stage); with per-layer slot
-// mappings each unit is one (token, layer).
+// (one layer's K|V rows of a token fit a 32 KB stage), with a shared or a
+// per-layer slot mapping.
 bool tma_path_supported(const CtxKvParams &p);
 cudaError_t launch_ctx_kv_write_tma(const CtxKvParams &p, int rotary_dim, bool fp8, cudaStream_t stream);
 

@@ -7,8 +7,7 @@
 // layer's [num_blocks, nkv, block_size, 256] cache as bf16 or fp8 e4m3 of
 // x / scale, slots < 0 not written).
 //
-// Data movement (with per-layer slot mappings Lp is 1 and every unit reads
-// its own layer's slot).  all_kv[t, l0 : l0 + Lp] -- every K and V row of Lp layers of
+// Data movement.  all_kv[t, l0 : l0 + Lp] -- every K and V row of Lp layers of
 // one token -- is one contiguous block of Lp * nkv * 512 bytes.  Each CTA runs
 // a ring of shared-memory stages: a producer warp reads the slot and position
 // of its next tokens, skips padding (nothing of a padded token is read), and
@@ -30,6 +29,13 @@
 // scale with one FMA correction step (Markstein's method: q0 = x*(1/s),
 // e = x - q0*s exactly, q = q0 + e*(1/s)), which yields the correctly rounded
 // fp32 quotient, then a saturating RNE pack to e4m3 pairs.
+//
+// Per-layer slot mappings (drafts whose layers span several KV-cache
+// groups): the producer prefetches each unit's per-layer slots one batch
+// ahead into a double-buffered shared table and writes a row offset per
+// layer into the stage (< 0: that layer is padding); a unit is copied when
+// any of its layers has a slot, and the consumers skip the padded layers'
+// rows.
 //
 // Every wait on an mbarrier is bounded (globaltimer); on expiry the CTA sets
 // DSPARK_FLAG_TIMEOUT, stops, waits (bounded) for its own copies in flight
@@ -204,12 +210,16 @@ __device__ __forceinline__ uint64_t rope_bf2(uint32_t y, uint32_t c, uint32_t yp
 // Shared-memory layout (dynamic): barriers and headers, per-layer tables,
 // then the stages (128-byte aligned).
 struct Layout {
-    uint32_t full, empty, hdr, abort, w1, off, scl, stages, stage_bytes, slab_bytes, total;
+    uint32_t full, empty, hdr, abort, w1, off, scl, pls, pdst, stages, stage_bytes, slab_bytes, total;
 };
 
 __host__ __device__ inline uint32_t align_up(uint32_t v, uint32_t a) { return (v + a - 1) / a * a; }
 
-__host__ __device__ inline Layout make_layout(int L, int S, uint32_t slab_bytes)
+// pl: layers per unit when every layer has its own slot mapping (then the
+// producer prefetches each unit's per-layer slots into a double-buffered
+// [2][32][pl] table and hands the consumers per-layer row offsets [S][pl]),
+// else 0.
+__host__ __device__ inline Layout make_layout(int L, int S, uint32_t slab_bytes, int pl = 0)
 {
     Layout y;
     uint32_t o = 0;
@@ -227,6 +237,10 @@ __host__ __device__ inline Layout make_layout(int L, int S, uint32_t slab_bytes)
     o = y.off + 8 * L;
     y.scl = align_up(o, 16);  // per layer, 48 bytes: (k, k), (v, v), (-1/k, -1/k), (-1/v, -1/v), k bound, v bound
     o = y.scl + 48 * L;
+    y.pls = align_up(o, 16);
+    o = y.pls + 2 * 32 * 8 * pl;
+    y.pdst = align_up(o, 16);
+    o = y.pdst + 8 * S * pl;
     y.stages = align_up(o, 128);
     y.slab_bytes = slab_bytes;
     y.stage_bytes = align_up(slab_bytes + kCsBytes, 128);
@@ -254,7 +268,8 @@ __global__ void __launch_bounds__(kThreads, 2) ctx_kv_tma_kernel(const TmaParams
     extern __shared__ __align__(128) unsigned char smem[];
     const CtxKvParams &p = tp.p;
     const int L = p.num_layers, H = p.num_kv_heads, S = tp.stages, NP = tp.pieces, Lp = tp.layers_per_piece;
-    const Layout lay = make_layout(L, S, (uint32_t)Lp * H * 512u);
+    const bool PL = p.layer_slots != nullptr;  // one slot mapping per layer
+    const Layout lay = make_layout(L, S, (uint32_t)Lp * H * 512u, PL ? Lp : 0);
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + lay.full);
     uint64_t *empty = reinterpret_cast<uint64_t *>(smem + lay.empty);
     StageHdr *hdr = reinterpret_cast<StageHdr *>(smem + lay.hdr);
@@ -263,6 +278,8 @@ __global__ void __launch_bounds__(kThreads, 2) ctx_kv_tma_kernel(const TmaParams
     unsigned char **layer_base = reinterpret_cast<unsigned char **>(smem + lay.off);
     uint32_t *scl = reinterpret_cast<uint32_t *>(smem + lay.scl);
     unsigned char *stages = smem + lay.stages;
+    long long *pls = reinterpret_cast<long long *>(smem + lay.pls);    // [2][32][Lp] prefetched per-layer slots
+    long long *pdst = reinterpret_cast<long long *>(smem + lay.pdst);  // [S][Lp] per-layer row offsets (< 0: none)
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     if (tid == 0) {
@@ -296,37 +313,67 @@ __global__ void __launch_bounds__(kThreads, 2) ctx_kv_tma_kernel(const TmaParams
             u_end = units;
             step = G;
         }
-        auto fetch = [&](long long base, long long &slot, long long &pos) {
+        // row offset of a slot's (block, offset) row for head 0 within a layer's cache
+        auto row_off = [&](long long slot) {
+            return (((slot >> p.block_size_log2) * H << p.block_size_log2) +
+                    (slot & ((1LL << p.block_size_log2) - 1))) *
+                   (FP8 ? kRowElems : 2 * kRowElems);
+        };
+        // Slot and position of unit base + lane * step.  With per-layer
+        // mappings the unit's layers' slots go to the prefetch table (buffer
+        // buf) and `slot` only says whether any of them is valid.
+        auto fetch = [&](long long base, long long &slot, long long &pos, int buf) {
             const long long u = base + (long long)lane * step;
             slot = -1;
             pos = 0;
             if (u < u_end) {
                 const long long t = NP == 1 ? u : u / NP;
-                if (p.layer_slots) {  // one layer per unit, its own mapping
-                    const int l = (int)(u - t * NP);
-                    slot = __ldg(reinterpret_cast<const int64_t *>(
-                               __ldg(reinterpret_cast<const unsigned long long *>(p.layer_slots) + l)) +
-                           t);
+                pos = __ldg(p.positions + t);
+                if (PL) {
+                    const int l0 = (NP == 1 ? 0 : (int)(u - t * NP)) * Lp;
+                    const int n = min(Lp, L - l0);
+                    long long *e = pls + (buf * 32 + lane) * Lp;
+                    bool any = false;
+                    for (int j = 0; j < n; j++) {
+                        const long long sj = __ldg(reinterpret_cast<const int64_t *>(__ldg(
+                                                       reinterpret_cast<const unsigned long long *>(p.layer_slots) +
+                                                       l0 + j)) +
+                                                   t);
+                        e[j] = sj;
+                        any |= sj >= 0;
+                    }
+                    slot = any ? 0 : -1;
                 } else {
                     slot = __ldg(p.slot_mapping + t);
                 }
-                pos = __ldg(p.positions + t);
             }
         };
-        auto vet = [&](long long base, long long &slot, long long pos) {
+        auto vet = [&](long long base, long long &slot, long long pos, int buf) {
             if (slot < 0)
                 return;
             const long long u = base + (long long)lane * step;
-            // a token's slot is reported once (by its first piece), a
-            // per-layer slot by its own unit
-            const bool first_piece = NP == 1 || p.layer_slots != nullptr || u % NP == 0;
-            if (slot >= p.capacity) {
-                if (first_piece)
-                    flags |= kFlagSlot;
-                slot = -1;
-            } else if (pos < 0 || pos >= p.max_pos) {
+            const bool first_piece = NP == 1 || u % NP == 0;  // a token is reported once
+            if (pos < 0 || pos >= p.max_pos) {
                 if (first_piece)
                     flags |= kFlagPos;
+                slot = -1;
+            } else if (PL) {
+                const long long t = NP == 1 ? u : u / NP;
+                const int n = min(Lp, L - (NP == 1 ? 0 : (int)(u - t * NP)) * Lp);
+                long long *e = pls + (buf * 32 + lane) * Lp;
+                bool any = false;
+                for (int j = 0; j < n; j++) {
+                    if (e[j] >= p.capacity) {
+                        flags |= kFlagSlot;
+                        e[j] = -1;
+                    }
+                    any |= e[j] >= 0;
+                }
+                if (!any)
+                    slot = -1;
+            } else if (slot >= p.capacity) {
+                if (first_piece)
+                    flags |= kFlagSlot;
                 slot = -1;
             }
         };
@@ -362,12 +409,14 @@ __global__ void __launch_bounds__(kThreads, 2) ctx_kv_tma_kernel(const TmaParams
         }
         long long base = u_first;
         long long ordinal = 0;  // index of unit `base` in this CTA's sequence
-        fetch(base, cur_slot, cur_pos);
-        for (; base < u_end && ok; base += 32 * step, ordinal += 32) {
+        int buf = 0;            // prefetch-table buffer of the batch at `base`
+        fetch(base, cur_slot, cur_pos, buf);
+        for (; base < u_end && ok; base += 32 * step, ordinal += 32, buf ^= 1) {
             const long long nbase = base + 32 * step;
             if (nbase < u_end)
-                fetch(nbase, nxt_slot, nxt_pos);
-            vet(base, cur_slot, cur_pos);
+                fetch(nbase, nxt_slot, nxt_pos, buf ^ 1);
+            vet(base, cur_slot, cur_pos, buf);
+            __syncwarp();  // lane 0 reads the other lanes' prefetched slots below
             for (int i = 0; i < 32; i++) {
                 const long long u = base + (long long)i * step;
                 if (u >= u_end)
@@ -390,9 +439,13 @@ __global__ void __launch_bounds__(kThreads, 2) ctx_kv_tma_kernel(const TmaParams
                             hdr[s].rows = 0;  // a speculatively copied padded unit: release it unread
                             mbar_arrive(full + s);
                         } else {
-                            hdr[s].dst = (((slot >> p.block_size_log2) * H << p.block_size_log2) +
-                                          (slot & ((1LL << p.block_size_log2) - 1))) *
-                                         (FP8 ? kRowElems : 2 * kRowElems);
+                            if (PL) {
+                                const long long *e = pls + (buf * 32 + i) * Lp;
+                                for (int j = 0; j < (int)(slab / 512u) / H; j++)
+                                    pdst[s * Lp + j] = e[j] >= 0 ? row_off(e[j]) : -1;
+                            } else {
+                                hdr[s].dst = row_off(slot);
+                            }
                             hdr[s].l0 = l0;
                             hdr[s].rows = (int)(slab / 512u);
                             if (spec) {
@@ -554,9 +607,10 @@ __global__ void __launch_bounds__(kThreads, 2) ctx_kv_tma_kernel(const TmaParams
                         const uint32_t rv = f2_to_bf2(rope_bf2(y[j], cw[j], yp, sw[j]));
                         ko[j] = rot_lane ? rv : y[j];  // both computed: a select, not a branch
                     }
-                    if (!active)
-                        continue;
-                    unsigned char *d = layer_base[l] + h_s.dst + h * head_bytes;
+                    const long long roff = PL ? pdst[s * Lp + lr] : h_s.dst;
+                    if (!active || roff < 0)
+                        continue;  // past the stage's rows, or a layer padded in its own mapping
+                    unsigned char *d = layer_base[l] + roff + h * head_bytes;
                     if (!FP8) {
                         st_stream_v4(d + 16 * q, make_uint4(ko[0], ko[1], ko[2], ko[3]));
                         st_stream_v4(d + 128 + 16 * q, make_uint4(y[4], y[5], y[6], y[7]));
@@ -601,21 +655,19 @@ bool plan_for(const CtxKvParams &p, Plan &pl)
     const int row_bytes = H * 512;
     if (row_bytes > kMaxSlabBytes || L > kMaxTmaLayers)
         return false;
-    // per-layer slot mappings: one layer per unit (each unit has one slot)
-    pl.Lp = p.layer_slots ? 1 : std::min(L, kMaxSlabBytes / row_bytes);
+    pl.Lp = std::min(L, kMaxSlabBytes / row_bytes);
     pl.NP = (L + pl.Lp - 1) / pl.Lp;
+    const int pl_tab = p.layer_slots ? pl.Lp : 0;
     // Three stages measured best on the bf16 long-context workload and as good
     // as four on the fp8 prefill one (a deeper ring of reads in flight slowed
     // the write-heavy bf16 workload); fewer when three would not leave room
-    // for two CTAs per SM.  Single-layer stages are small: up to about 48 KB
-    // of them per CTA keep as many bytes in flight.
-    const Layout one = make_layout(L, 1, (uint32_t)pl.Lp * row_bytes);
+    // for two CTAs per SM.
+    const Layout one = make_layout(L, 1, (uint32_t)pl.Lp * row_bytes, pl_tab);
     const int fixed = (int)one.stages;
-    const int cap = pl.Lp * row_bytes >= 8192 ? kStages : std::max(kStages, 49152 / (int)one.stage_bytes);
     int S = (kStageBudget - fixed) / (int)one.stage_bytes;
-    S = S < 2 ? 2 : (S > cap ? cap : S);
+    S = S < 2 ? 2 : (S > kStages ? kStages : S);
     pl.S = S;
-    pl.lay = make_layout(L, S, (uint32_t)pl.Lp * row_bytes);
+    pl.lay = make_layout(L, S, (uint32_t)pl.Lp * row_bytes, pl_tab);
     return pl.lay.total <= 113 * 1024;
 }
 

@@ -225,27 +225,35 @@ def l2_bytes() -> int:
 
 
 def copy_same_bytes(step_bytes: int, dev, stream, launches: int = 50) -> float:
-    """GB/s of PyTorch's own copy kernel when one launch moves the same number
-    of bytes as one write step (half read, half written), timed per launch
-    with CUDA events on rotated buffers that together exceed L2: the
-    streaming rate a single launch of this size reaches on this GPU, for
-    context beside the long-copy peak."""
+    """GB/s of PyTorch's own copy when one launch moves the same number of
+    bytes as one write step (half read, half written), replayed from one CUDA
+    graph (no host gaps, even for a few-MB copy) on rotated buffers that
+    together exceed L2: the streaming rate a single launch of this size
+    reaches on this GPU, for context beside the long-copy peak."""
     half = max(16, (step_bytes // 2) // 16 * 16)
     n_sets = max(1, math.ceil(3 * l2_bytes() / (2 * half)))
     bufs = [(torch.empty(half // 2, dtype=torch.bfloat16, device=dev).fill_(1.0),
              torch.empty(half // 2, dtype=torch.bfloat16, device=dev)) for _ in range(n_sets)]
     for i in range(5):
         bufs[i % n_sets][1].copy_(bufs[i % n_sets][0])
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(launches)]
     torch.cuda.synchronize()
-    for i, (e0, e1) in enumerate(ev):
-        src, dst = bufs[i % n_sets]
-        e0.record(stream)
-        dst.copy_(src)
-        e1.record(stream)
+    side = torch.cuda.Stream()
+    side.wait_stream(stream)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=side):
+        for i in range(launches):
+            src, dst = bufs[i % n_sets]
+            dst.copy_(src)
+    stream.wait_stream(side)
+    graph.replay()
     torch.cuda.synchronize()
-    ms = sum(e0.elapsed_time(e1) for e0, e1 in ev) / launches
-    del bufs
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    graph.replay()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / launches
+    del graph, bufs
     return 2 * half / (ms * 1e-3) / 1e9
 
 

@@ -262,13 +262,14 @@ struct TmaParams {
 // 64 + 8q..), so the 8 lanes of a row read 128 contiguous bytes per load.
 __device__ __forceinline__ int w1_slot(int l, int jj, int c) { return l * 32 + jj * 16 + c; }
 
-template <int ROT, bool FP8>
+// PL: every layer has its own slot mapping (p.layer_slots); a template
+// parameter, so the shared-mapping path carries none of its branches.
+template <int ROT, bool FP8, bool PL>
 __global__ void __launch_bounds__(kThreads, 2) ctx_kv_tma_kernel(const TmaParams tp)
 {
     extern __shared__ __align__(128) unsigned char smem[];
     const CtxKvParams &p = tp.p;
     const int L = p.num_layers, H = p.num_kv_heads, S = tp.stages, NP = tp.pieces, Lp = tp.layers_per_piece;
-    const bool PL = p.layer_slots != nullptr;  // one slot mapping per layer
     const Layout lay = make_layout(L, S, (uint32_t)Lp * H * 512u, PL ? Lp : 0);
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + lay.full);
     uint64_t *empty = reinterpret_cast<uint64_t *>(smem + lay.empty);
@@ -671,7 +672,7 @@ bool plan_for(const CtxKvParams &p, Plan &pl)
     return pl.lay.total <= 113 * 1024;
 }
 
-template <int ROT, bool FP8>
+template <int ROT, bool FP8, bool PL>
 cudaError_t launch_tma_variant(const TmaParams &tp, uint32_t smem_bytes, cudaStream_t stream)
 {
     static std::mutex mu;
@@ -692,7 +693,7 @@ cudaError_t launch_tma_variant(const TmaParams &tp, uint32_t smem_bytes, cudaStr
                 return e;
         }
         if (smem_set[dev] < smem_bytes) {
-            e = cudaFuncSetAttribute(ctx_kv_tma_kernel<ROT, FP8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+            e = cudaFuncSetAttribute(ctx_kv_tma_kernel<ROT, FP8, PL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      (int)smem_bytes);
             if (e != cudaSuccess)
                 return e;
@@ -703,8 +704,26 @@ cudaError_t launch_tma_variant(const TmaParams &tp, uint32_t smem_bytes, cudaStr
     const long long units = tp.p.num_ctx * (long long)tp.pieces;
     const long long want = 2LL * sms;
     const int blocks = (int)(units < want ? units : want);
-    ctx_kv_tma_kernel<ROT, FP8><<<blocks, kThreads, smem_bytes, stream>>>(tp);
+    ctx_kv_tma_kernel<ROT, FP8, PL><<<blocks, kThreads, smem_bytes, stream>>>(tp);
     return cudaGetLastError();
+}
+
+template <bool PL>
+cudaError_t launch_rot(const TmaParams &tp, int rotary_dim, bool fp8, uint32_t smem, cudaStream_t stream)
+{
+    switch (rotary_dim) {
+    case 16:
+        return fp8 ? launch_tma_variant<16, true, PL>(tp, smem, stream)
+                   : launch_tma_variant<16, false, PL>(tp, smem, stream);
+    case 32:
+        return fp8 ? launch_tma_variant<32, true, PL>(tp, smem, stream)
+                   : launch_tma_variant<32, false, PL>(tp, smem, stream);
+    case 64:
+        return fp8 ? launch_tma_variant<64, true, PL>(tp, smem, stream)
+                   : launch_tma_variant<64, false, PL>(tp, smem, stream);
+    default:
+        return cudaErrorInvalidValue;
+    }
 }
 
 }  // namespace
@@ -728,16 +747,9 @@ cudaError_t launch_ctx_kv_write_tma(const CtxKvParams &p, int rotary_dim, bool f
     tp.h_magic = (0x100000000ull + p.num_kv_heads - 1) / (uint64_t)p.num_kv_heads;
     tp.contiguous = 0;
     const uint32_t smem = pl.lay.total;
-    switch (rotary_dim) {
-    case 16:
-        return fp8 ? launch_tma_variant<16, true>(tp, smem, stream) : launch_tma_variant<16, false>(tp, smem, stream);
-    case 32:
-        return fp8 ? launch_tma_variant<32, true>(tp, smem, stream) : launch_tma_variant<32, false>(tp, smem, stream);
-    case 64:
-        return fp8 ? launch_tma_variant<64, true>(tp, smem, stream) : launch_tma_variant<64, false>(tp, smem, stream);
-    default:
-        return cudaErrorInvalidValue;
-    }
+    if (p.layer_slots)
+        return launch_rot<true>(tp, rotary_dim, fp8, smem, stream);
+    return launch_rot<false>(tp, rotary_dim, fp8, smem, stream);
 }
 
 }  // namespace dspark

@@ -31,8 +31,9 @@ _LIB_PATH = os.path.join(_HERE, "libctx_kv_oracle.so")
 
 KV_BF16 = 0
 KV_FP8_E4M3 = 1
-HEAD_DIM = 128
+HEAD_DIM = 128          # the pages' head dim
 ROW = 256
+MAX_HEAD_DIM = 256      # the general write's largest head dim
 
 ERRORS = {
     0: "ok", -1: "bad argument", -2: "slot beyond the cache", -3: "duplicate valid slot",
@@ -68,6 +69,7 @@ class OracleInputs(ctypes.Structure):
         ("num_layers", ctypes.c_int32), ("num_kv_heads", ctypes.c_int32),
         ("block_size", ctypes.c_int32), ("rotary_dim", ctypes.c_int32),
         ("kv_dtype", ctypes.c_int32), ("eps", ctypes.c_float), ("layer_slots", ctypes.c_void_p),
+        ("head_dim", ctypes.c_int32),
     ]
 
 
@@ -87,6 +89,8 @@ def lib():
         L.dspark_oracle_e4m3_rne_sat.restype = ctypes.c_uint8
         L.dspark_oracle_gemma_knorm.argtypes = [P, P, ctypes.c_float, P, P]
         L.dspark_oracle_gemma_knorm.restype = ctypes.c_int
+        L.dspark_oracle_gemma_knorm_n.argtypes = [P, P, ctypes.c_int, ctypes.c_float, P, P]
+        L.dspark_oracle_gemma_knorm_n.restype = ctypes.c_int
         L.dspark_oracle_rope_pair.argtypes = [ctypes.c_uint16] * 4 + [P, P]
         L.dspark_oracle_rope_pair.restype = None
         L.dspark_oracle_row.argtypes = [P, ctypes.c_int64, ctypes.c_int32, ctypes.c_int32, P, P, P, P]
@@ -186,13 +190,19 @@ def project_context_kv(x_bits: np.ndarray, w_bits: np.ndarray) -> np.ndarray:
 
 
 def gemma_knorm(k_bits: np.ndarray, w_bits: np.ndarray, eps: float):
-    """Step 2 on one 128-element K row (bf16 bits) -> (y, y_alt, n_ambiguous)."""
+    """Step 2 on one K row (bf16 bits; 128 elements through the pages' entry
+    point, any other length through the head-dim general one)
+    -> (y, y_alt, n_ambiguous)."""
     k = np.ascontiguousarray(k_bits, dtype=np.uint16)
     w = np.ascontiguousarray(w_bits, dtype=np.uint16)
-    assert k.shape == (HEAD_DIM,) and w.shape == (HEAD_DIM,)
-    y = np.empty(HEAD_DIM, np.uint16)
-    ya = np.empty(HEAD_DIM, np.uint16)
-    n = lib().dspark_oracle_gemma_knorm(_ptr(k), _ptr(w), ctypes.c_float(eps), _ptr(y), _ptr(ya))
+    assert k.ndim == 1 and w.shape == k.shape and 1 <= k.shape[0] <= MAX_HEAD_DIM
+    D = k.shape[0]
+    y = np.empty(D, np.uint16)
+    ya = np.empty(D, np.uint16)
+    if D == HEAD_DIM:
+        n = lib().dspark_oracle_gemma_knorm(_ptr(k), _ptr(w), ctypes.c_float(eps), _ptr(y), _ptr(ya))
+    else:
+        n = lib().dspark_oracle_gemma_knorm_n(_ptr(k), _ptr(w), D, ctypes.c_float(eps), _ptr(y), _ptr(ya))
     return y, ya, n
 
 
@@ -213,16 +223,19 @@ def dest_row(slot: int, h: int, num_kv_heads: int, block_size: int, num_blocks: 
 class Problem:
     """Host copies of one write call's inputs, kept alive for the C side.
 
-    Arrays: all_kv / knorm_w / cos_sin as uint16 bf16 bits, positions and
-    slot_mapping int64, k_scale / v_scale float32 ``[L]``."""
+    Arrays: all_kv ``[T, L, 2, H, D]`` / knorm_w ``[L, D]`` / cos_sin as
+    uint16 bf16 bits, positions and slot_mapping int64, k_scale / v_scale
+    float32 ``[L]``.  The head dim D is all_kv's last extent (128 on the
+    pages); cache rows hold 2D elements."""
 
     def __init__(self, all_kv, knorm_w, positions, slot_mapping, cos_sin, k_scale, v_scale,
                  *, num_blocks: int, block_size: int, rotary_dim: int, kv_dtype: int, eps: float,
                  layer_slots=None):
         self.all_kv = np.ascontiguousarray(all_kv, dtype=np.uint16)
         T, L, two, H, D = self.all_kv.shape
-        assert two == 2 and D == HEAD_DIM
-        self.knorm_w = np.ascontiguousarray(knorm_w, dtype=np.uint16).reshape(L, HEAD_DIM)
+        assert two == 2 and 1 <= D <= MAX_HEAD_DIM
+        self.D, self.row = D, 2 * D
+        self.knorm_w = np.ascontiguousarray(knorm_w, dtype=np.uint16).reshape(L, D)
         self.positions = np.ascontiguousarray(positions, dtype=np.int64).reshape(T)
         self.slot_mapping = np.ascontiguousarray(slot_mapping, dtype=np.int64).reshape(T)
         self.cos_sin = np.ascontiguousarray(cos_sin, dtype=np.uint16)
@@ -240,7 +253,7 @@ class Problem:
             _ptr(self.cos_sin), _ptr(self.k_scale), _ptr(self.v_scale),
             T, self.cos_sin.shape[0], self.num_blocks, L, H, self.block_size, self.rotary_dim,
             self.kv_dtype, ctypes.c_float(self.eps).value,
-            _ptr(self.layer_slots) if self.layer_slots is not None else None,
+            _ptr(self.layer_slots) if self.layer_slots is not None else None, D,
         )
 
     @property
@@ -251,7 +264,7 @@ class Problem:
         _check(lib().dspark_oracle_check_inputs(ctypes.byref(self.c)))
 
     def new_caches(self, fill_byte: int = 0xFF):
-        shape = (self.num_blocks, self.H, self.block_size, ROW)
+        shape = (self.num_blocks, self.H, self.block_size, self.row)
         out = []
         for _ in range(self.L):
             c = np.empty(shape, dtype=self.elem_dtype)
@@ -265,7 +278,9 @@ class Problem:
         t_end = self.T if t_end is None else t_end
         for c in caches:
             assert c.flags["C_CONTIGUOUS"] and c.dtype == self.elem_dtype
-        cap = alt_cap if alt_cap is not None else max(1024, (t_end - t_begin) * self.L * self.H // 4)
+        # about one tie per 2^9 norm outputs, each giving up to three more
+        # candidates for itself and its rotation partner: D/16 per row is ample
+        cap = alt_cap if alt_cap is not None else max(4096, (t_end - t_begin) * self.L * self.H * self.D // 16)
         ptrs = (ctypes.c_void_p * self.L)(*[_ptr(c) for c in caches])
         al = np.empty(cap, np.int32)
         ae = np.empty(cap, np.int64)
@@ -278,11 +293,11 @@ class Problem:
         return al[:k].copy(), ae[:k].copy(), av[:k].copy()
 
     def rows(self, row_ids):
-        """Stored 256-element rows for flat row ids ``(t*L + l)*H + h``, with
+        """Stored 2D-element rows for flat row ids ``(t*L + l)*H + h``, with
         alternates as (index into row_ids, dim, value)."""
         ids = np.ascontiguousarray(row_ids, dtype=np.int64).reshape(-1)
         n = ids.shape[0]
-        out = np.empty((n, ROW), dtype=self.elem_dtype)
+        out = np.empty((n, self.row), dtype=self.elem_dtype)
         cap = max(1024, n * 8)
         ar = np.empty(cap, np.int64)
         ad = np.empty(cap, np.int32)

@@ -10,7 +10,8 @@
  * the DSpark draft model page, MiniMaxM3DSparkModel.precompute_and_store_context_kv):
  * for every context token t whose slot is >= 0, every layer l and every KV
  * head h,
- *   1. k = all_kv[t, l, 0, h, :], v = all_kv[t, l, 1, h, :]   (bf16, 128 each)
+ *   1. k = all_kv[t, l, 0, h, :], v = all_kv[t, l, 1, h, :]   (bf16, D each;
+ *      D = 128 on the pages, any head_dim up to 256 here)
  *   2. Gemma RMSNorm of k:  y = k * rsqrt(mean(k^2) + eps) * (1 + w[l]),
  *      materialised to bf16 (the page states fp32 evaluation; this oracle
  *      evaluates in fp64 and reports both bf16 neighbours as admissible when
@@ -23,9 +24,9 @@
  *      each output rounded once to bf16; dims >= r pass through
  *   4. store: raw bf16 K'|V, or fp8 e4m3 (OCP, round to nearest even,
  *      saturating at +-448) of x / scale with the division in fp32
- *   5. the 256-element row K'|V goes to layer l's paged cache
- *      [num_blocks, nkv, block_size, 256] at block slot / block_size,
- *      head h, offset slot % block_size.
+ *   5. the 2D-element row K'|V goes to layer l's paged cache
+ *      [num_blocks, nkv, block_size, 2D] at block slot / block_size,
+ *      head h, offset slot % block_size (any block size >= 1).
  * Slots < 0 are padding: nothing is read or written for them.
  */
 #include <math.h>
@@ -33,8 +34,8 @@
 #include <stdlib.h>
 #include <string.h>
 
-#define ORACLE_HEAD_DIM 128
-#define ORACLE_ROW 256
+#define ORACLE_HEAD_DIM 128     /* the pages' head dim: the default */
+#define ORACLE_MAX_HEAD_DIM 256
 #define ORACLE_TIE_REL 3.814697265625e-06 /* 2^-18 */
 
 enum { ORACLE_KV_BF16 = 0, ORACLE_KV_FP8_E4M3 = 1 };
@@ -52,8 +53,8 @@ enum {
 
 /* Everything one write call reads (host memory). */
 typedef struct {
-    const uint16_t *all_kv;       /* bf16 bits [T][L][2][H][128] */
-    const uint16_t *knorm_w;      /* bf16 bits [L][128] */
+    const uint16_t *all_kv;       /* bf16 bits [T][L][2][H][D] */
+    const uint16_t *knorm_w;      /* bf16 bits [L][D] */
     const int64_t *positions;     /* [T] */
     const int64_t *slot_mapping;  /* [T], < 0 = padding */
     const uint16_t *cos_sin;      /* bf16 bits [max_pos][r] */
@@ -72,7 +73,15 @@ typedef struct {
      * KV-cache groups, DSpark draft model page, _shared_slot_mapping), or
      * NULL: slot_mapping is shared by every layer. */
     const int64_t *layer_slots;
+    /* D, the head dim of K and V (1..256); 0 means the pages' 128.  all_kv
+     * is then [T][L][2][H][D], knorm_w [L][D], cache rows 2D elements. */
+    int32_t head_dim;
 } dspark_oracle_inputs;
+
+static int head_dim_of(const dspark_oracle_inputs *in)
+{
+    return in->head_dim ? in->head_dim : ORACLE_HEAD_DIM;
+}
 
 /* The slot of token t in layer l's cache. */
 static int64_t slot_of(const dspark_oracle_inputs *in, int64_t t, int32_t l)
@@ -176,21 +185,21 @@ uint8_t dspark_oracle_e4m3_rne_sat(float xf)
 }
 
 /* ------------------------------------------------------------------ */
-/* Step 2: Gemma RMSNorm of one K row.  y[d] is the bf16 rounding (ties to
+/* Step 2: Gemma RMSNorm of one K row of n elements.  y[d] is the bf16 rounding (ties to
  * even) of the exact value; y_alt[d] is the other bf16 neighbour when the
  * exact value lies within ORACLE_TIE_REL (relative) of a rounding midpoint,
  * else y[d] again.  Returns the number of such ambiguous dims. */
-int dspark_oracle_gemma_knorm(const uint16_t *k, const uint16_t *w, float eps,
-                              uint16_t *y, uint16_t *y_alt)
+int dspark_oracle_gemma_knorm_n(const uint16_t *k, const uint16_t *w, int n, float eps,
+                                uint16_t *y, uint16_t *y_alt)
 {
     double ss = 0.0;
-    for (int d = 0; d < ORACLE_HEAD_DIM; d++) {
+    for (int d = 0; d < n; d++) {
         double kd = dspark_oracle_bf16_decode(k[d]);
         ss += kd * kd;
     }
-    double inv = 1.0 / sqrt(ss / (double)ORACLE_HEAD_DIM + (double)eps);
+    double inv = 1.0 / sqrt(ss / (double)n + (double)eps);
     int amb = 0;
-    for (int d = 0; d < ORACLE_HEAD_DIM; d++) {
+    for (int d = 0; d < n; d++) {
         double v = dspark_oracle_bf16_decode(k[d]) * inv *
                    (1.0 + dspark_oracle_bf16_decode(w[d]));
         uint16_t dn = dspark_oracle_bf16_rne(v * (1.0 - ORACLE_TIE_REL));
@@ -203,6 +212,13 @@ int dspark_oracle_gemma_knorm(const uint16_t *k, const uint16_t *w, float eps,
         }
     }
     return amb;
+}
+
+/* The same at the pages' head dim, 128. */
+int dspark_oracle_gemma_knorm(const uint16_t *k, const uint16_t *w, float eps,
+                              uint16_t *y, uint16_t *y_alt)
+{
+    return dspark_oracle_gemma_knorm_n(k, w, ORACLE_HEAD_DIM, eps, y, y_alt);
 }
 
 /* Step 3 for one rotated pair (i, i + r/2): exact products in fp64, one
@@ -227,21 +243,24 @@ static uint16_t encode_elem(uint16_t x, int kv_dtype, float scale)
 }
 
 /* ------------------------------------------------------------------ */
-/* One output row.  out: 256 stored elements (uint16 bf16 bits, or uint8
+/* One output row.  out: 2D stored elements (uint16 bf16 bits, or uint8
  * e4m3 codes when kv_dtype is fp8).  Every other admissible value of a K
  * element (from a bf16 tie in the norm) is appended to alt_dim/alt_val
- * (room for 3 * 128 entries); *n_alt receives their count. */
+ * (room for 3 * D entries); *n_alt receives their count. */
 int dspark_oracle_row(const dspark_oracle_inputs *in, int64_t t, int32_t l, int32_t h,
                       void *out, int32_t *alt_dim, uint16_t *alt_val, int32_t *n_alt)
 {
     const int L = in->num_layers, H = in->num_kv_heads, r = in->rotary_dim;
+    const int D = head_dim_of(in);
     if (t < 0 || t >= in->num_ctx || l < 0 || l >= L || h < 0 || h >= H)
         return ORACLE_ERR_ARG;
-    const int64_t base = (((t * L + l) * 2 + 0) * H + h) * ORACLE_HEAD_DIM;
-    const int64_t vbase = (((t * L + l) * 2 + 1) * H + h) * ORACLE_HEAD_DIM;
+    if (D < 1 || D > ORACLE_MAX_HEAD_DIM)
+        return ORACLE_ERR_ARG;
+    const int64_t base = (((t * L + l) * 2 + 0) * H + h) * D;
+    const int64_t vbase = (((t * L + l) * 2 + 1) * H + h) * D;
     const uint16_t *k = in->all_kv + base;
     const uint16_t *v = in->all_kv + vbase;
-    const uint16_t *w = in->knorm_w + (int64_t)l * ORACLE_HEAD_DIM;
+    const uint16_t *w = in->knorm_w + (int64_t)l * D;
     const int64_t pos = in->positions[t];
     if (pos < 0 || pos >= in->max_pos)
         return ORACLE_ERR_POS_RANGE;
@@ -249,12 +268,12 @@ int dspark_oracle_row(const dspark_oracle_inputs *in, int64_t t, int32_t l, int3
     const float ks = in->kv_dtype == ORACLE_KV_FP8_E4M3 ? in->k_scale[l] : 1.0f;
     const float vs = in->kv_dtype == ORACLE_KV_FP8_E4M3 ? in->v_scale[l] : 1.0f;
 
-    uint16_t y[ORACLE_HEAD_DIM], y_alt[ORACLE_HEAD_DIM];
-    dspark_oracle_gemma_knorm(k, w, in->eps, y, y_alt);
+    uint16_t y[ORACLE_MAX_HEAD_DIM], y_alt[ORACLE_MAX_HEAD_DIM];
+    dspark_oracle_gemma_knorm_n(k, w, D, in->eps, y, y_alt);
 
-    uint16_t res[ORACLE_ROW];
+    uint16_t res[2 * ORACLE_MAX_HEAD_DIM];
     int na = 0;
-    for (int d = 0; d < ORACLE_HEAD_DIM; d++) {
+    for (int d = 0; d < D; d++) {
         /* candidate K' values of dim d; the first is the primary one, built
          * from the correctly rounded norm outputs */
         uint16_t cand[4];
@@ -302,23 +321,23 @@ int dspark_oracle_row(const dspark_oracle_inputs *in, int64_t t, int32_t l, int3
             }
         }
     }
-    for (int d = 0; d < ORACLE_HEAD_DIM; d++)
-        res[ORACLE_HEAD_DIM + d] = encode_elem(v[d], in->kv_dtype, vs);
+    for (int d = 0; d < D; d++)
+        res[D + d] = encode_elem(v[d], in->kv_dtype, vs);
 
     if (in->kv_dtype == ORACLE_KV_FP8_E4M3) {
         uint8_t *o8 = (uint8_t *)out;
-        for (int d = 0; d < ORACLE_ROW; d++)
+        for (int d = 0; d < 2 * D; d++)
             o8[d] = (uint8_t)res[d];
     } else {
-        memcpy(out, res, sizeof res);
+        memcpy(out, res, (size_t)(2 * D) * sizeof(uint16_t));
     }
     if (n_alt)
         *n_alt = na;
     return ORACLE_OK;
 }
 
-/* Step 5: the row of layer l's cache [num_blocks, H, block_size, 256] that
- * (slot, h) addresses, counted in 256-element rows; -1 for padding, -2 when
+/* Step 5: the row of layer l's cache [num_blocks, H, block_size, 2D] that
+ * (slot, h) addresses, counted in 2D-element rows; -1 for padding, -2 when
  * the slot lies beyond the cache. */
 int64_t dspark_oracle_dest_row(int64_t slot, int32_t h, int32_t num_kv_heads,
                                int32_t block_size, int64_t num_blocks)
@@ -346,7 +365,9 @@ int dspark_oracle_check_inputs(const dspark_oracle_inputs *in)
     if (!in || in->num_ctx < 0 || in->num_layers <= 0 || in->num_kv_heads <= 0 ||
         in->block_size <= 0 || in->num_blocks <= 0 || in->max_pos <= 0)
         return ORACLE_ERR_ARG;
-    if (in->rotary_dim <= 0 || in->rotary_dim > ORACLE_HEAD_DIM || in->rotary_dim % 2)
+    if (head_dim_of(in) < 1 || head_dim_of(in) > ORACLE_MAX_HEAD_DIM)
+        return ORACLE_ERR_ARG;
+    if (in->rotary_dim <= 0 || in->rotary_dim > head_dim_of(in) || in->rotary_dim % 2)
         return ORACLE_ERR_ARG;
     if (in->kv_dtype != ORACLE_KV_BF16 && in->kv_dtype != ORACLE_KV_FP8_E4M3)
         return ORACLE_ERR_ARG;
@@ -395,7 +416,7 @@ int dspark_oracle_check_inputs(const dspark_oracle_inputs *in)
 
 /* The whole write for tokens [t_begin, t_end): every valid row computed by
  * dspark_oracle_row and stored into caches[l] (host buffers, one per layer,
- * each [num_blocks, H, block_size, 256] of the cache dtype).  Admissible
+ * each [num_blocks, H, block_size, 2D] of the cache dtype).  Admissible
  * alternates are reported as (layer, element index in that layer's cache,
  * value), up to alt_cap of them; *n_alt receives how many there were in
  * total.  Returns ORACLE_ERR_ALT_CAP (after writing everything) when more
@@ -412,10 +433,11 @@ int dspark_oracle_write(const dspark_oracle_inputs *in, void *const *caches,
         return ORACLE_ERR_ARG;
     const int L = in->num_layers, H = in->num_kv_heads;
     const size_t esz = in->kv_dtype == ORACLE_KV_FP8_E4M3 ? 1 : 2;
+    const int64_t row_elems = 2 * (int64_t)head_dim_of(in);
     int64_t total_alt = 0;
-    int32_t rd[3 * ORACLE_HEAD_DIM];
-    uint16_t rv[3 * ORACLE_HEAD_DIM];
-    uint16_t row[ORACLE_ROW];
+    int32_t rd[3 * ORACLE_MAX_HEAD_DIM];
+    uint16_t rv[3 * ORACLE_MAX_HEAD_DIM];
+    uint16_t row[2 * ORACLE_MAX_HEAD_DIM];
     for (int64_t t = t_begin; t < t_end; t++) {
         for (int l = 0; l < L; l++) {
             const int64_t slot = slot_of(in, t, l);
@@ -428,11 +450,11 @@ int dspark_oracle_write(const dspark_oracle_inputs *in, void *const *caches,
                     return rc;
                 int64_t dst = dspark_oracle_dest_row(slot, h, H, in->block_size, in->num_blocks);
                 uint8_t *layer = (uint8_t *)caches[l];
-                memcpy(layer + (size_t)dst * ORACLE_ROW * esz, row, ORACLE_ROW * esz);
+                memcpy(layer + (size_t)(dst * row_elems) * esz, row, (size_t)row_elems * esz);
                 for (int j = 0; j < na; j++) {
                     if (total_alt < alt_cap) {
                         alt_layer[total_alt] = l;
-                        alt_elem[total_alt] = dst * ORACLE_ROW + rd[j];
+                        alt_elem[total_alt] = dst * row_elems + rd[j];
                         alt_val[total_alt] = rv[j];
                     }
                     total_alt++;
@@ -446,7 +468,7 @@ int dspark_oracle_write(const dspark_oracle_inputs *in, void *const *caches,
 }
 
 /* Rows (t, l, h) given as flat indices (t * L + l) * H + h, whatever their
- * slot: out is [n][256] stored elements; alternates as (index into the row
+ * slot: out is [n][2D] stored elements; alternates as (index into the row
  * list, dim, value). */
 int dspark_oracle_rows(const dspark_oracle_inputs *in, const int64_t *row_ids, int64_t n,
                        void *out, int64_t *alt_row, int32_t *alt_dim, uint16_t *alt_val,
@@ -454,9 +476,10 @@ int dspark_oracle_rows(const dspark_oracle_inputs *in, const int64_t *row_ids, i
 {
     const int L = in->num_layers, H = in->num_kv_heads;
     const size_t esz = in->kv_dtype == ORACLE_KV_FP8_E4M3 ? 1 : 2;
+    const int64_t row_elems = 2 * (int64_t)head_dim_of(in);
     int64_t total_alt = 0;
-    int32_t rd[3 * ORACLE_HEAD_DIM];
-    uint16_t rv[3 * ORACLE_HEAD_DIM];
+    int32_t rd[3 * ORACLE_MAX_HEAD_DIM];
+    uint16_t rv[3 * ORACLE_MAX_HEAD_DIM];
     for (int64_t i = 0; i < n; i++) {
         int64_t id = row_ids[i];
         if (id < 0 || id >= in->num_ctx * L * H)
@@ -465,7 +488,7 @@ int dspark_oracle_rows(const dspark_oracle_inputs *in, const int64_t *row_ids, i
         int32_t l = (int32_t)((id / H) % L);
         int32_t h = (int32_t)(id % H);
         int32_t na = 0;
-        int rc = dspark_oracle_row(in, t, l, h, (uint8_t *)out + (size_t)i * ORACLE_ROW * esz,
+        int rc = dspark_oracle_row(in, t, l, h, (uint8_t *)out + (size_t)(i * row_elems) * esz,
                                    rd, rv, &na);
         if (rc != ORACLE_OK)
             return rc;

@@ -70,6 +70,13 @@ class Workload:
     tokens_per_request: int = 0
     blocks_per_request: int = 0
     seed: int = BASE_SEED
+    # D of K and V: the pages' 128, or another head dim (64, 256) of the
+    # general write; cache rows hold 2D elements
+    head_dim: int = HEAD_DIM
+
+    @property
+    def row_elems(self) -> int:
+        return 2 * self.head_dim
 
     @property
     def capacity(self) -> int:
@@ -81,7 +88,7 @@ class Workload:
 
     @property
     def layer_cache_bytes(self) -> int:
-        return self.num_blocks * self.num_kv_heads * self.block_size * ROW_ELEMS * self.elem_size
+        return self.num_blocks * self.num_kv_heads * self.block_size * self.row_elems * self.elem_size
 
     @property
     def num_rows(self) -> int:
@@ -123,6 +130,47 @@ WORKLOADS: list[Workload] = [
 ]
 
 WORKLOADS_BY_NAME = {w.name: w for w in WORKLOADS}
+
+# Prefill-sized writes in layouts the pages' kernel refuses (head dims 64 and
+# 256, rotary dims other than 16 / 32 / 64, block sizes that are not powers
+# of two), for the general write: same value recipe, blocktable slots.
+GENERAL_WORKLOADS: list[Workload] = [
+    Workload(
+        name="gen_head64", num_ctx=8192, num_layers=5, num_kv_heads=8, rotary_dim=64, head_dim=64,
+        block_size=16, num_blocks=4096, max_pos=32768, rope_theta=1e6, slots="blocktable", pad_count=164,
+        requests=32, tokens_per_request=256, blocks_per_request=16, seed=BASE_SEED + 10,
+    ),
+    Workload(
+        name="gen_head256_fp8", num_ctx=8192, num_layers=5, num_kv_heads=4, rotary_dim=64, head_dim=256,
+        block_size=32, num_blocks=2048, max_pos=32768, rope_theta=1e6, kv_dtype=KV_FP8, slots="blocktable",
+        pad_count=164, requests=32, tokens_per_request=256, blocks_per_request=8, seed=BASE_SEED + 11,
+    ),
+    Workload(
+        name="gen_block48_fp8", num_ctx=8192, num_layers=5, num_kv_heads=8, rotary_dim=32,
+        block_size=48, num_blocks=2048, max_pos=32768, rope_theta=1e6, kv_dtype=KV_FP8, slots="blocktable",
+        pad_count=164, requests=32, tokens_per_request=256, blocks_per_request=6, seed=BASE_SEED + 12,
+    ),
+    Workload(
+        name="gen_rot24", num_ctx=8192, num_layers=5, num_kv_heads=8, rotary_dim=24,
+        block_size=16, num_blocks=4096, max_pos=32768, rope_theta=1e6, slots="blocktable", pad_count=164,
+        requests=32, tokens_per_request=256, blocks_per_request=16, seed=BASE_SEED + 13,
+    ),
+    Workload(
+        name="gen_rot128", num_ctx=8192, num_layers=5, num_kv_heads=8, rotary_dim=128,
+        block_size=64, num_blocks=2048, max_pos=32768, rope_theta=1e6, slots="blocktable", pad_count=164,
+        requests=32, tokens_per_request=256, blocks_per_request=4, seed=BASE_SEED + 14,
+    ),
+]
+
+GENERAL_WORKLOADS_BY_NAME = {w.name: w for w in GENERAL_WORKLOADS}
+
+
+def pages_layout(wl: Workload) -> bool:
+    """Whether the pages' kernel takes this layout (writer page,
+    rotary_dims_supported and DSparkContextKVWriter._validate: head_dim 128,
+    rotary_dim 16 / 32 / 64, a power-of-two block size)."""
+    bs = wl.block_size
+    return wl.head_dim == HEAD_DIM and wl.rotary_dim in (16, 32, 64) and bs > 0 and bs & (bs - 1) == 0
 
 
 @dataclass
@@ -216,7 +264,7 @@ def generate(wl: Workload, seed: int | None = None, with_all_kv: bool = True) ->
     g = torch.Generator().manual_seed(wl.seed if seed is None else seed)
     T, L, H = wl.num_ctx, wl.num_layers, wl.num_kv_heads
     if with_all_kv:
-        kv = torch.randn((T, L, 2, H, HEAD_DIM), generator=g, dtype=torch.float32)
+        kv = torch.randn((T, L, 2, H, wl.head_dim), generator=g, dtype=torch.float32)
         if wl.kv_std != 1.0:
             kv.mul_(wl.kv_std)
         if wl.outlier_frac > 0:
@@ -226,7 +274,7 @@ def generate(wl: Workload, seed: int | None = None, with_all_kv: bool = True) ->
         del kv
     else:
         all_kv = torch.empty((0,), dtype=torch.bfloat16)
-    knorm_w = (torch.randn((L, HEAD_DIM), generator=g) * wl.w_std).to(torch.bfloat16).contiguous()
+    knorm_w = (torch.randn((L, wl.head_dim), generator=g) * wl.w_std).to(torch.bfloat16).contiguous()
     pos, slots = _positions_and_slots(wl, g)
     cos_sin = rope_cos_sin_cache(wl.max_pos, wl.rotary_dim, wl.rope_theta)
     if wl.kv_dtype == KV_FP8:
@@ -239,10 +287,11 @@ def generate(wl: Workload, seed: int | None = None, with_all_kv: bool = True) ->
 
 
 def make_caches(wl: Workload, device="cpu", fill: int | None = PREFILL_BYTE) -> list[torch.Tensor]:
-    """One separately allocated ``[num_blocks, nkv, block_size, 256]`` cache per
-    layer, every byte set to ``fill`` (left uninitialised when ``fill`` is None)."""
+    """One separately allocated ``[num_blocks, nkv, block_size, 2 * head_dim]``
+    cache per layer, every byte set to ``fill`` (left uninitialised when
+    ``fill`` is None)."""
     dtype = torch.bfloat16 if wl.kv_dtype == KV_BF16 else torch.uint8
-    shape = (wl.num_blocks, wl.num_kv_heads, wl.block_size, ROW_ELEMS)
+    shape = (wl.num_blocks, wl.num_kv_heads, wl.block_size, wl.row_elems)
     caches = []
     for _ in range(wl.num_layers):
         c = torch.empty(shape, dtype=dtype, device=device)
@@ -261,20 +310,20 @@ def take_tokens(inp: Inputs, count: int) -> Inputs:
 
 def compulsory_bytes(wl: Workload, num_valid_tokens: int) -> int:
     """Bytes the write must move at least: per token its slot (and, when
-    valid, its position and cos|sin row); per valid row the 512-byte K|V read
-    and the 512-byte (bf16) or 256-byte (fp8) cache write; plus the K-norm
-    weights and the 2*L scales."""
+    valid, its position and cos|sin row); per valid row the K|V read (512
+    bytes at head dim 128) and the cache write (512 bytes bf16, 256 fp8);
+    plus the K-norm weights and the 2*L scales."""
     L, H, r = wl.num_layers, wl.num_kv_heads, wl.rotary_dim
     valid_rows = num_valid_tokens * L * H
-    out_row = ROW_ELEMS * wl.elem_size
+    out_row = wl.row_elems * wl.elem_size
     per_tok = 8 * wl.num_ctx + num_valid_tokens * (8 + 2 * r)
-    return valid_rows * (ROW_ELEMS * 2 + out_row) + per_tok + L * HEAD_DIM * 2 + 2 * L * 4
+    return valid_rows * (wl.row_elems * 2 + out_row) + per_tok + L * wl.head_dim * 2 + 2 * L * 4
 
 
 def describe(wl: Workload) -> dict:
     return {
         "workload": wl.name, "num_ctx": wl.num_ctx, "layers": wl.num_layers,
-        "nkv": wl.num_kv_heads, "head_dim": HEAD_DIM, "rotary_dim": wl.rotary_dim,
+        "nkv": wl.num_kv_heads, "head_dim": wl.head_dim, "rotary_dim": wl.rotary_dim,
         "block_size": wl.block_size, "num_blocks": wl.num_blocks, "kv_cache_dtype": wl.kv_dtype,
         "max_pos": wl.max_pos,
     }

@@ -42,9 +42,10 @@ import workloads as wk  # noqa: E402
 
 METRIC = "context-KV write GB/s and rows/s on 1 GB300; % of HBM roofline"
 UNIT = "GB/s"
+# sources of the write kernels and of the host layer that picks one
 KERNEL_SRCS = [os.path.join(ROOT, "speculative_decoding_draft_ctx_gb300", "csrc", f)
-               for f in ("ctx_kv_tma.cu", "ctx_kv_kernel.cu", "ctx_kv_api.cpp", "ctx_kv_internal.h",
-                         "ctx_kv_device.cuh")]
+               for f in ("ctx_kv_tma.cu", "ctx_kv_kernel.cu", "ctx_kv_general.cu", "ctx_kv_api.cpp",
+                         "ctx_kv_internal.h", "ctx_kv_device.cuh")]
 QK_METRIC = "draft-token QK-norm/RoPE/KV-insert GB/s on 1 GB300; % of HBM roofline"
 PROJ_METRIC = "fused context-KV projection + write TFLOP/s on 1 GB300; % of bf16 tensor roofline"
 NORM_METRIC = "context-state Gemma RMSNorm GB/s on 1 GB300; % of HBM roofline"
@@ -59,10 +60,12 @@ def parse_args(argv=None):
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--config", default="long_context",
-                    choices=[w.name for w in wk.WORKLOADS] + [w.name for w in wk.QK_WORKLOADS] +
-                    [w.name for w in wk.PROJ_WORKLOADS] + [w.name for w in wk.NORM_WORKLOADS],
-                    help="a context-KV write workload, a qk_* workload of the draft-token QK insert, or a "
-                         "proj_* workload of the projection with the write fused into it")
+                    choices=[w.name for w in wk.WORKLOADS] + [w.name for w in wk.GENERAL_WORKLOADS] +
+                    [w.name for w in wk.QK_WORKLOADS] + [w.name for w in wk.PROJ_WORKLOADS] +
+                    [w.name for w in wk.NORM_WORKLOADS],
+                    help="a context-KV write workload (gen_*: a layout only the general write takes), a qk_* "
+                         "workload of the draft-token QK insert, a proj_* workload of the projection with the "
+                         "write fused into it, or an hn_* workload of the hidden-state norm")
     ap.add_argument("--e2e-steps", type=int, default=30)
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="oracle sample budget")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -79,7 +82,7 @@ def parse_args(argv=None):
 
 def select_workload(args) -> wk.Workload:
     """The named workload, or a smaller case of it with the same recipe."""
-    wl = wk.WORKLOADS_BY_NAME[args.config]
+    wl = wk.WORKLOADS_BY_NAME.get(args.config) or wk.GENERAL_WORKLOADS_BY_NAME[args.config]
     if args.num_ctx is None and args.num_blocks is None:
         return wl
     T = args.num_ctx or wl.num_ctx
@@ -270,7 +273,7 @@ class OracleSample:
         self.p = oracle.problem_from_inputs(self.sub)
         p = self.p
         # host caches stay untouched except for the sampled rows (lazily backed)
-        shape = (p.num_blocks, p.H, p.block_size, 256)
+        shape = (p.num_blocks, p.H, p.block_size, p.row)
         self.caches = [np.empty(shape, dtype=p.elem_dtype) for _ in range(p.L)]
         nv = self.sub.num_valid_tokens
         self.bytes = wk.compulsory_bytes(self.sub.workload, nv)
@@ -405,7 +408,7 @@ def run_ours(args):
 
     # input sets rotated across steps so that each step's reads and writes
     # miss L2 (one set when the workload alone is larger than L2)
-    foot = base.all_kv.numel() * 2 + step_rows * 256 * wl.elem_size
+    foot = base.all_kv.numel() * 2 + step_rows * wl.row_elems * wl.elem_size
     n_sets = max(1, math.ceil(3 * l2_bytes() / foot))
     sets = []
     for i in range(n_sets):
@@ -414,7 +417,8 @@ def run_ours(args):
     k_scales = [sets[0].k_scale[l:l + 1].clone() for l in range(wl.num_layers)]
     v_scales = [sets[0].v_scale[l:l + 1].clone() for l in range(wl.num_layers)]
     caches = wk.make_caches(wl, device=dev, fill=None)
-    writer = dk.ContextKVWriter(caches, k_scales, v_scales, "fp8" if fp8 else "auto")
+    general = not wk.pages_layout(wl)
+    writer = dk.ContextKVWriter(caches, k_scales, v_scales, "fp8" if fp8 else "auto", general=general)
     stream = torch.cuda.current_stream()
 
     if args.layer_slots:
@@ -424,14 +428,14 @@ def run_ours(args):
         # every layer's rows are written at its own group's slots: the valid rows of each layer count
         step_rows = int(sum(int((s >= 0).sum()) for s in sets[0].extra["slots"])) * wl.num_kv_heads
         valid_layer_tokens = step_rows // wl.num_kv_heads
-        step_bytes = (valid_layer_tokens * wl.num_kv_heads * (2 * wk.ROW_ELEMS + wk.ROW_ELEMS * wl.elem_size) +
+        step_bytes = (valid_layer_tokens * wl.num_kv_heads * (2 * wl.row_elems + wl.row_elems * wl.elem_size) +
                       wk.compulsory_bytes(wl, 0) + base.num_valid_tokens * (8 + 2 * wl.rotary_dim) +
                       8 * wl.num_ctx * (wl.num_layers - 1))
 
     # per-layer mappings: each input set has its own slot tensors, so its own
     # writer (and pointer table): nothing is rebuilt while a graph captures
-    writers = ([dk.ContextKVWriter(caches, k_scales, v_scales, "fp8" if fp8 else "auto") for _ in range(n_sets)]
-               if args.layer_slots else [writer])
+    writers = ([dk.ContextKVWriter(caches, k_scales, v_scales, "fp8" if fp8 else "auto", general=general)
+                for _ in range(n_sets)] if args.layer_slots else [writer])
 
     def step(i):
         d = sets[i % n_sets]

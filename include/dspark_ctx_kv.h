@@ -226,6 +226,42 @@ int dspark_ctx_kv_write_layer_slots(const void *all_kv, const void *knorm_w, con
                                     const float *const *v_scales, int L, int nkv, int block_size, int rotary_dim,
                                     float eps, int kv_dtype, unsigned int *error_flags, cudaStream_t stream);
 
+/*
+ * dspark_ctx_kv_write_general -- the same write for the layouts the pages'
+ * kernel refuses and hands to the unfused path (writer page,
+ * DSparkContextKVWriter._validate and rotary_dims_supported accept only
+ * head_dim 128, rotary_dim 16 / 32 / 64 and power-of-two block sizes):
+ *
+ *  head_dim      D = 64, 128 or 256.  all_kv is bf16 [num_ctx, L, 2, nkv, D],
+ *                knorm_w bf16 [L, D], every layer's cache
+ *                [num_blocks, nkv, block_size, 2D] (K at [0, D), V at [D, 2D)).
+ *  rotary_dim    any even value in [2, D]: NeoX pairs (i, i + r/2), cos_sin
+ *                bf16 [max_pos, rotary_dim] (cos | sin).
+ *  block_size    any value >= 1: block slot / block_size, offset
+ *                slot % block_size.
+ *  slot_mapping, exactly one of the two is given: a mapping shared by every
+ *  layer_slot_mappings  layer (device int64 [num_ctx]) or a device table of
+ *                L device pointers to per-layer mappings (8-byte aligned).
+ * Every other argument, the alignment rules (16-byte buffers, 16-element
+ * layer offsets), the error flags and the statuses are those of
+ * dspark_ctx_kv_write_ex / dspark_ctx_kv_write_layer_slots; an unsupported
+ * head_dim is DSPARK_ERR_INVALID_ARG, an odd or out-of-range rotary_dim
+ * DSPARK_ERR_UNSUPPORTED_ROTARY_DIM, block_size < 1 DSPARK_ERR_BLOCK_SIZE.
+ * A call in the pages' layout takes the same kernels as dspark_ctx_kv_write_ex.
+ * One launch; allocates, copies and synchronises nothing.
+ */
+int dspark_ctx_kv_write_general(const void *all_kv, const void *knorm_w, const int64_t *positions,
+                                const int64_t *slot_mapping, const int64_t *const *layer_slot_mappings,
+                                int64_t num_ctx, const void *cos_sin, int64_t max_pos, void *layer0_cache,
+                                int64_t num_blocks, const int64_t *cache_offsets, const float *const *k_scales,
+                                const float *const *v_scales, int L, int nkv, int head_dim, int block_size,
+                                int rotary_dim, float eps, int kv_dtype, unsigned int *error_flags,
+                                cudaStream_t stream);
+
+/* 1 when dspark_ctx_kv_write_general handles this layout (head_dim 64, 128
+ * or 256; rotary_dim even in [2, head_dim]; block_size >= 1), else 0. */
+int dspark_ctx_kv_general_supported(int head_dim, int rotary_dim, int block_size);
+
 /* 1 when the kernel handles this head (writer page, rotary_dims_supported:
  * head_dim 128 and rotary_dim 16, 32 or 64), else 0. */
 int dspark_ctx_kv_rotary_dims_supported(int rotary_dim, int head_dim);
@@ -256,6 +292,11 @@ typedef struct {
  * layers share shape, stride and dtype; every cache starts a multiple of 16
  * elements from layer 0's.  Otherwise the status of the first violation. */
 int dspark_ctx_kv_validate_layers(int L, const dspark_cache_desc *layers);
+
+/* As dspark_ctx_kv_validate_layers for dspark_ctx_kv_write_general: the
+ * last dim may be 128, 256 or 512 (head_dim 64, 128, 256) and the block size
+ * any value >= 1; every other rule is the same. */
+int dspark_ctx_kv_validate_layers_general(int L, const dspark_cache_desc *layers);
 
 /*
  * Offset/pointer tables (writer page, DSparkContextKVWriter._ensure_tables):

@@ -39,6 +39,7 @@ EXPORTS = (
     "dspark_ctx_kv_last_error", "dspark_ctx_kv_status_string", "dspark_qknorm_rope_kv_insert",
     "dspark_ctx_kv_project", "dspark_ctx_kv_project_write", "dspark_gemma_rms_norm",
     "dspark_ctx_kv_write_layer_slots", "dspark_ctx_kv_tables_update_slots", "dspark_ctx_kv_tables_layer_slots",
+    "dspark_ctx_kv_write_general", "dspark_ctx_kv_general_supported", "dspark_ctx_kv_validate_layers_general",
 )
 
 
@@ -120,6 +121,13 @@ def lib() -> ctypes.CDLL:
         L.dspark_ctx_kv_tables_update_slots.restype = I
         L.dspark_ctx_kv_tables_layer_slots.argtypes = [P]
         L.dspark_ctx_kv_tables_layer_slots.restype = P
+        L.dspark_ctx_kv_write_general.argtypes = [P, P, P, P, P, I64, P, I64, P, I64, P, P, P, I, I, I, I, I,
+                                                  ctypes.c_float, I, P, P]
+        L.dspark_ctx_kv_write_general.restype = I
+        L.dspark_ctx_kv_general_supported.argtypes = [I, I, I]
+        L.dspark_ctx_kv_general_supported.restype = I
+        L.dspark_ctx_kv_validate_layers_general.argtypes = [I, ctypes.POINTER(CacheDesc)]
+        L.dspark_ctx_kv_validate_layers_general.restype = I
         _lib = L
         return L
 
@@ -229,6 +237,24 @@ def dspark_ctx_kv_write_layer_slots(all_kv, knorm_w, positions, layer_slot_mappi
         float(eps), kv_dtype_code(kv_dtype), _addr(error_flags), _stream(stream)))
 
 
+def dspark_ctx_kv_write_general(all_kv, knorm_w, positions, slot_mapping, layer_slot_mappings, num_ctx, cos_sin,
+                                max_pos, layer0_cache, num_blocks, cache_offsets, k_scales, v_scales, L, nkv,
+                                head_dim, block_size, rotary_dim, eps, kv_dtype, error_flags=None, stream=None):
+    """``dspark_ctx_kv_write_general``: head dims 64 / 128 / 256, any even
+    rotary_dim up to the head dim, any block size; a shared ``slot_mapping``
+    or a per-layer ``layer_slot_mappings`` pointer table (an address), the
+    other None."""
+    check(lib().dspark_ctx_kv_write_general(
+        _addr(all_kv), _addr(knorm_w), _addr(positions), _addr(slot_mapping), _addr(layer_slot_mappings),
+        int(num_ctx), _addr(cos_sin), int(max_pos), _addr(layer0_cache), int(num_blocks), _addr(cache_offsets),
+        _addr(k_scales), _addr(v_scales), int(L), int(nkv), int(head_dim), int(block_size), int(rotary_dim),
+        float(eps), kv_dtype_code(kv_dtype), _addr(error_flags), _stream(stream)))
+
+
+def dspark_ctx_kv_general_supported(head_dim: int, rotary_dim: int, block_size: int) -> bool:
+    return bool(lib().dspark_ctx_kv_general_supported(int(head_dim), int(rotary_dim), int(block_size)))
+
+
 def dspark_ctx_kv_rotary_dims_supported(rotary_dim: int, head_dim: int) -> bool:
     return bool(lib().dspark_ctx_kv_rotary_dims_supported(int(rotary_dim), int(head_dim)))
 
@@ -270,6 +296,11 @@ def cache_desc(cache, kv_cache_dtype, k_scale, v_scale) -> CacheDesc:
 def dspark_ctx_kv_validate_layers(descs) -> None:
     arr = (CacheDesc * len(descs))(*descs)
     check(lib().dspark_ctx_kv_validate_layers(len(descs), arr))
+
+
+def dspark_ctx_kv_validate_layers_general(descs) -> None:
+    arr = (CacheDesc * len(descs))(*descs)
+    check(lib().dspark_ctx_kv_validate_layers_general(len(descs), arr))
 
 
 class Tables:

@@ -25,6 +25,8 @@ TMA_SRC = os.path.join(CSRC, "ctx_kv_tma.cu")
 QK_SRC = os.path.join(CSRC, "qk_insert_kernel.cu")
 PROJ_SRC = os.path.join(CSRC, "proj_gemm.cu")
 NORM_SRC = os.path.join(CSRC, "hidden_norm.cu")
+GENERAL_SRC = os.path.join(CSRC, "ctx_kv_general.cu")
+CU_SRCS = (KERNEL_SRC, TMA_SRC, QK_SRC, PROJ_SRC, NORM_SRC, GENERAL_SRC)
 API_SRC = os.path.join(CSRC, "ctx_kv_api.cpp")
 HEADERS = [os.path.join(CSRC, "ctx_kv_internal.h"), os.path.join(CSRC, "ctx_kv_device.cuh"),
            os.path.join(INCLUDE, "dspark_ctx_kv.h")]
@@ -46,7 +48,7 @@ def _stale() -> bool:
     if not os.path.exists(LIB_PATH):
         return True
     t = os.path.getmtime(LIB_PATH)
-    return any(os.path.getmtime(s) > t for s in [KERNEL_SRC, TMA_SRC, QK_SRC, PROJ_SRC, NORM_SRC, API_SRC, *HEADERS])
+    return any(os.path.getmtime(s) > t for s in [*CU_SRCS, API_SRC, *HEADERS])
 
 
 def _run(cmd):
@@ -65,7 +67,7 @@ def build(force: bool = False, verbose: bool = False) -> str:
         home = cuda_home()
         nvcc = os.path.join(home, "bin", "nvcc")
         objs, cmds = [], []
-        for src in (KERNEL_SRC, TMA_SRC, QK_SRC, PROJ_SRC, NORM_SRC):
+        for src in CU_SRCS:
             obj = os.path.join(BUILD_DIR, os.path.basename(src)[:-3] + ".o")
             cmd = [nvcc, *ARCH, "-lineinfo", "-O3", "-std=c++17", "-Xcompiler", "-fPIC",
                    "-I", INCLUDE, "-c", src, "-o", obj]
@@ -80,7 +82,7 @@ def build(force: bool = False, verbose: bool = False) -> str:
         with ThreadPoolExecutor(len(cmds)) as ex:
             outs = list(ex.map(_run, cmds))
         if verbose:
-            sys.stderr.write("".join(outs[:5]))
+            sys.stderr.write("".join(outs[:len(CU_SRCS)]))
         tmp = LIB_PATH + f".tmp{os.getpid()}"
         _run([nvcc, *ARCH, "-shared", "-o", tmp, *objs, "-lpthread", "-ldl", "-lrt"])
         os.replace(tmp, LIB_PATH)

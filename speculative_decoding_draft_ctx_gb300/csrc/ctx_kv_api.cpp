@@ -42,14 +42,16 @@ int ok()
     return DSPARK_OK;
 }
 
-// Which kernel serves a call: the pipelined one where the shape allows,
-// else the generic one.  DSPARK_CTX_KV_KERNEL=generic pins the generic
-// kernel for the calls made while it is set (both compute the same result;
-// the tests run each).
-bool force_generic()
+// Which kernel serves a call: for the pages' layouts the pipelined one where
+// the shape allows, else the generic one; the general kernel for every other
+// layout.  DSPARK_CTX_KV_KERNEL=generic pins the generic kernel for the
+// pages' layouts and =general the general kernel for every layout, for the
+// calls made while it is set (all compute the same result; the tests run
+// each).
+bool force_kernel(const char *name)
 {
     const char *e = std::getenv("DSPARK_CTX_KV_KERNEL");
-    return e && std::strcmp(e, "generic") == 0;
+    return e && std::strcmp(e, name) == 0;
 }
 
 bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
@@ -64,12 +66,16 @@ int log2_exact(int64_t v)
     return n;
 }
 
+// Which layouts a call accepts: the pages' (head_dim 128, rotary_dim 16 /
+// 32 / 64, power-of-two block sizes) or the general write's.
+enum class Rules { pages, general };
+
 // The write with a shared or a per-layer slot mapping (exactly one is given).
 int write_common(const void *all_kv, const void *knorm_w, const int64_t *positions, const int64_t *slot_mapping,
                  const int64_t *const *layer_slots, int64_t num_ctx, const void *cos_sin, int64_t max_pos,
                  void *layer0_cache, int64_t num_blocks, const int64_t *cache_offsets, const float *const *k_scales,
-                 const float *const *v_scales, int L, int nkv, int block_size, int rotary_dim, float eps,
-                 int kv_dtype, unsigned int *error_flags, cudaStream_t stream);
+                 const float *const *v_scales, int L, int nkv, int head_dim, int block_size, int rotary_dim,
+                 float eps, int kv_dtype, unsigned int *error_flags, cudaStream_t stream, Rules rules);
 
 }  // namespace
 
@@ -108,8 +114,8 @@ int dspark_ctx_kv_write_ex(const void *all_kv, const void *knorm_w, const int64_
     if (num_ctx > 0 && !slot_mapping)
         return fail(DSPARK_ERR_INVALID_ARG, "null slot_mapping");
     return write_common(all_kv, knorm_w, positions, slot_mapping, nullptr, num_ctx, cos_sin, max_pos, layer0_cache,
-                        num_blocks, cache_offsets, k_scales, v_scales, L, nkv, block_size, rotary_dim, eps,
-                        kv_dtype, error_flags, stream);
+                        num_blocks, cache_offsets, k_scales, v_scales, L, nkv, DSPARK_HEAD_DIM, block_size,
+                        rotary_dim, eps, kv_dtype, error_flags, stream, Rules::pages);
 }
 
 int dspark_ctx_kv_write_layer_slots(const void *all_kv, const void *knorm_w, const int64_t *positions,
@@ -122,19 +128,53 @@ int dspark_ctx_kv_write_layer_slots(const void *all_kv, const void *knorm_w, con
     if (num_ctx > 0 && (!layer_slot_mappings || !aligned(layer_slot_mappings, 8)))
         return fail(DSPARK_ERR_INVALID_ARG, "layer_slot_mappings must be an 8-byte aligned device pointer table");
     return write_common(all_kv, knorm_w, positions, nullptr, layer_slot_mappings, num_ctx, cos_sin, max_pos,
-                        layer0_cache, num_blocks, cache_offsets, k_scales, v_scales, L, nkv, block_size, rotary_dim,
-                        eps, kv_dtype, error_flags, stream);
+                        layer0_cache, num_blocks, cache_offsets, k_scales, v_scales, L, nkv, DSPARK_HEAD_DIM,
+                        block_size, rotary_dim, eps, kv_dtype, error_flags, stream, Rules::pages);
+}
+
+int dspark_ctx_kv_general_supported(int head_dim, int rotary_dim, int block_size)
+{
+    return (head_dim == 64 || head_dim == 128 || head_dim == 256) && rotary_dim >= 2 && rotary_dim <= head_dim &&
+           rotary_dim % 2 == 0 && block_size >= 1;
+}
+
+int dspark_ctx_kv_write_general(const void *all_kv, const void *knorm_w, const int64_t *positions,
+                                const int64_t *slot_mapping, const int64_t *const *layer_slot_mappings,
+                                int64_t num_ctx, const void *cos_sin, int64_t max_pos, void *layer0_cache,
+                                int64_t num_blocks, const int64_t *cache_offsets, const float *const *k_scales,
+                                const float *const *v_scales, int L, int nkv, int head_dim, int block_size,
+                                int rotary_dim, float eps, int kv_dtype, unsigned int *error_flags,
+                                cudaStream_t stream)
+{
+    if (num_ctx > 0 && (slot_mapping == nullptr) == (layer_slot_mappings == nullptr))
+        return fail(DSPARK_ERR_INVALID_ARG, "give exactly one of slot_mapping and layer_slot_mappings");
+    if (num_ctx > 0 && layer_slot_mappings && !aligned(layer_slot_mappings, 8))
+        return fail(DSPARK_ERR_ALIGNMENT, "layer_slot_mappings must be 8-byte aligned");
+    return write_common(all_kv, knorm_w, positions, slot_mapping, layer_slot_mappings, num_ctx, cos_sin, max_pos,
+                        layer0_cache, num_blocks, cache_offsets, k_scales, v_scales, L, nkv, head_dim, block_size,
+                        rotary_dim, eps, kv_dtype, error_flags, stream, Rules::general);
 }
 
 }  // extern "C"
 
 namespace {
 
+// Granlund-Montgomery magic of an invariant divisor d >= 3 that is not a
+// power of two, for dividends 0 <= n < 2^63: with l = ceil(log2 d),
+// m = ceil(2^(63 + l) / d) < 2^64 and floor(n / d) = umulhi(n, m) >> (l - 1).
+void block_divisor(int64_t d, uint64_t *magic, int *shift)
+{
+    const int l = log2_exact(d);
+    const unsigned __int128 num = (unsigned __int128)1 << (63 + l);
+    *magic = (uint64_t)((num + (unsigned __int128)(d - 1)) / (unsigned __int128)d);
+    *shift = l - 1;
+}
+
 int write_common(const void *all_kv, const void *knorm_w, const int64_t *positions, const int64_t *slot_mapping,
                  const int64_t *const *layer_slots, int64_t num_ctx, const void *cos_sin, int64_t max_pos,
                  void *layer0_cache, int64_t num_blocks, const int64_t *cache_offsets, const float *const *k_scales,
-                 const float *const *v_scales, int L, int nkv, int block_size, int rotary_dim, float eps,
-                 int kv_dtype, unsigned int *error_flags, cudaStream_t stream)
+                 const float *const *v_scales, int L, int nkv, int head_dim, int block_size, int rotary_dim,
+                 float eps, int kv_dtype, unsigned int *error_flags, cudaStream_t stream, Rules rules)
 {
     // Scalar checks first: they need no device and no pointer.
     if (num_ctx < 0)
@@ -144,18 +184,29 @@ int write_common(const void *all_kv, const void *knorm_w, const int64_t *positio
     if (num_blocks <= 0 || max_pos <= 0)
         return fail(DSPARK_ERR_INVALID_ARG, "num_blocks=%lld max_pos=%lld must be >= 1",
                     (long long)num_blocks, (long long)max_pos);
-    if (!dspark_ctx_kv_rotary_dims_supported(rotary_dim, DSPARK_HEAD_DIM))
-        return fail(DSPARK_ERR_UNSUPPORTED_ROTARY_DIM, "rotary_dim %d not in {16, 32, 64}", rotary_dim);
-    if (!pow2(block_size))
-        return fail(DSPARK_ERR_BLOCK_SIZE, "block size %d is not a power of two", block_size);
+    if (rules == Rules::pages) {
+        if (!dspark_ctx_kv_rotary_dims_supported(rotary_dim, DSPARK_HEAD_DIM))
+            return fail(DSPARK_ERR_UNSUPPORTED_ROTARY_DIM, "rotary_dim %d not in {16, 32, 64}", rotary_dim);
+        if (!pow2(block_size))
+            return fail(DSPARK_ERR_BLOCK_SIZE, "block size %d is not a power of two", block_size);
+    } else {
+        if (head_dim != 64 && head_dim != 128 && head_dim != 256)
+            return fail(DSPARK_ERR_INVALID_ARG, "head_dim %d not 64, 128 or 256", head_dim);
+        if (rotary_dim < 2 || rotary_dim > head_dim || rotary_dim % 2 != 0)
+            return fail(DSPARK_ERR_UNSUPPORTED_ROTARY_DIM, "rotary_dim %d not even in [2, %d]", rotary_dim,
+                        head_dim);
+        if (block_size < 1)
+            return fail(DSPARK_ERR_BLOCK_SIZE, "block size %d < 1", block_size);
+    }
     if (kv_dtype != DSPARK_KV_BF16 && kv_dtype != DSPARK_KV_FP8_E4M3)
         return fail(DSPARK_ERR_DTYPE, "kv dtype %d unknown", kv_dtype);
     if (!(eps >= 0.0f) || std::isinf(eps))
         return fail(DSPARK_ERR_INVALID_ARG, "eps must be finite and >= 0");
+    const int64_t row_elems = 2 * (int64_t)head_dim;
     const int64_t capacity = num_blocks * (int64_t)block_size;
-    if (capacity / block_size != num_blocks || num_blocks > (INT64_MAX / nkv) / block_size / DSPARK_CACHE_ROW)
+    if (capacity / block_size != num_blocks || num_blocks > (INT64_MAX / nkv) / block_size / row_elems)
         return fail(DSPARK_ERR_INVALID_ARG, "cache of %lld blocks too large", (long long)num_blocks);
-    if (num_ctx > (INT64_MAX / L) / nkv / (2 * DSPARK_HEAD_DIM))
+    if (num_ctx > (INT64_MAX / L) / nkv / row_elems)
         return fail(DSPARK_ERR_INVALID_ARG, "num_ctx %lld too large", (long long)num_ctx);
     if (num_ctx == 0)
         return ok();  // nothing to store, and no launch
@@ -189,12 +240,28 @@ int write_common(const void *all_kv, const void *knorm_w, const int64_t *positio
     p.capacity = capacity;
     p.num_layers = L;
     p.num_kv_heads = nkv;
-    p.block_size_log2 = log2_exact(block_size);
+    p.block_size_log2 = pow2(block_size) ? log2_exact(block_size) : -1;
     p.eps = eps;
+    p.rotary_dim = rotary_dim;
+    p.block_size = block_size;
+    if (!pow2(block_size))
+        block_divisor(block_size, &p.bs_magic, &p.bs_magic_shift);
     const bool fp8 = kv_dtype == DSPARK_KV_FP8_E4M3;
-    cudaError_t e = (!force_generic() && dspark::tma_path_supported(p))
-                        ? dspark::launch_ctx_kv_write_tma(p, rotary_dim, fp8, stream)
-                        : dspark::launch_ctx_kv_write(p, rotary_dim, fp8, stream);
+    // the pipelined kernel where its stage holds a token's rows; else the
+    // generic kernel (the pages' layouts) or the general one (any other)
+    const bool pages_layout = head_dim == DSPARK_HEAD_DIM && pow2(block_size) &&
+                              dspark_ctx_kv_rotary_dims_supported(rotary_dim, DSPARK_HEAD_DIM);
+    cudaError_t e;
+    if (force_kernel("general"))
+        e = dspark::launch_ctx_kv_general(p, head_dim, fp8, stream);
+    else if (pages_layout && force_kernel("generic"))
+        e = dspark::launch_ctx_kv_write(p, rotary_dim, fp8, stream);
+    else if (dspark::tma_path_supported(p, head_dim))
+        e = dspark::launch_ctx_kv_write_tma(p, head_dim, fp8, stream);
+    else if (pages_layout)
+        e = dspark::launch_ctx_kv_write(p, rotary_dim, fp8, stream);
+    else
+        e = dspark::launch_ctx_kv_general(p, head_dim, fp8, stream);
     if (e != cudaSuccess)
         return fail(DSPARK_ERR_CUDA, "launch failed: %s", cudaGetErrorString(e));
     return ok();
@@ -439,7 +506,11 @@ int dspark_gemma_rms_norm(const void *x, const void *w, void *out, int64_t rows,
     return ok();
 }
 
-int dspark_ctx_kv_validate_layers(int L, const dspark_cache_desc *layers)
+}  // extern "C"
+
+namespace {
+
+int validate_layers(int L, const dspark_cache_desc *layers, Rules rules)
 {
     if (L <= 0 || !layers)
         return fail(DSPARK_ERR_INVALID_ARG, "no layers");
@@ -450,12 +521,14 @@ int dspark_ctx_kv_validate_layers(int L, const dspark_cache_desc *layers)
             return fail(DSPARK_ERR_DTYPE, "layer %d: kv_cache_dtype unsupported", l);
         if (!a.data)
             return fail(DSPARK_ERR_INVALID_ARG, "layer %d: KV cache not bound", l);
-        if (a.ndim != 4 || a.shape[3] != DSPARK_CACHE_ROW)
+        const bool row_ok = rules == Rules::pages ? a.shape[3] == DSPARK_CACHE_ROW
+                                                  : (a.shape[3] == 128 || a.shape[3] == 256 || a.shape[3] == 512);
+        if (a.ndim != 4 || !row_ok)
             return fail(DSPARK_ERR_INVALID_ARG, "layer %d: unexpected cache shape", l);
         for (int d = 0; d < 4; d++)
             if (a.shape[d] <= 0)
                 return fail(DSPARK_ERR_INVALID_ARG, "layer %d: KV cache not bound (empty)", l);
-        if (!pow2(a.shape[2]))
+        if (rules == Rules::pages && !pow2(a.shape[2]))
             return fail(DSPARK_ERR_BLOCK_SIZE, "layer %d: block size %lld is not a power of two", l,
                         (long long)a.shape[2]);
         int64_t expect = 1;
@@ -483,6 +556,20 @@ int dspark_ctx_kv_validate_layers(int L, const dspark_cache_desc *layers)
             return fail(DSPARK_ERR_ALIGNMENT, "layer caches are not 16-element aligned to each other");
     }
     return ok();
+}
+
+}  // namespace
+
+extern "C" {
+
+int dspark_ctx_kv_validate_layers(int L, const dspark_cache_desc *layers)
+{
+    return validate_layers(L, layers, Rules::pages);
+}
+
+int dspark_ctx_kv_validate_layers_general(int L, const dspark_cache_desc *layers)
+{
+    return validate_layers(L, layers, Rules::general);
 }
 
 }  // extern "C"

@@ -32,19 +32,30 @@ struct CtxKvParams {
     int32_t num_layers;
     int32_t num_kv_heads;
     int32_t head_chunks;         // ceil(num_kv_heads / heads per unit)
-    int32_t block_size_log2;
+    int32_t block_size_log2;     // -1 (general kernel only): not a power of two
     float eps;
+    // general kernel only (launch_ctx_kv_general)
+    int32_t rotary_dim;          // even, 2..head_dim
+    int32_t block_size;
+    int32_t bs_magic_shift;      // block = umulhi(slot, bs_magic) >> bs_magic_shift
+    uint64_t bs_magic;           //   when block_size_log2 < 0
 };
 
 // Generic kernel (any layer count and head count): enqueues the write on
 // `stream`.  Returns cudaSuccess or the launch error.
 cudaError_t launch_ctx_kv_write(const CtxKvParams &p, int rotary_dim, bool fp8, cudaStream_t stream);
 
-// Pipelined bulk-copy kernel: handles up to 32 layers and up to 64 KV heads
-// (one layer's K|V rows of a token fit a 32 KB stage), with a shared or a
-// per-layer slot mapping.
-bool tma_path_supported(const CtxKvParams &p);
-cudaError_t launch_ctx_kv_write_tma(const CtxKvParams &p, int rotary_dim, bool fp8, cudaStream_t stream);
+// The write for head dims 64, 128 and 256, any even rotary_dim up to the
+// head dim and any block size (ctx_kv_general.cu): all_kv [T, L, 2, H, D],
+// knorm_w [L, D], cache rows of 2D elements.
+cudaError_t launch_ctx_kv_general(const CtxKvParams &p, int head_dim, bool fp8, cudaStream_t stream);
+
+// Pipelined bulk-copy kernel: head dims 64, 128 and 256, any even rotary dim
+// up to the head dim (p.rotary_dim), any block size; up to 32 layers, and one
+// layer's K|V rows of a token must fit a 32 KB stage (nkv * 4 * head_dim
+// bytes); a shared or a per-layer slot mapping.
+bool tma_path_supported(const CtxKvParams &p, int head_dim);
+cudaError_t launch_ctx_kv_write_tma(const CtxKvParams &p, int head_dim, bool fp8, cudaStream_t stream);
 
 // Draft-token fused QK-norm / RoPE / KV insert (qk_insert_kernel.cu).
 struct QkInsertParams {

@@ -1,14 +1,16 @@
 // sm_103a pipelined kernel of the DSpark fused context-KV write (the fast
-// path; ctx_kv_kernel.cu keeps the generic one).
+// path; ctx_kv_kernel.cu and ctx_kv_general.cu keep the fallbacks).
 //
 // Defining passage: vLLM DSpark context-KV writer page, module docstring (one
 // launch for all draft layers: Gemma RMSNorm of K in fp32 materialised to
 // bf16, partial NeoX RoPE at the token's position, K|V stored into each
-// layer's [num_blocks, nkv, block_size, 256] cache as bf16 or fp8 e4m3 of
-// x / scale, slots < 0 not written).
+// layer's [num_blocks, nkv, block_size, 2D] cache as bf16 or fp8 e4m3 of
+// x / scale, slots < 0 not written).  The pages' head dim D is 128; this
+// kernel also takes 64 and 256, any even rotary_dim up to D and any block
+// size (the layouts their writer hands to the unfused path).
 //
 // Data movement.  all_kv[t, l0 : l0 + Lp] -- every K and V row of Lp layers of
-// one token -- is one contiguous block of Lp * nkv * 512 bytes.  Each CTA runs
+// one token -- is one contiguous block of Lp * nkv * 4D bytes.  Each CTA runs
 // a ring of shared-memory stages: a producer warp reads the slot and position
 // of its next tokens, skips padding (nothing of a padded token is read), and
 // for each valid (token, layer piece) issues one bulk asynchronous copy
@@ -19,12 +21,16 @@
 // registers, so the HBM queue stays full with few warps.
 //
 // Compute mapping.  A consumer warp handles 4 rows per instruction: 8 lanes
-// per row, each lane holding dims [8q, 8q+8) and [64+8q, 64+8q+8) of K and of
-// V (q = lane % 8), so every 16-byte shared load is conflict-free and every
-// 16-byte (bf16) or 8-byte (fp8) global store of a warp covers 4 whole
-// 128-byte (64-byte) segments.  Sum of squares: 8 paired FMAs + 3 xor shuffles
-// within the row's 8 lanes.  RoPE (only dims < 64 can rotate): the partner of
-// dim d is d +- r/2, r/16 lanes away within the row's 8 lanes.  fp8: the
+// per row, each lane holding the D/64 chunks [64k + 8q, 64k + 8q + 8) of K
+// and of V (q = lane % 8), so every 16-byte shared load is conflict-free and
+// every 16-byte (bf16) or 8-byte (fp8) global store of a warp covers 4 whole
+// 128-byte (64-byte) segments.  Sum of squares: paired FMAs + 3 xor shuffles
+// within the row's 8 lanes.  RoPE with r = 16, 32 or 64: the partner of dim
+// d is d +- r/2, r/16 lanes away within the row's 8 lanes (one xor shuffle).
+// Any other even r: the normed row is written back over its K row in the
+// stage, and after a __syncwarp each rotated dim reads its partner there; the
+// token's cos|sin row is staged per warp from global memory (a row of 2r
+// bytes need not be a multiple of the 16 a bulk copy moves).  fp8: the
 // quotient x / scale is formed from the correctly rounded reciprocal of the
 // scale with one FMA correction step (Markstein's method: q0 = x*(1/s),
 // e = x - q0*s exactly, q = q0 + e*(1/s)), which yields the correctly rounded
@@ -65,6 +71,7 @@ constexpr int kMaxTmaLayers = 32;
 // What the producer tells the consumers about a stage.
 struct StageHdr {
     long long dst;  // byte offset of the token's row for head 0 within a layer's cache
+    long long pos;  // the token's position (rotary dims other than 16 / 32 / 64)
     int l0;         // first layer in the stage
     int rows;       // rows in the stage (layers * nkv); < 0: end of work
 };
@@ -210,7 +217,7 @@ __device__ __forceinline__ uint64_t rope_bf2(uint32_t y, uint32_t c, uint32_t yp
 // Shared-memory layout (dynamic): barriers and headers, per-layer tables,
 // then the stages (128-byte aligned).
 struct Layout {
-    uint32_t full, empty, hdr, abort, w1, off, scl, pls, pdst, stages, stage_bytes, slab_bytes, total;
+    uint32_t full, empty, hdr, abort, w1, off, scl, pls, pdst, csw, stages, stage_bytes, slab_bytes, total;
 };
 
 __host__ __device__ inline uint32_t align_up(uint32_t v, uint32_t a) { return (v + a - 1) / a * a; }
@@ -218,8 +225,10 @@ __host__ __device__ inline uint32_t align_up(uint32_t v, uint32_t a) { return (v
 // pl: layers per unit when every layer has its own slot mapping (then the
 // producer prefetches each unit's per-layer slots into a double-buffered
 // [2][32][pl] table and hands the consumers per-layer row offsets [S][pl]),
-// else 0.
-__host__ __device__ inline Layout make_layout(int L, int S, uint32_t slab_bytes, int pl = 0)
+// else 0.  D: the head dim.  xor_rot: r is 16, 32 or 64 (the cos|sin row is
+// bulk-copied into each stage); else every consumer warp stages it in its own
+// 2D-byte slot.
+__host__ __device__ inline Layout make_layout(int L, int S, uint32_t slab_bytes, int pl, int D, bool xor_rot)
 {
     Layout y;
     uint32_t o = 0;
@@ -232,7 +241,7 @@ __host__ __device__ inline Layout make_layout(int L, int S, uint32_t slab_bytes,
     y.abort = o;
     o += 16;
     y.w1 = align_up(o, 16);
-    o = y.w1 + 4 * kHeadDim * L;  // 32 float4 slots per layer
+    o = y.w1 + 4 * D * L;  // D / 4 float4 slots per layer
     y.off = align_up(o, 8);  // per layer: its cache's base address
     o = y.off + 8 * L;
     y.scl = align_up(o, 16);  // per layer, 48 bytes: (k, k), (v, v), (-1/k, -1/k), (-1/v, -1/v), k bound, v bound
@@ -241,9 +250,11 @@ __host__ __device__ inline Layout make_layout(int L, int S, uint32_t slab_bytes,
     o = y.pls + 2 * 32 * 8 * pl;
     y.pdst = align_up(o, 16);
     o = y.pdst + 8 * S * pl;
+    y.csw = align_up(o, 16);
+    o = y.csw + (xor_rot ? 0 : kConsumerWarps * 2 * D);
     y.stages = align_up(o, 128);
     y.slab_bytes = slab_bytes;
-    y.stage_bytes = align_up(slab_bytes + kCsBytes, 128);
+    y.stage_bytes = align_up(slab_bytes + (xor_rot ? kCsBytes : 0), 128);
     y.total = y.stages + y.stage_bytes * S;
     return y;
 }
@@ -258,19 +269,30 @@ struct TmaParams {
 };
 
 // w1 table: float4 slot of (layer l, half jj of an 8-dim chunk, chunk c of
-// the 16 chunks): lane q reads slots c = q (dims 8q..) and c = 8 + q (dims
-// 64 + 8q..), so the 8 lanes of a row read 128 contiguous bytes per load.
-__device__ __forceinline__ int w1_slot(int l, int jj, int c) { return l * 32 + jj * 16 + c; }
+// the D/8 chunks): lane q reads slots c = 8k + q (dims 64k + 8q..), so the 8
+// lanes of a row read 128 contiguous bytes per load.
+template <int D>
+__device__ __forceinline__ int w1_slot(int l, int jj, int c)
+{
+    return l * (D / 4) + jj * (D / 8) + c;
+}
 
-// PL: every layer has its own slot mapping (p.layer_slots); a template
-// parameter, so the shared-mapping path carries none of its branches.
-template <int ROT, bool FP8, bool PL>
+// D: the head dim (64, 128, 256).  ROT: the rotary dim when it is 16, 32 or
+// 64 (partners one xor shuffle away), or 0: any even p.rotary_dim up to D
+// (partners through shared memory).  PL: every layer has its own slot
+// mapping (p.layer_slots).  Template parameters, so each path carries none
+// of the others' branches.
+template <int D, int ROT, bool FP8, bool PL>
 __global__ void __launch_bounds__(kThreads, 2) ctx_kv_tma_kernel(const TmaParams tp)
 {
+    constexpr int NC = D / 64;                  // 8-dim chunks of K (and of V) per lane
+    constexpr uint32_t kRowIn = 4 * D;          // bytes of one K|V row pair in all_kv
+    constexpr int kCacheRow = FP8 ? 2 * D : 4 * D;  // bytes of one cache row
+    constexpr bool kXor = ROT != 0;
     extern __shared__ __align__(128) unsigned char smem[];
     const CtxKvParams &p = tp.p;
     const int L = p.num_layers, H = p.num_kv_heads, S = tp.stages, NP = tp.pieces, Lp = tp.layers_per_piece;
-    const Layout lay = make_layout(L, S, (uint32_t)Lp * H * 512u, PL ? Lp : 0);
+    const Layout lay = make_layout(L, S, (uint32_t)Lp * H * kRowIn, PL ? Lp : 0, D, kXor);
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + lay.full);
     uint64_t *empty = reinterpret_cast<uint64_t *>(smem + lay.empty);
     StageHdr *hdr = reinterpret_cast<StageHdr *>(smem + lay.hdr);
@@ -314,11 +336,19 @@ __global__ void __launch_bounds__(kThreads, 2) ctx_kv_tma_kernel(const TmaParams
             u_end = units;
             step = G;
         }
-        // row offset of a slot's (block, offset) row for head 0 within a layer's cache
+        // byte offset of a slot's (block, offset) row for head 0 within a
+        // layer's cache: a power-of-two block size shifts, any other divides
+        // by a multiply-high with the host's magic number
         auto row_off = [&](long long slot) {
-            return (((slot >> p.block_size_log2) * H << p.block_size_log2) +
-                    (slot & ((1LL << p.block_size_log2) - 1))) *
-                   (FP8 ? kRowElems : 2 * kRowElems);
+            long long blk, off;
+            if (p.block_size_log2 >= 0) {
+                blk = slot >> p.block_size_log2;
+                off = slot & ((1LL << p.block_size_log2) - 1);
+            } else {
+                blk = (long long)(__umul64hi((unsigned long long)slot, p.bs_magic) >> p.bs_magic_shift);
+                off = slot - blk * p.block_size;
+            }
+            return (blk * H * p.block_size + off) * kCacheRow;
         };
         // Slot and position of unit base + lane * step.  With per-layer
         // mappings the unit's layers' slots go to the prefetch table (buffer
@@ -392,7 +422,7 @@ __global__ void __launch_bounds__(kThreads, 2) ctx_kv_tma_kernel(const TmaParams
         auto unit_span = [&](long long u, long long &t, int &l0, uint32_t &slab) {
             t = NP == 1 ? u : u / NP;
             l0 = (NP == 1 ? 0 : (int)(u - t * NP)) * Lp;
-            slab = (uint32_t)min(Lp, L - l0) * H * 512u;
+            slab = (uint32_t)min(Lp, L - l0) * H * kRowIn;
         };
         int nspec = 0;
         for (long long u = u_first; u < u_end && nspec < S; u += step)
@@ -404,7 +434,7 @@ __global__ void __launch_bounds__(kThreads, 2) ctx_kv_tma_kernel(const TmaParams
                 uint32_t slab;
                 unit_span(u_first + i * step, t, l0, slab);
                 mbar_expect_tx(full + i, slab);
-                bulk_g2s(stages + (size_t)i * lay.stage_bytes, p.all_kv + (t * L + l0) * 2LL * H * kHeadDim, slab,
+                bulk_g2s(stages + (size_t)i * lay.stage_bytes, p.all_kv + (t * L + l0) * 2LL * H * D, slab,
                          full + i, stream_once);
             }
         }
@@ -442,21 +472,28 @@ __global__ void __launch_bounds__(kThreads, 2) ctx_kv_tma_kernel(const TmaParams
                         } else {
                             if (PL) {
                                 const long long *e = pls + (buf * 32 + i) * Lp;
-                                for (int j = 0; j < (int)(slab / 512u) / H; j++)
+                                for (int j = 0; j < (int)(slab / kRowIn) / H; j++)
                                     pdst[s * Lp + j] = e[j] >= 0 ? row_off(e[j]) : -1;
                             } else {
                                 hdr[s].dst = row_off(slot);
                             }
                             hdr[s].l0 = l0;
-                            hdr[s].rows = (int)(slab / 512u);
+                            hdr[s].pos = pos;
+                            hdr[s].rows = (int)(slab / kRowIn);
+                            // the cos|sin row rides along in the xor modes (2r = 32, 64 or
+                            // 128 bytes); otherwise the consumers fetch it themselves
+                            const uint32_t cs_bytes = kXor ? 2u * ROT : 0u;
                             if (spec) {
-                                mbar_arrive_expect_tx(full + s, 2u * ROT);
+                                if (kXor)
+                                    mbar_arrive_expect_tx(full + s, cs_bytes);
+                                else
+                                    mbar_arrive(full + s);
                             } else {
-                                mbar_arrive_expect_tx(full + s, slab + 2u * ROT);
-                                bulk_g2s(dst, p.all_kv + (t * L + l0) * 2LL * H * kHeadDim, slab, full + s,
-                                         stream_once);
+                                mbar_arrive_expect_tx(full + s, slab + cs_bytes);
+                                bulk_g2s(dst, p.all_kv + (t * L + l0) * 2LL * H * D, slab, full + s, stream_once);
                             }
-                            bulk_g2s(dst + lay.slab_bytes, p.cos_sin + pos * ROT, 2u * ROT, full + s, keep);
+                            if (kXor)
+                                bulk_g2s(dst + lay.slab_bytes, p.cos_sin + pos * ROT, 2u * ROT, full + s, keep);
                         }
                     }
                 }
@@ -502,10 +539,10 @@ __global__ void __launch_bounds__(kThreads, 2) ctx_kv_tma_kernel(const TmaParams
     } else {
         // ---------------------------------------------------------- consumers
         // per-layer tables: (1 + w) in fp32, cache offsets, scale constants
-        for (int i = tid; i < L * kHeadDim; i += 32 * kConsumerWarps) {
-            const int l = i / kHeadDim, d = i % kHeadDim;
+        for (int i = tid; i < L * D; i += 32 * kConsumerWarps) {
+            const int l = i / D, d = i % D;
             const int c = d / 8, j = d % 8;  // chunk c holds dims 8c .. 8c+7
-            reinterpret_cast<float *>(w1)[w1_slot(l, j / 4, c) * 4 + (j % 4)] =
+            reinterpret_cast<float *>(w1)[w1_slot<D>(l, j / 4, c) * 4 + (j % 4)] =
                 1.0f + __uint_as_float((uint32_t)__ldg(p.knorm_w + i) << 16);
         }
         for (int l = tid; l < L; l += 32 * kConsumerWarps) {
@@ -528,13 +565,15 @@ __global__ void __launch_bounds__(kThreads, 2) ctx_kv_tma_kernel(const TmaParams
         }
         asm volatile("bar.sync 1, %0;" ::"n"(32 * kConsumerWarps) : "memory");
 
-        const int q = lane & 7;      // 8-dim chunk of the row's first and second half
+        const int q = lane & 7;      // 8-dim chunk of each 64-dim segment of the row
         const int rr = lane >> 3;    // row of the 4-row group
-        constexpr int kPartner = ROT / 16;
+        constexpr int kPartner = kXor ? ROT / 16 : 1;
         constexpr int kRotLanes = ROT / 8;
-        const bool rot_lane = q < kRotLanes;
+        const bool rot_lane = kXor && q < kRotLanes;
+        const int rdim = kXor ? ROT : p.rotary_dim, half = rdim >> 1;
+        uint16_t *csw = reinterpret_cast<uint16_t *>(smem + lay.csw) + warp * D;  // this warp's cos|sin slot
         // bytes between the rows of consecutive heads in a cache
-        const long long head_bytes = (long long)(FP8 ? kRowElems : 2 * kRowElems) << p.block_size_log2;
+        const long long head_bytes = (long long)kCacheRow * p.block_size;
         int gmod = 0;  // row groups seen so far, over all stages, modulo the consumer warps
         int s = 0;          // ring slot of the current round
         uint32_t ph = 0;    // its phase parity
@@ -549,36 +588,45 @@ __global__ void __launch_bounds__(kThreads, 2) ctx_kv_tma_kernel(const TmaParams
             const int first = (warp - gmod) & (kConsumerWarps - 1);  // this warp's first group here
             gmod = (gmod + ngroups) & (kConsumerWarps - 1);
             if (first < ngroups) {
-                const unsigned char *stage = stages + (size_t)s * lay.stage_bytes;
-                // cos and sign * sin (bf16 pairs) of this token for the lane's 8 dims
+                unsigned char *stage = stages + (size_t)s * lay.stage_bytes;
+                // xor modes: cos and sign * sin (bf16 pairs) of this token for the lane's first 8 dims
                 uint32_t cw[4] = {0, 0, 0, 0}, sw[4] = {0, 0, 0, 0};
-                if (rot_lane) {
-                    const unsigned char *cs = stage + lay.slab_bytes + 16 * (q & (kPartner - 1));
-                    const uint4 c4 = lds128(cs), s4 = lds128(cs + ROT);  // sin half: r/2 elements later
-                    const uint32_t flip = (q & kPartner) ? 0u : 0x80008000u;  // lower half subtracts
-                    cw[0] = c4.x, cw[1] = c4.y, cw[2] = c4.z, cw[3] = c4.w;
-                    sw[0] = s4.x ^ flip, sw[1] = s4.y ^ flip, sw[2] = s4.z ^ flip, sw[3] = s4.w ^ flip;
+                if constexpr (kXor) {
+                    if (rot_lane) {
+                        const unsigned char *cs = stage + lay.slab_bytes + 16 * (q & (kPartner - 1));
+                        const uint4 c4 = lds128(cs), s4 = lds128(cs + ROT);  // sin half: r/2 elements later
+                        const uint32_t flip = (q & kPartner) ? 0u : 0x80008000u;  // lower half subtracts
+                        cw[0] = c4.x, cw[1] = c4.y, cw[2] = c4.z, cw[3] = c4.w;
+                        sw[0] = s4.x ^ flip, sw[1] = s4.y ^ flip, sw[2] = s4.z ^ flip, sw[3] = s4.w ^ flip;
+                    }
+                } else {
+                    // the token's cos|sin row into this warp's slot, as 4-byte words (r is even)
+                    const uint32_t *src = reinterpret_cast<const uint32_t *>(p.cos_sin + h_s.pos * rdim);
+                    uint32_t *dst = reinterpret_cast<uint32_t *>(csw);
+                    for (int k = lane; k < half; k += 32)
+                        dst[k] = __ldg(src + k);
+                    __syncwarp();
                 }
                 for (int g = first; g < ngroups; g += kConsumerWarps) {
-                    const int r = g * 4 + rr;
-                    const bool active = r < R;
-                    const int rc = active ? r : R - 1;
+                    const int row = g * 4 + rr;
+                    const bool active = row < R;
+                    const int rc = active ? row : R - 1;
                     const int lr = (int)(((uint64_t)(uint32_t)rc * tp.h_magic) >> 32);
                     const int h = rc - lr * H;
                     const int l = h_s.l0 + lr;
-                    const unsigned char *krow = stage + ((size_t)(2 * lr) * H + h) * 256;
-                    const unsigned char *vrow = krow + (size_t)H * 256;
-                    const uint4 ka = lds128(krow + 16 * q), kb = lds128(krow + 128 + 16 * q);
-                    const uint4 va = lds128(vrow + 16 * q), vb = lds128(vrow + 128 + 16 * q);
-                    const uint32_t kw[8] = {ka.x, ka.y, ka.z, ka.w, kb.x, kb.y, kb.z, kb.w};
-                    uint64_t x2[8];
+                    unsigned char *krow = stage + ((size_t)(2 * lr) * H + h) * (2 * D);
+                    const unsigned char *vrow = krow + (size_t)H * (2 * D);
+                    uint64_t x2[4 * NC];
 #pragma unroll
-                    for (int j = 0; j < 8; j++)
-                        x2[j] = bf2_to_f2(kw[j]);
+                    for (int k = 0; k < NC; k++) {
+                        const uint4 a = lds128(krow + 128 * k + 16 * q);
+                        x2[4 * k] = bf2_to_f2(a.x), x2[4 * k + 1] = bf2_to_f2(a.y);
+                        x2[4 * k + 2] = bf2_to_f2(a.z), x2[4 * k + 3] = bf2_to_f2(a.w);
+                    }
                     // sum of squares: two accumulator chains of packed FMAs
                     uint64_t a0 = mul2(x2[0], x2[0]), a1 = mul2(x2[1], x2[1]);
 #pragma unroll
-                    for (int j = 2; j < 8; j += 2) {
+                    for (int j = 2; j < 4 * NC; j += 2) {
                         a0 = fma2(x2[j], x2[j], a0);
                         a1 = fma2(x2[j + 1], x2[j + 1], a1);
                     }
@@ -588,46 +636,97 @@ __global__ void __launch_bounds__(kThreads, 2) ctx_kv_tma_kernel(const TmaParams
                     ss += __shfl_xor_sync(0xffffffffu, ss, 4);
                     ss += __shfl_xor_sync(0xffffffffu, ss, 2);
                     ss += __shfl_xor_sync(0xffffffffu, ss, 1);
-                    float inv;  // ss/128 + eps >= eps > 0 (hardware reciprocal square root)
-                    asm("rsqrt.approx.ftz.f32 %0, %1;" : "=f"(inv) : "f"(fmaf(ss, 1.0f / kHeadDim, p.eps)));
+                    float inv;  // ss/D + eps >= eps > 0 (hardware reciprocal square root)
+                    asm("rsqrt.approx.ftz.f32 %0, %1;" : "=f"(inv) : "f"(fmaf(ss, 1.0f / D, p.eps)));
                     const uint64_t inv2 = pr(inv, inv);
-                    const float4 wa0 = w1[w1_slot(l, 0, q)], wa1 = w1[w1_slot(l, 1, q)];
-                    const float4 wb0 = w1[w1_slot(l, 0, 8 + q)], wb1 = w1[w1_slot(l, 1, 8 + q)];
-                    const uint64_t w2[8] = {pr(wa0.x, wa0.y), pr(wa0.z, wa0.w), pr(wa1.x, wa1.y), pr(wa1.z, wa1.w),
-                                            pr(wb0.x, wb0.y), pr(wb0.z, wb0.w), pr(wb1.x, wb1.y), pr(wb1.z, wb1.w)};
                     // y = bf16((k * inv) * (1 + w))
-                    uint32_t y[8];
+                    uint32_t y[4 * NC];
 #pragma unroll
-                    for (int j = 0; j < 8; j++)
-                        y[j] = f2_to_bf2(mul2(mul2(x2[j], inv2), w2[j]));
-                    // RoPE on the first chunk (dims 8q .. 8q+7); the partner is kPartner lanes away
-                    uint32_t ko[4];
+                    for (int k = 0; k < NC; k++) {
+                        const float4 wa = w1[w1_slot<D>(l, 0, 8 * k + q)], wb = w1[w1_slot<D>(l, 1, 8 * k + q)];
+                        y[4 * k] = f2_to_bf2(mul2(mul2(x2[4 * k], inv2), pr(wa.x, wa.y)));
+                        y[4 * k + 1] = f2_to_bf2(mul2(mul2(x2[4 * k + 1], inv2), pr(wa.z, wa.w)));
+                        y[4 * k + 2] = f2_to_bf2(mul2(mul2(x2[4 * k + 2], inv2), pr(wb.x, wb.y)));
+                        y[4 * k + 3] = f2_to_bf2(mul2(mul2(x2[4 * k + 3], inv2), pr(wb.z, wb.w)));
+                    }
+                    uint32_t ko[4 * NC];
+                    if constexpr (kXor) {
+                        // RoPE on the first chunk (dims 8q .. 8q+7); the partner is kPartner lanes away
 #pragma unroll
-                    for (int j = 0; j < 4; j++) {
-                        const uint32_t yp = __shfl_xor_sync(0xffffffffu, y[j], kPartner);
-                        const uint32_t rv = f2_to_bf2(rope_bf2(y[j], cw[j], yp, sw[j]));
-                        ko[j] = rot_lane ? rv : y[j];  // both computed: a select, not a branch
+                        for (int j = 0; j < 4; j++) {
+                            const uint32_t yp = __shfl_xor_sync(0xffffffffu, y[j], kPartner);
+                            const uint32_t rv = f2_to_bf2(rope_bf2(y[j], cw[j], yp, sw[j]));
+                            ko[j] = rot_lane ? rv : y[j];  // both computed: a select, not a branch
+                        }
+#pragma unroll
+                        for (int j = 4; j < 4 * NC; j++)
+                            ko[j] = y[j];
+                    } else {
+                        // the normed row over its K row in the stage (the row's 8 lanes own it),
+                        // then each rotated dim d reads its partner d +- r/2 there
+#pragma unroll
+                        for (int k = 0; k < NC; k++)
+                            *reinterpret_cast<uint4 *>(krow + 128 * k + 16 * q) =
+                                make_uint4(y[4 * k], y[4 * k + 1], y[4 * k + 2], y[4 * k + 3]);
+                        __syncwarp();
+                        const uint16_t *yrow = reinterpret_cast<const uint16_t *>(krow);
+#pragma unroll
+                        for (int k = 0; k < NC; k++) {
+                            const int d0 = 64 * k + 8 * q;
+#pragma unroll
+                            for (int j = 0; j < 4; j++) {
+                                ko[4 * k + j] = y[4 * k + j];
+                                if (d0 + 2 * j < rdim) {
+                                    float o[2];
+#pragma unroll
+                                    for (int b = 0; b < 2; b++) {
+                                        const int d = d0 + 2 * j + b;  // d < r: r is even
+                                        const bool lower = d < half;
+                                        const int fi = lower ? d : d - half;
+                                        const float yd = __uint_as_float(b ? (y[4 * k + j] & 0xffff0000u)
+                                                                           : (y[4 * k + j] << 16));
+                                        const float c = __uint_as_float((uint32_t)csw[fi] << 16);
+                                        const float sn = __uint_as_float((uint32_t)csw[half + fi] << 16);
+                                        const float yp = __uint_as_float((uint32_t)yrow[lower ? d + half : d - half] << 16);
+                                        o[b] = fmaf(yd, c, lower ? -(yp * sn) : yp * sn);
+                                    }
+                                    ko[4 * k + j] = pack_bf16x2(o[0], o[1]);
+                                }
+                            }
+                        }
                     }
                     const long long roff = PL ? pdst[s * Lp + lr] : h_s.dst;
                     if (!active || roff < 0)
                         continue;  // past the stage's rows, or a layer padded in its own mapping
-                    unsigned char *d = layer_base[l] + roff + h * head_bytes;
+                    unsigned char *dg = layer_base[l] + roff + h * head_bytes;
                     if (!FP8) {
-                        st_stream_v4(d + 16 * q, make_uint4(ko[0], ko[1], ko[2], ko[3]));
-                        st_stream_v4(d + 128 + 16 * q, make_uint4(y[4], y[5], y[6], y[7]));
-                        st_stream_v4(d + 256 + 16 * q, va);
-                        st_stream_v4(d + 384 + 16 * q, vb);
+#pragma unroll
+                        for (int k = 0; k < NC; k++)
+                            st_stream_v4(dg + 128 * k + 16 * q, make_uint4(ko[4 * k], ko[4 * k + 1], ko[4 * k + 2],
+                                                                          ko[4 * k + 3]));
+#pragma unroll
+                        for (int k = 0; k < NC; k++)
+                            st_stream_v4(dg + 2 * D + 128 * k + 16 * q, lds128(vrow + 128 * k + 16 * q));
                     } else {
                         const ulonglong2 sv = reinterpret_cast<const ulonglong2 *>(scl + 12 * l)[0];
                         const ulonglong2 nv = reinterpret_cast<const ulonglong2 *>(scl + 12 * l)[1];
                         const uint2 b2 = *reinterpret_cast<const uint2 *>(scl + 12 * l + 8);
                         const uint64_t ks2 = sv.x, vs2 = sv.y, kn2 = nv.x, vn2 = nv.y;
-                        st_stream_v2(d + 8 * q, quantise8(make_uint4(ko[0], ko[1], ko[2], ko[3]), b2.x, ks2, kn2));
-                        st_stream_v2(d + 64 + 8 * q, quantise8(make_uint4(y[4], y[5], y[6], y[7]), b2.x, ks2, kn2));
-                        st_stream_v2(d + 128 + 8 * q, quantise8(va, b2.y, vs2, vn2));
-                        st_stream_v2(d + 192 + 8 * q, quantise8(vb, b2.y, vs2, vn2));
+#pragma unroll
+                        for (int k = 0; k < NC; k++)
+                            st_stream_v2(dg + 64 * k + 8 * q,
+                                         quantise8(make_uint4(ko[4 * k], ko[4 * k + 1], ko[4 * k + 2], ko[4 * k + 3]),
+                                                   b2.x, ks2, kn2));
+#pragma unroll
+                        for (int k = 0; k < NC; k++)
+                            st_stream_v2(dg + D + 64 * k + 8 * q, quantise8(lds128(vrow + 128 * k + 16 * q), b2.y, vs2, vn2));
                     }
                 }
+            }
+            if constexpr (!kXor) {
+                // the stage was written through the generic proxy; order that
+                // before the producer's next bulk copy into it
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
             }
             __syncwarp();
             if (lane == 0)
@@ -650,29 +749,39 @@ struct Plan {
     Layout lay;
 };
 
-bool plan_for(const CtxKvParams &p, Plan &pl)
+// xor modes (r = 16, 32, 64) are built for the pages' head dim 128; every
+// other layout takes the shared-memory RoPE (ROT = 0).
+bool xor_mode(int head_dim, int rotary_dim)
+{
+    return head_dim == 128 && (rotary_dim == 16 || rotary_dim == 32 || rotary_dim == 64);
+}
+
+bool plan_for(const CtxKvParams &p, int head_dim, Plan &pl)
 {
     const int L = p.num_layers, H = p.num_kv_heads;
-    const int row_bytes = H * 512;
+    if (head_dim != 64 && head_dim != 128 && head_dim != 256)
+        return false;
+    const int row_bytes = H * 4 * head_dim;
     if (row_bytes > kMaxSlabBytes || L > kMaxTmaLayers)
         return false;
     pl.Lp = std::min(L, kMaxSlabBytes / row_bytes);
     pl.NP = (L + pl.Lp - 1) / pl.Lp;
     const int pl_tab = p.layer_slots ? pl.Lp : 0;
+    const bool xr = xor_mode(head_dim, p.rotary_dim);
     // Three stages measured best on the bf16 long-context workload and as good
     // as four on the fp8 prefill one (a deeper ring of reads in flight slowed
     // the write-heavy bf16 workload); fewer when three would not leave room
     // for two CTAs per SM.
-    const Layout one = make_layout(L, 1, (uint32_t)pl.Lp * row_bytes, pl_tab);
+    const Layout one = make_layout(L, 1, (uint32_t)pl.Lp * row_bytes, pl_tab, head_dim, xr);
     const int fixed = (int)one.stages;
     int S = (kStageBudget - fixed) / (int)one.stage_bytes;
     S = S < 2 ? 2 : (S > kStages ? kStages : S);
     pl.S = S;
-    pl.lay = make_layout(L, S, (uint32_t)pl.Lp * row_bytes, pl_tab);
+    pl.lay = make_layout(L, S, (uint32_t)pl.Lp * row_bytes, pl_tab, head_dim, xr);
     return pl.lay.total <= 113 * 1024;
 }
 
-template <int ROT, bool FP8, bool PL>
+template <int D, int ROT, bool FP8, bool PL>
 cudaError_t launch_tma_variant(const TmaParams &tp, uint32_t smem_bytes, cudaStream_t stream)
 {
     static std::mutex mu;
@@ -693,7 +802,7 @@ cudaError_t launch_tma_variant(const TmaParams &tp, uint32_t smem_bytes, cudaStr
                 return e;
         }
         if (smem_set[dev] < smem_bytes) {
-            e = cudaFuncSetAttribute(ctx_kv_tma_kernel<ROT, FP8, PL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+            e = cudaFuncSetAttribute(ctx_kv_tma_kernel<D, ROT, FP8, PL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      (int)smem_bytes);
             if (e != cudaSuccess)
                 return e;
@@ -704,40 +813,51 @@ cudaError_t launch_tma_variant(const TmaParams &tp, uint32_t smem_bytes, cudaStr
     const long long units = tp.p.num_ctx * (long long)tp.pieces;
     const long long want = 2LL * sms;
     const int blocks = (int)(units < want ? units : want);
-    ctx_kv_tma_kernel<ROT, FP8, PL><<<blocks, kThreads, smem_bytes, stream>>>(tp);
+    ctx_kv_tma_kernel<D, ROT, FP8, PL><<<blocks, kThreads, smem_bytes, stream>>>(tp);
     return cudaGetLastError();
 }
 
-template <bool PL>
-cudaError_t launch_rot(const TmaParams &tp, int rotary_dim, bool fp8, uint32_t smem, cudaStream_t stream)
+template <int D, int ROT, bool PL>
+cudaError_t launch_dtype(const TmaParams &tp, bool fp8, uint32_t smem, cudaStream_t stream)
 {
-    switch (rotary_dim) {
-    case 16:
-        return fp8 ? launch_tma_variant<16, true, PL>(tp, smem, stream)
-                   : launch_tma_variant<16, false, PL>(tp, smem, stream);
-    case 32:
-        return fp8 ? launch_tma_variant<32, true, PL>(tp, smem, stream)
-                   : launch_tma_variant<32, false, PL>(tp, smem, stream);
-    case 64:
-        return fp8 ? launch_tma_variant<64, true, PL>(tp, smem, stream)
-                   : launch_tma_variant<64, false, PL>(tp, smem, stream);
-    default:
+    return fp8 ? launch_tma_variant<D, ROT, true, PL>(tp, smem, stream)
+               : launch_tma_variant<D, ROT, false, PL>(tp, smem, stream);
+}
+
+template <bool PL>
+cudaError_t launch_layout(const TmaParams &tp, int head_dim, int rotary_dim, bool fp8, uint32_t smem,
+                          cudaStream_t stream)
+{
+    if (head_dim == 64)
+        return launch_dtype<64, 0, PL>(tp, fp8, smem, stream);
+    if (head_dim == 256)
+        return launch_dtype<256, 0, PL>(tp, fp8, smem, stream);
+    if (head_dim != 128)
         return cudaErrorInvalidValue;
+    switch (xor_mode(head_dim, rotary_dim) ? rotary_dim : 0) {
+    case 16:
+        return launch_dtype<128, 16, PL>(tp, fp8, smem, stream);
+    case 32:
+        return launch_dtype<128, 32, PL>(tp, fp8, smem, stream);
+    case 64:
+        return launch_dtype<128, 64, PL>(tp, fp8, smem, stream);
+    default:
+        return launch_dtype<128, 0, PL>(tp, fp8, smem, stream);
     }
 }
 
 }  // namespace
 
-bool tma_path_supported(const CtxKvParams &p)
+bool tma_path_supported(const CtxKvParams &p, int head_dim)
 {
     Plan pl;
-    return plan_for(p, pl);
+    return plan_for(p, head_dim, pl);
 }
 
-cudaError_t launch_ctx_kv_write_tma(const CtxKvParams &p, int rotary_dim, bool fp8, cudaStream_t stream)
+cudaError_t launch_ctx_kv_write_tma(const CtxKvParams &p, int head_dim, bool fp8, cudaStream_t stream)
 {
     Plan pl;
-    if (!plan_for(p, pl))
+    if (!plan_for(p, head_dim, pl))
         return cudaErrorInvalidValue;
     TmaParams tp;
     tp.p = p;
@@ -748,8 +868,8 @@ cudaError_t launch_ctx_kv_write_tma(const CtxKvParams &p, int rotary_dim, bool f
     tp.contiguous = 0;
     const uint32_t smem = pl.lay.total;
     if (p.layer_slots)
-        return launch_rot<true>(tp, rotary_dim, fp8, smem, stream);
-    return launch_rot<false>(tp, rotary_dim, fp8, smem, stream);
+        return launch_layout<true>(tp, head_dim, p.rotary_dim, fp8, smem, stream);
+    return launch_layout<false>(tp, head_dim, p.rotary_dim, fp8, smem, stream);
 }
 
 }  // namespace dspark

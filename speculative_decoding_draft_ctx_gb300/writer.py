@@ -12,16 +12,22 @@ pointer tables and the write all run in the C library.
 from __future__ import annotations
 
 from ._binding import (
-    HEAD_DIM, DSparkError, Tables, cache_desc, dspark_ctx_kv_rotary_dims_supported,
-    dspark_ctx_kv_project, dspark_ctx_kv_project_write, dspark_ctx_kv_validate_layers, dspark_ctx_kv_write,
-    dspark_ctx_kv_write_ex, dspark_ctx_kv_write_layer_slots, dspark_gemma_rms_norm, dspark_qknorm_rope_kv_insert,
-    kv_dtype_code,
+    HEAD_DIM, DSparkError, Tables, cache_desc, dspark_ctx_kv_general_supported, dspark_ctx_kv_rotary_dims_supported,
+    dspark_ctx_kv_project, dspark_ctx_kv_project_write, dspark_ctx_kv_validate_layers,
+    dspark_ctx_kv_validate_layers_general, dspark_ctx_kv_write, dspark_ctx_kv_write_ex, dspark_ctx_kv_write_general,
+    dspark_ctx_kv_write_layer_slots, dspark_gemma_rms_norm, dspark_qknorm_rope_kv_insert, kv_dtype_code,
 )
 
 
 def rotary_dims_supported(rotary_dim: int, head_dim: int) -> bool:
     """The kernel rotates the leading 16, 32 or 64 dims of a 128-dim head."""
     return dspark_ctx_kv_rotary_dims_supported(rotary_dim, head_dim)
+
+
+def general_layout_supported(head_dim: int, rotary_dim: int, block_size: int) -> bool:
+    """The general write's rule: head_dim 64, 128 or 256, rotary_dim even in
+    [2, head_dim], any block size >= 1."""
+    return dspark_ctx_kv_general_supported(head_dim, rotary_dim, block_size)
 
 
 class ContextKVWriter:
@@ -31,17 +37,24 @@ class ContextKVWriter:
     or uint8 (``"fp8"``); ``k_scales[l]``, ``v_scales[l]``: fp32 CUDA tensors.
     The offset tables are rebuilt only when a cache or scale moves, and never
     while the current stream is capturing a CUDA graph.
+
+    ``general=True`` also takes the layouts the pages' writer refuses: caches
+    ``[num_blocks, nkv, block_size, 2 * head_dim]`` with head_dim 64, 128 or
+    256, any block size, and any even rotary_dim up to the head dim (the
+    general write; the pages' layouts still run on their own kernels).
     """
 
-    def __init__(self, kv_caches, k_scales, v_scales, kv_cache_dtype="auto"):
+    def __init__(self, kv_caches, k_scales, v_scales, kv_cache_dtype="auto", general=False):
         self.kv_caches = list(kv_caches)
         self.k_scales = list(k_scales)
         self.v_scales = list(v_scales)
         self.kv_cache_dtype = kv_cache_dtype
-        dspark_ctx_kv_validate_layers(self._descs())
+        self.general = bool(general)
+        (dspark_ctx_kv_validate_layers_general if self.general else dspark_ctx_kv_validate_layers)(self._descs())
         c0 = self.kv_caches[0]
         self.num_layers = len(self.kv_caches)
         self.num_blocks, self.num_kv_heads, self.block_size = (int(s) for s in c0.shape[:3])
+        self.head_dim = int(c0.shape[3]) // 2
         self._dtype = kv_dtype_code(kv_cache_dtype)
         self._tables = Tables(self.num_layers)
 
@@ -50,10 +63,10 @@ class ContextKVWriter:
                 for c, k, v in zip(self.kv_caches, self.k_scales, self.v_scales)]
 
     @staticmethod
-    def supported(kv_caches, k_scales, v_scales, kv_cache_dtype="auto") -> bool:
+    def supported(kv_caches, k_scales, v_scales, kv_cache_dtype="auto", general=False) -> bool:
+        check = dspark_ctx_kv_validate_layers_general if general else dspark_ctx_kv_validate_layers
         try:
-            dspark_ctx_kv_validate_layers([cache_desc(c, kv_cache_dtype, k, v)
-                                           for c, k, v in zip(kv_caches, k_scales, v_scales)])
+            check([cache_desc(c, kv_cache_dtype, k, v) for c, k, v in zip(kv_caches, k_scales, v_scales)])
         except DSparkError:
             return False
         return len(kv_caches) > 0
@@ -72,7 +85,7 @@ class ContextKVWriter:
         the pages' _shared_slot_mapping; otherwise each layer's rows go to
         its own slots)."""
         num_ctx, L, two, nkv, hd = all_kv.shape
-        if L != self.num_layers or nkv != self.num_kv_heads or two != 2 or hd != HEAD_DIM:
+        if L != self.num_layers or nkv != self.num_kv_heads or two != 2 or hd != self.head_dim:
             raise DSparkError(1, f"all_kv shape {tuple(all_kv.shape)} does not match the layers")
         if num_ctx == 0:
             return
@@ -88,6 +101,15 @@ class ContextKVWriter:
         t = self._tables
         if per_layer is not None:
             t.update_slots(per_layer, stream)
+        if self.general:
+            dspark_ctx_kv_write_general(all_kv, k_norm_weight, positions,
+                                        slot_mapping if per_layer is None else None,
+                                        t.layer_slots if per_layer is not None else None, num_ctx, cos_sin_cache,
+                                        cos_sin_cache.shape[0], self.kv_caches[0], self.num_blocks, t.cache_offsets,
+                                        t.k_scales, t.v_scales, L, nkv, self.head_dim, self.block_size, rotary_dim,
+                                        eps, self._dtype, error_flags, stream)
+            return
+        if per_layer is not None:
             dspark_ctx_kv_write_layer_slots(all_kv, k_norm_weight, positions, t.layer_slots, num_ctx,
                                             cos_sin_cache, cos_sin_cache.shape[0], self.kv_caches[0],
                                             self.num_blocks, t.cache_offsets, t.k_scales, t.v_scales, L, nkv,

@@ -37,19 +37,21 @@ def _alt_ok(g_val, fp8, alts):
 
 
 def compare_rows(gpu: np.ndarray, ora: np.ndarray, alt_index: dict, fp8: bool) -> list:
-    """gpu, ora: [n, 256] stored elements; alt_index: {(row, dim): [values]}.
-    Returns a list of (row, dim, gpu, oracle) mismatches (empty = parity)."""
+    """gpu, ora: [n, 2D] stored elements (K in [0, D), V in [D, 2D); D = 128
+    on the pages); alt_index: {(row, dim): [values]}.  Returns a list of
+    (row, dim, gpu, oracle) mismatches (empty = parity)."""
     assert gpu.shape == ora.shape and gpu.dtype == ora.dtype
+    D = gpu.shape[1] // 2
     bad = []
     d = np.abs(ordered(gpu, fp8) - ordered(ora, fp8))
     if fp8:
         viol = d > FP8_CODES
     else:
         viol = np.zeros_like(d, dtype=bool)
-        viol[:, :128] = d[:, :128] > BF16_K_ULPS
-        viol[:, 128:] = d[:, 128:] != 0
+        viol[:, :D] = d[:, :D] > BF16_K_ULPS
+        viol[:, D:] = d[:, D:] != 0
     for r, c in np.argwhere(viol):
-        if c < 128 and _alt_ok(gpu[r, c], fp8, alt_index.get((int(r), int(c)), ())):
+        if c < D and _alt_ok(gpu[r, c], fp8, alt_index.get((int(r), int(c)), ())):
             continue
         bad.append((int(r), int(c), int(gpu[r, c]), int(ora[r, c])))
     return bad
@@ -69,8 +71,9 @@ def compare_caches(gpu_caches, ora_caches, alts, fp8: bool):
     al, ae, av = alts
     problems = []
     for l, (g, o) in enumerate(zip(gpu_caches, ora_caches)):
-        g = g.reshape(-1, 256)
-        o = o.reshape(-1, 256)
+        row = o.shape[-1]
+        g = g.reshape(-1, row)
+        o = o.reshape(-1, row)
         fill = 0xFF if fp8 else 0xFFFF
         unwritten = (o == fill).all(axis=1)
         if not np.array_equal(g[unwritten], o[unwritten]):
@@ -81,7 +84,7 @@ def compare_caches(gpu_caches, ora_caches, alts, fp8: bool):
         idx = {}
         pos_of = {int(r): i for i, r in enumerate(wr)}
         for e, v in zip(ae[sel].tolist(), av[sel].tolist()):
-            r, c = divmod(e, 256)
+            r, c = divmod(e, row)
             if r in pos_of:
                 idx.setdefault((pos_of[r], c), []).append(v)
         bad = compare_rows(g[wr], o[wr], idx, fp8)
@@ -102,8 +105,9 @@ def device_inputs(inp: wk.Inputs, device="cuda"):
     return d
 
 
-def gpu_write(inp: wk.Inputs, caches=None, error_flags=None, stream=None):
-    """Run the write on the GPU through the C ABI (ContextKVWriter) and return
+def gpu_write(inp: wk.Inputs, caches=None, error_flags=None, stream=None, general=None):
+    """Run the write on the GPU through the C ABI (ContextKVWriter; its
+    general mode when asked or when the layout is not the pages') and return
     the device caches."""
     import speculative_decoding_draft_ctx_gb300 as dk
 
@@ -111,8 +115,10 @@ def gpu_write(inp: wk.Inputs, caches=None, error_flags=None, stream=None):
     d = device_inputs(inp)
     if caches is None:
         caches = wk.make_caches(wl, device="cuda")
+    if general is None:
+        general = not wk.pages_layout(wl)
     w = dk.ContextKVWriter(caches, d.extra["k_scales"], d.extra["v_scales"],
-                           "fp8" if wl.kv_dtype == wk.KV_FP8 else "auto")
+                           "fp8" if wl.kv_dtype == wk.KV_FP8 else "auto", general=general)
     w(d.all_kv, d.knorm_w, d.eps, d.positions, d.cos_sin, wl.rotary_dim, d.slot_mapping,
       stream=stream, error_flags=error_flags)
     torch.cuda.synchronize()

@@ -248,3 +248,72 @@ def test_projection_argument_checks(L):
         dk.dspark_ctx_kv_project_write(FAKE, FAKE, 4, 4096, FAKE, FAKE, FAKE, FAKE, 64, FAKE, 4, FAKE, FAKE, FAKE,
                                        2, 1, 16, 48, 1e-6, 0, stream=0)
     assert ei.value.name == "DSPARK_ERR_UNSUPPORTED_ROTARY_DIM"
+
+
+# ------------------------------------------------------------ the general write
+# (layouts the writer page's _validate / rotary_dims_supported refuse)
+
+def gcall(expect_ok=False, **over):
+    a = dict(all_kv=FAKE, knorm_w=FAKE, positions=FAKE, slot_mapping=FAKE, layer_slot_mappings=None, num_ctx=4,
+             cos_sin=FAKE, max_pos=64, layer0_cache=FAKE, num_blocks=4, cache_offsets=FAKE, k_scales=FAKE,
+             v_scales=FAKE, L=2, nkv=2, head_dim=64, block_size=24, rotary_dim=18, eps=1e-6, kv_dtype=0)
+    a.update(over)
+    if expect_ok:
+        dk.dspark_ctx_kv_write_general(**a, stream=0)
+        return "DSPARK_OK"
+    with pytest.raises(dk.DSparkError) as ei:
+        dk.dspark_ctx_kv_write_general(**a, stream=0)
+    return ei.value.name
+
+
+def test_general_write_argument_checks(L):
+    for hd in (0, 32, 96, 192, 512):
+        assert gcall(head_dim=hd) == "DSPARK_ERR_INVALID_ARG"
+    for hd, r in ((64, 0), (64, 7), (64, 66), (128, 130), (256, 258), (256, -2)):
+        assert gcall(head_dim=hd, rotary_dim=r) == "DSPARK_ERR_UNSUPPORTED_ROTARY_DIM"
+    for bs in (0, -3):
+        assert gcall(block_size=bs) == "DSPARK_ERR_BLOCK_SIZE"
+    # exactly one slot source
+    assert gcall(layer_slot_mappings=FAKE) == "DSPARK_ERR_INVALID_ARG"
+    assert gcall(slot_mapping=None) == "DSPARK_ERR_INVALID_ARG"
+    assert gcall(slot_mapping=None, layer_slot_mappings=FAKE + 4) == "DSPARK_ERR_ALIGNMENT"
+    assert gcall(kv_dtype=3) == "DSPARK_ERR_DTYPE"
+    assert gcall(eps=float("nan")) == "DSPARK_ERR_INVALID_ARG"
+    assert gcall(num_blocks=1 << 58) == "DSPARK_ERR_INVALID_ARG"
+    for over in (dict(all_kv=FAKE + 8), dict(knorm_w=FAKE + 8), dict(cos_sin=FAKE + 4),
+                 dict(layer0_cache=FAKE + 8), dict(cache_offsets=FAKE + 4), dict(error_flags=FAKE + 2)):
+        assert gcall(**over) == "DSPARK_ERR_ALIGNMENT"
+    # the pages' layout through the general entry: the same buffer checks
+    assert gcall(head_dim=128, rotary_dim=32, block_size=16, all_kv=FAKE + 8) == "DSPARK_ERR_ALIGNMENT"
+    # no tokens: OK, no launch, no slot source needed
+    assert gcall(num_ctx=0, slot_mapping=None, expect_ok=True) == "DSPARK_OK"
+
+
+def test_general_supported_rule(L):
+    for hd in (64, 128, 256):
+        for r in range(2, hd + 1, 2):
+            assert dk.general_layout_supported(hd, r, 1)
+        assert not dk.general_layout_supported(hd, hd + 2, 16)
+        assert not dk.general_layout_supported(hd, 3, 16)
+        assert not dk.general_layout_supported(hd, 16, 0)
+    assert dk.general_layout_supported(128, 32, 48)
+    assert not dk.general_layout_supported(96, 32, 16)
+
+
+def test_general_layout_rules(L):
+    def general_status(descs):
+        try:
+            dk.dspark_ctx_kv_validate_layers_general(descs)
+            return "DSPARK_OK"
+        except dk.DSparkError as e:
+            return e.name
+
+    for last in (128, 256, 512):
+        assert general_status([desc(shape=(8, 2, 24, last))]) == "DSPARK_OK"
+    assert general_status([desc(shape=(8, 2, 24, 384))]) == "DSPARK_ERR_INVALID_ARG"
+    assert general_status([desc(shape=(8, 2, 1, 128))]) == "DSPARK_OK"
+    assert status_of([desc(shape=(8, 2, 24, 256))]) == "DSPARK_ERR_BLOCK_SIZE"  # the pages' rule
+    assert status_of([desc(shape=(8, 2, 16, 512))]) == "DSPARK_ERR_INVALID_ARG"
+    span = 8 * 2 * 24 * 512 * 2
+    assert general_status([desc(shape=(8, 2, 24, 512)), desc(data=FAKE + span + 16, shape=(8, 2, 24, 512))]) == \
+        "DSPARK_ERR_ALIGNMENT"

@@ -159,6 +159,7 @@ __host__ __device__ constexpr int min_blocks()
 template <int D, bool FP8>
 __global__ void __launch_bounds__(kThreads, min_blocks<D>()) ctx_kv_general_kernel(const CtxKvParams p)
 {
+    pdl_enter();
     constexpr int E = D / 16;  // bf16 per lane
     constexpr int W = E / 2;   // 32-bit words per lane
     constexpr int HPU = heads_per_unit<D>();
@@ -354,8 +355,7 @@ cudaError_t launch_variant(const CtxKvParams &p, cudaStream_t stream)
     const int64_t units = q.num_ctx * (int64_t)q.num_layers * q.head_chunks;
     const int64_t need = (units + kWarps - 1) / kWarps;
     const int blocks = (int)(need < max_blocks ? need : max_blocks);
-    ctx_kv_general_kernel<D, FP8><<<blocks, kThreads, 0, stream>>>(q);
-    return cudaGetLastError();
+    return launch_pdl(ctx_kv_general_kernel<D, FP8>, blocks, kThreads, 0, stream, q);
 }
 
 }  // namespace

@@ -7,7 +7,51 @@
 
 #include <cuda_runtime_api.h>
 
+#ifdef __CUDACC__
+#include <cstdlib>
+#include <cstring>
+#include <utility>
+
+#include <cuda_runtime.h>
+#endif
+
 namespace dspark {
+
+#ifdef __CUDACC__
+// Launches `kernel` with programmatic stream serialization allowed, so that
+// it may start while the previous kernel of the stream drains (the kernel
+// itself executes griddepcontrol.wait before touching global memory).
+// DSPARK_PDL=0 launches it the plain way.
+template <typename... Params, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(Params...), int blocks, int threads, size_t smem, cudaStream_t stream,
+                       Args &&...args)
+{
+    const char *env = std::getenv("DSPARK_PDL");
+    const bool pdl = !(env && std::strcmp(env, "0") == 0);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)blocks);
+    cfg.blockDim = dim3((unsigned)threads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = pdl ? attr : nullptr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
+// The kernel side of launch_pdl, before any global memory access: wait for
+// the stream's previous kernel to finish and its writes to be visible, then
+// let the next kernel be scheduled as this grid's CTAs exit (it is scheduled
+// only once every CTA of this grid has issued this or exited, so it never
+// takes a slot one of ours still waits for).
+__device__ __forceinline__ void pdl_enter()
+{
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+#endif
 
 constexpr int kHeadDim = 128;
 constexpr int kRowElems = 256;

@@ -111,6 +111,7 @@ __device__ __forceinline__ float load_scale(const float *const *table, int l)
 template <int ROT, bool FP8>
 __global__ void __launch_bounds__(kThreads) ctx_kv_write_kernel(const CtxKvParams p)
 {
+    pdl_enter();
     constexpr int kRotLanes = ROT / 8;  // K lanes holding rotary dims
     constexpr int kPartner = ROT / 16;  // lane distance of a rotated pair
     const int lane = threadIdx.x & 31;
@@ -267,8 +268,7 @@ cudaError_t launch_variant(const CtxKvParams &p, cudaStream_t stream)
     const int64_t warps_per_block = kThreads / 32;
     const int64_t need = (units + warps_per_block - 1) / warps_per_block;
     const int blocks = (int)(need < max_blocks ? need : max_blocks);
-    ctx_kv_write_kernel<ROT, FP8><<<blocks, kThreads, 0, stream>>>(p);
-    return cudaGetLastError();
+    return launch_pdl(ctx_kv_write_kernel<ROT, FP8>, blocks, kThreads, 0, stream, p);
 }
 
 }  // namespace

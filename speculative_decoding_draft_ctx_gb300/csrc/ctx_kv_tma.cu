@@ -314,6 +314,7 @@ __global__ void __launch_bounds__(kThreads, 2) ctx_kv_tma_kernel(const TmaParams
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     __syncthreads();
+    pdl_enter();  // launched with launch_pdl: the barriers above need no global memory
 
     const long long units = p.num_ctx * (long long)NP;
     const long long G = gridDim.x;
@@ -813,8 +814,7 @@ cudaError_t launch_tma_variant(const TmaParams &tp, uint32_t smem_bytes, cudaStr
     const long long units = tp.p.num_ctx * (long long)tp.pieces;
     const long long want = 2LL * sms;
     const int blocks = (int)(units < want ? units : want);
-    ctx_kv_tma_kernel<D, ROT, FP8, PL><<<blocks, kThreads, smem_bytes, stream>>>(tp);
-    return cudaGetLastError();
+    return launch_pdl(ctx_kv_tma_kernel<D, ROT, FP8, PL>, blocks, kThreads, smem_bytes, stream, tp);
 }
 
 template <int D, int ROT, bool PL>

@@ -77,6 +77,7 @@ template <int kChunks>
 __global__ void __launch_bounds__(kThreadsN, kChunks <= 4 ? 4 : (kChunks <= 8 ? 3 : 2))
     gemma_norm_kernel(const uint16_t *x, const uint16_t *w, uint16_t *out, int64_t rows, int hidden, float eps)
 {
+    pdl_enter();
     const int lane = threadIdx.x & 31;
     const int chunks = hidden >> 3;
     const float inv_n = 1.0f / (float)hidden;
@@ -129,6 +130,7 @@ __global__ void __launch_bounds__(kThreadsN) gemma_norm_split_kernel(const uint1
                                                                      uint16_t *out, int64_t rows, int hidden,
                                                                      float eps)
 {
+    pdl_enter();
     constexpr int kRowsPerCta = kWarpsN / 4, kChunksS = 4;  // 128 threads x 4 chunks = 4096 elements
     __shared__ float part[kWarpsN];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -190,6 +192,7 @@ __global__ void __launch_bounds__(kThreadsN, 4)
     gemma_norm_two_pass_kernel(const uint16_t *x, const uint16_t *w, uint16_t *out, int64_t rows, int hidden,
                                float eps)
 {
+    pdl_enter();
     const int lane = threadIdx.x & 31;
     const int chunks = hidden >> 3;
     const float inv_n = 1.0f / (float)hidden;
@@ -269,12 +272,11 @@ cudaError_t launch_norm_variant(const uint16_t *x, const uint16_t *w, uint16_t *
     const int64_t need = (rows + rows_per_cta - 1) / rows_per_cta;
     const int blocks = (int)(need < max_blocks ? need : max_blocks);
     if constexpr (kChunks > 0)
-        gemma_norm_kernel<kChunks><<<blocks, kThreadsN, 0, stream>>>(x, w, out, rows, hidden, eps);
+        return launch_pdl(gemma_norm_kernel<kChunks>, blocks, kThreadsN, 0, stream, x, w, out, rows, hidden, eps);
     else if constexpr (kChunks == 0)
-        gemma_norm_two_pass_kernel<<<blocks, kThreadsN, 0, stream>>>(x, w, out, rows, hidden, eps);
+        return launch_pdl(gemma_norm_two_pass_kernel, blocks, kThreadsN, 0, stream, x, w, out, rows, hidden, eps);
     else
-        gemma_norm_split_kernel<<<blocks, kThreadsN, 0, stream>>>(x, w, out, rows, hidden, eps);
-    return cudaGetLastError();
+        return launch_pdl(gemma_norm_split_kernel, blocks, kThreadsN, 0, stream, x, w, out, rows, hidden, eps);
 }
 
 }  // namespace

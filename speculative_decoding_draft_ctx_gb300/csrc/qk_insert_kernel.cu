@@ -80,6 +80,7 @@ __device__ __forceinline__ int w1_slot(int norm, int jj, int c) { return norm * 
 template <int ROT, bool FP8>
 __global__ void __launch_bounds__(kThreads, 3) qk_insert_kernel(const QkInsertParams p)
 {
+    pdl_enter();
     constexpr int kPartner = ROT / 16;  // lane distance of a rotated pair
     constexpr int kRotLanes = ROT / 8;  // lanes whose first word holds rotary dims
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -273,8 +274,7 @@ cudaError_t launch_variant(const QkInsertParams &p, cudaStream_t stream)
         max_blocks = cached_blocks[dev];
     }
     const int blocks = (int)(p.num_tokens < max_blocks ? p.num_tokens : max_blocks);
-    qk_insert_kernel<ROT, FP8><<<blocks, kThreads, 0, stream>>>(p);
-    return cudaGetLastError();
+    return launch_pdl(qk_insert_kernel<ROT, FP8>, blocks, kThreads, 0, stream, p);
 }
 
 }  // namespace

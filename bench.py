@@ -228,17 +228,20 @@ def l2_bytes() -> int:
 
 
 def copy_same_bytes(step_bytes: int, dev, stream, launches: int = 50) -> float:
-    """GB/s of PyTorch's own copy when one launch moves the same number of
-    bytes as one write step (half read, half written), replayed from one CUDA
-    graph (no host gaps, even for a few-MB copy) on rotated buffers that
-    together exceed L2: the streaming rate a single launch of this size
-    reaches on this GPU, for context beside the long-copy peak."""
+    """GB/s of a plain PyTorch elementwise copy kernel (dst = src * 1 in
+    bf16, exact) when one launch moves the same number of bytes as one write
+    step (half read, half written), replayed from one CUDA graph (no host
+    gaps, even for a few-MB copy) on rotated buffers that together exceed L2:
+    the streaming rate a single SM-kernel launch of this size reaches on this
+    GPU, for context beside the long-copy peak.  (A Tensor.copy_ of
+    contiguous same-dtype buffers is a memcpy, which a graph runs on a copy
+    engine at about half the rate, so it is not used here.)"""
     half = max(16, (step_bytes // 2) // 16 * 16)
     n_sets = max(1, math.ceil(3 * l2_bytes() / (2 * half)))
     bufs = [(torch.empty(half // 2, dtype=torch.bfloat16, device=dev).fill_(1.0),
              torch.empty(half // 2, dtype=torch.bfloat16, device=dev)) for _ in range(n_sets)]
     for i in range(5):
-        bufs[i % n_sets][1].copy_(bufs[i % n_sets][0])
+        torch.mul(bufs[i % n_sets][0], 1, out=bufs[i % n_sets][1])
     torch.cuda.synchronize()
     side = torch.cuda.Stream()
     side.wait_stream(stream)
@@ -246,7 +249,7 @@ def copy_same_bytes(step_bytes: int, dev, stream, launches: int = 50) -> float:
     with torch.cuda.graph(graph, stream=side):
         for i in range(launches):
             src, dst = bufs[i % n_sets]
-            dst.copy_(src)
+            torch.mul(src, 1, out=dst)
     stream.wait_stream(side)
     graph.replay()
     torch.cuda.synchronize()

@@ -135,7 +135,7 @@ def measured_peaks(key: str = "hbm_gbs"):
             d = json.load(f)
         return float(d[key]), "measured"
     except (OSError, KeyError, ValueError):
-        return {"hbm_gbs": FALLBACK_HBM_GBS, "bf16_tflops": 1900.0}[key], "fallback"
+        return {"hbm_gbs": FALLBACK_HBM_GBS, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}[key], "fallback"
 
 
 def kernel_sha() -> str:
@@ -789,7 +789,13 @@ def run_proj(args):
     _, cublas_ms = timed(cublas_only, side_steps)
     _, unfused_ms = timed(unfused, side_steps)
     value = whole_job_rate(flops, args.steps, ws, total_ms) / 1e12
-    peak, peak_kind = measured_peaks("bf16_tflops")
+    # the timed loop is one launch after another: while the sampled clocks
+    # show the power cap, the sustained cuBLAS figure is the fair peak, else
+    # the burst one
+    clocks = clk.summary()
+    capped = "sw_power_cap" in (clocks or {}).get("reasons", [])
+    peak, peak_kind = measured_peaks("bf16_tflops_sustained" if capped else "bf16_tflops")
+    peak_kind += " sustained (power cap seen)" if capped else " burst"
     achieved = flops / (fused_ms * 1e-3) / 1e12
 
     e2e = None
@@ -845,7 +851,7 @@ def run_proj(args):
             "compare_ms_per_step": {"fused_projection_write": fused_ms, "projection_alone": proj_ms,
                                     "cublas_matmul_alone": cublas_ms,
                                     "unfused_cublas_matmul_then_write": unfused_ms},
-            "cpu_baseline": cpu, "e2e": e2e, "clocks": clk.summary(), "gpu_launches": args.steps,
+            "cpu_baseline": cpu, "e2e": e2e, "clocks": clocks, "gpu_launches": args.steps,
             "kernel_avg_us": fused_ms * 1e3,
         }
         print(json.dumps(line), flush=True)

@@ -27,10 +27,11 @@
 // 128-byte (64-byte) segments.  Sum of squares: paired FMAs + 3 xor shuffles
 // within the row's 8 lanes.  RoPE with r = 16, 32 or 64: the partner of dim
 // d is d +- r/2, r/16 lanes away within the row's 8 lanes (one xor shuffle).
-// Any other even r: the normed row is written back over its K row in the
-// stage, and after a __syncwarp each rotated dim reads its partner there; the
-// token's cos|sin row is staged per warp from global memory (a row of 2r
-// bytes need not be a multiple of the 16 a bulk copy moves).  fp8: the
+// Any other even r: the normed row goes to a per-warp shared scratch (rows
+// padded by 4 bytes, so the warp's partner reads hit 32 different banks), and
+// after a __syncwarp each rotated dim reads its partner there; the token's
+// cos|sin row is staged per warp from global memory (a row of 2r bytes need
+// not be a multiple of the 16 a bulk copy moves).  fp8: the
 // quotient x / scale is formed from the correctly rounded reciprocal of the
 // scale with one FMA correction step (Markstein's method: q0 = x*(1/s),
 // e = x - q0*s exactly, q = q0 + e*(1/s)), which yields the correctly rounded
@@ -250,8 +251,11 @@ __host__ __device__ inline Layout make_layout(int L, int S, uint32_t slab_bytes,
     o = y.pls + 2 * 32 * 8 * pl;
     y.pdst = align_up(o, 16);
     o = y.pdst + 8 * S * pl;
+    // per consumer warp (rotary dims other than 16/32/64): the token's cos|sin
+    // row (2D bytes) and its 4 rows' normed K, each padded by 4 bytes so the
+    // warp's partner reads spread over all 32 banks
     y.csw = align_up(o, 16);
-    o = y.csw + (xor_rot ? 0 : kConsumerWarps * 2 * D);
+    o = y.csw + (xor_rot ? 0 : kConsumerWarps * (10 * D + 64));
     y.stages = align_up(o, 128);
     y.slab_bytes = slab_bytes;
     y.stage_bytes = align_up(slab_bytes + (xor_rot ? kCsBytes : 0), 128);
@@ -572,7 +576,11 @@ __global__ void __launch_bounds__(kThreads, 2) ctx_kv_tma_kernel(const TmaParams
         constexpr int kRotLanes = ROT / 8;
         const bool rot_lane = kXor && q < kRotLanes;
         const int rdim = kXor ? ROT : p.rotary_dim, half = rdim >> 1;
-        uint16_t *csw = reinterpret_cast<uint16_t *>(smem + lay.csw) + warp * D;  // this warp's cos|sin slot
+        uint16_t *csw = reinterpret_cast<uint16_t *>(smem + lay.csw + warp * (10 * D + 64));  // cos|sin row
+        // this lane's row of the warp's normed-K scratch: rows D + 2 elements
+        // apart, so lane (q, rr)'s 2-byte element 8q + e falls in bank
+        // 4q + rr + e/2 and the warp's 32 lanes hit 32 different banks
+        uint16_t *yrow = csw + D + rr * (D + 2);
         // bytes between the rows of consecutive heads in a cache
         const long long head_bytes = (long long)kCacheRow * p.block_size;
         int gmod = 0;  // row groups seen so far, over all stages, modulo the consumer warps
@@ -589,7 +597,7 @@ __global__ void __launch_bounds__(kThreads, 2) ctx_kv_tma_kernel(const TmaParams
             const int first = (warp - gmod) & (kConsumerWarps - 1);  // this warp's first group here
             gmod = (gmod + ngroups) & (kConsumerWarps - 1);
             if (first < ngroups) {
-                unsigned char *stage = stages + (size_t)s * lay.stage_bytes;
+                const unsigned char *stage = stages + (size_t)s * lay.stage_bytes;
                 // xor modes: cos and sign * sin (bf16 pairs) of this token for the lane's first 8 dims
                 uint32_t cw[4] = {0, 0, 0, 0}, sw[4] = {0, 0, 0, 0};
                 if constexpr (kXor) {
@@ -615,7 +623,7 @@ __global__ void __launch_bounds__(kThreads, 2) ctx_kv_tma_kernel(const TmaParams
                     const int lr = (int)(((uint64_t)(uint32_t)rc * tp.h_magic) >> 32);
                     const int h = rc - lr * H;
                     const int l = h_s.l0 + lr;
-                    unsigned char *krow = stage + ((size_t)(2 * lr) * H + h) * (2 * D);
+                    const unsigned char *krow = stage + ((size_t)(2 * lr) * H + h) * (2 * D);
                     const unsigned char *vrow = krow + (size_t)H * (2 * D);
                     uint64_t x2[4 * NC];
 #pragma unroll
@@ -663,14 +671,16 @@ __global__ void __launch_bounds__(kThreads, 2) ctx_kv_tma_kernel(const TmaParams
                         for (int j = 4; j < 4 * NC; j++)
                             ko[j] = y[j];
                     } else {
-                        // the normed row over its K row in the stage (the row's 8 lanes own it),
-                        // then each rotated dim d reads its partner d +- r/2 there
+                        // the normed row into the warp's scratch (the row's 8 lanes own it; the
+                        // previous group's partner reads are done first), then each rotated dim
+                        // d reads its partner d +- r/2 there
+                        __syncwarp();
 #pragma unroll
                         for (int k = 0; k < NC; k++)
-                            *reinterpret_cast<uint4 *>(krow + 128 * k + 16 * q) =
-                                make_uint4(y[4 * k], y[4 * k + 1], y[4 * k + 2], y[4 * k + 3]);
+#pragma unroll
+                            for (int w = 0; w < 4; w++)  // 4-byte stores: the rows are only 4-byte aligned
+                                reinterpret_cast<uint32_t *>(yrow + 64 * k + 8 * q)[w] = y[4 * k + w];
                         __syncwarp();
-                        const uint16_t *yrow = reinterpret_cast<const uint16_t *>(krow);
 #pragma unroll
                         for (int k = 0; k < NC; k++) {
                             const int d0 = 64 * k + 8 * q;
@@ -723,11 +733,6 @@ __global__ void __launch_bounds__(kThreads, 2) ctx_kv_tma_kernel(const TmaParams
                             st_stream_v2(dg + D + 64 * k + 8 * q, quantise8(lds128(vrow + 128 * k + 16 * q), b2.y, vs2, vn2));
                     }
                 }
-            }
-            if constexpr (!kXor) {
-                // the stage was written through the generic proxy; order that
-                // before the producer's next bulk copy into it
-                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
             }
             __syncwarp();
             if (lane == 0)

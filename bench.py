@@ -298,13 +298,22 @@ def calibrate_tokens(inp: wk.Inputs, seconds: float) -> int:
 
 
 def cpu_baseline(inp: wk.Inputs, seconds: float):
+    """The oracle on a bounded sample: one thread as it stands (the line's
+    value), and the same sample split over every host core by token ranges
+    (each thread the unchanged single-threaded write on its own tokens)."""
     n = calibrate_tokens(inp, seconds)
     s = OracleSample(inp, n)
     dt = s.run()
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else (os.cpu_count() or 1)
+    t0 = time.perf_counter()
+    s.p.write_threads(s.caches, cores)
+    dt_all = time.perf_counter() - t0
     return {
         "value": s.bytes / dt / 1e9, "unit": UNIT, "cores": 1, "kind": "oracle",
         "rows_per_s": s.rows / dt, "seconds": dt,
         "sample": f"first {n} of {inp.workload.num_ctx} tokens ({s.rows} valid rows), one thread, plain C oracle",
+        "all_cores": {"value": s.bytes / dt_all / 1e9, "unit": UNIT, "cores": cores, "seconds": dt_all,
+                      "sample": "the same tokens split over every host core by token ranges"},
     }
 
 

@@ -54,7 +54,7 @@ def build(force: bool = False) -> str:
         if force or stale:
             tmp = _LIB_PATH + f".tmp{os.getpid()}"
             cmd = ["gcc", "-std=c11", "-O2", "-ffp-contract=off", "-fno-fast-math",
-                   "-Wall", "-shared", "-fPIC", "-o", tmp, _SRC, _SRC_QK, "-lm"]
+                   "-Wall", "-shared", "-fPIC", "-pthread", "-o", tmp, _SRC, _SRC_QK, "-lm"]
             subprocess.run(cmd, check=True)
             os.replace(tmp, _LIB_PATH)
     return _LIB_PATH
@@ -103,6 +103,8 @@ def lib():
         L.dspark_oracle_write.argtypes = [P, P, ctypes.c_int64, ctypes.c_int64, P, P, P,
                                           ctypes.c_int64, P]
         L.dspark_oracle_write.restype = ctypes.c_int
+        L.dspark_oracle_write_threads.argtypes = [P, P, ctypes.c_int64, ctypes.c_int64, ctypes.c_int32]
+        L.dspark_oracle_write_threads.restype = ctypes.c_int
         L.dspark_oracle_rows.argtypes = [P, P, ctypes.c_int64, P, P, P, P, ctypes.c_int64, P]
         L.dspark_oracle_rows.restype = ctypes.c_int
         L.dspark_oracle_gemma_norm_rows.argtypes = [P, P, ctypes.c_int64, ctypes.c_int64, ctypes.c_float, P, P]
@@ -291,6 +293,15 @@ class Problem:
         _check(rc)
         k = n.value
         return al[:k].copy(), ae[:k].copy(), av[:k].copy()
+
+    def write_threads(self, caches, nthreads: int, t_begin: int = 0, t_end: int | None = None):
+        """The same write split over ``nthreads`` host threads by token
+        ranges (timing on every core); the alternates are not returned."""
+        t_end = self.T if t_end is None else t_end
+        for c in caches:
+            assert c.flags["C_CONTIGUOUS"] and c.dtype == self.elem_dtype
+        ptrs = (ctypes.c_void_p * self.L)(*[_ptr(c) for c in caches])
+        _check(lib().dspark_oracle_write_threads(ctypes.byref(self.c), ptrs, t_begin, t_end, int(nthreads)))
 
     def rows(self, row_ids):
         """Stored 2D-element rows for flat row ids ``(t*L + l)*H + h``, with

@@ -30,6 +30,7 @@
  * Slots < 0 are padding: nothing is read or written for them.
  */
 #include <math.h>
+#include <pthread.h>
 #include <stdint.h>
 #include <stdlib.h>
 #include <string.h>
@@ -465,6 +466,71 @@ int dspark_oracle_write(const dspark_oracle_inputs *in, void *const *caches,
     if (n_alt)
         *n_alt = total_alt;
     return total_alt > alt_cap ? ORACLE_ERR_ALT_CAP : ORACLE_OK;
+}
+
+/* The same write split over n host threads by token ranges (for timing
+ * the oracle on every host core): each thread runs dspark_oracle_write on
+ * its own range with its own alternate buffers, which it discards; valid
+ * slots are distinct, so the threads write disjoint cache rows.  Nothing of
+ * the arithmetic changes.  Returns the first failing thread's status. */
+typedef struct {
+    const dspark_oracle_inputs *in;
+    void *const *caches;
+    int64_t t_begin, t_end, cap;
+    int rc;
+} oracle_range;
+
+static void *oracle_range_run(void *arg)
+{
+    oracle_range *r = (oracle_range *)arg;
+    int32_t *al = (int32_t *)malloc((size_t)r->cap * sizeof(int32_t));
+    int64_t *ae = (int64_t *)malloc((size_t)r->cap * sizeof(int64_t));
+    uint16_t *av = (uint16_t *)malloc((size_t)r->cap * sizeof(uint16_t));
+    int64_t n = 0;
+    r->rc = (al && ae && av) ? dspark_oracle_write(r->in, r->caches, r->t_begin, r->t_end, al, ae, av, r->cap, &n)
+                             : ORACLE_ERR_NOMEM;
+    if (r->rc == ORACLE_ERR_ALT_CAP)
+        r->rc = ORACLE_OK; /* the caches are complete; only the discarded alternates overflowed */
+    free(al);
+    free(ae);
+    free(av);
+    return NULL;
+}
+
+int dspark_oracle_write_threads(const dspark_oracle_inputs *in, void *const *caches, int64_t t_begin,
+                                int64_t t_end, int32_t nthreads)
+{
+    if (nthreads < 1 || nthreads > 1024 || t_begin < 0 || t_begin > t_end)
+        return ORACLE_ERR_ARG;
+    oracle_range *r = (oracle_range *)calloc((size_t)nthreads, sizeof(oracle_range));
+    pthread_t *th = (pthread_t *)calloc((size_t)nthreads, sizeof(pthread_t));
+    if (!r || !th) {
+        free(r);
+        free(th);
+        return ORACLE_ERR_NOMEM;
+    }
+    const int64_t n = t_end - t_begin;
+    int started = 0, rc = ORACLE_OK;
+    for (int i = 0; i < nthreads; i++) {
+        r[i].in = in;
+        r[i].caches = caches;
+        r[i].t_begin = t_begin + n * i / nthreads;
+        r[i].t_end = t_begin + n * (i + 1) / nthreads;
+        r[i].cap = 1 << 16;
+        if (pthread_create(&th[i], NULL, oracle_range_run, &r[i]) != 0) {
+            rc = ORACLE_ERR_NOMEM;
+            break;
+        }
+        started++;
+    }
+    for (int i = 0; i < started; i++) {
+        pthread_join(th[i], NULL);
+        if (rc == ORACLE_OK && r[i].rc != ORACLE_OK)
+            rc = r[i].rc;
+    }
+    free(r);
+    free(th);
+    return rc;
 }
 
 /* Rows (t, l, h) given as flat indices (t * L + l) * H + h, whatever their

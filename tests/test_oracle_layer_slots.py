@@ -66,3 +66,17 @@ def test_duplicates_are_per_layer(oracle_lib):
     p = oracle_lib.problem_from_inputs(inp, layer_slots=ls2)
     with pytest.raises(oracle_lib.OracleError, match="duplicate"):
         p.write(p.new_caches())
+
+
+@pytest.mark.parametrize("nthreads", [1, 3, 7])
+def test_threaded_oracle_write_equals_the_single_threaded_one(oracle_lib, nthreads):
+    """The timing helper that splits the write over host threads by token
+    ranges writes the same caches byte for byte."""
+    inp = wk.generate(wk.WORKLOADS[2].with_(num_ctx=101, pad_count=5))
+    p = oracle_lib.problem_from_inputs(inp)
+    a = p.new_caches()
+    p.write(a)
+    b = p.new_caches()
+    p.write_threads(b, nthreads)
+    for x, y in zip(a, b):
+        assert np.array_equal(x, y)

@@ -572,6 +572,7 @@ def run_ours(args):
             "clocks": clocks,
             "gpu_launches": args.steps,
             "kernel_avg_us": avg_launch_ms * 1e3,
+            "kernel_median_us": statistics.median(launch_ms) * 1e3,
         }
         print(json.dumps(line), flush=True)
     if pg:

@@ -139,12 +139,18 @@ def measured_peaks(key: str = "hbm_gbs"):
 
 
 def kernel_sha() -> str:
-    """Hash of the kernel sources: recorded DRAM counters are only reported
-    while it matches the one they were taken on."""
+    """Hash of the kernel sources' code (comments and whitespace removed):
+    recorded DRAM counters are only reported while it matches the one they
+    were taken on."""
+    import re
+
     h = hashlib.sha256()
     for path in KERNEL_SRCS:
-        with open(path, "rb") as f:
-            h.update(f.read())
+        with open(path, encoding="utf-8") as f:
+            src = f.read()
+        src = re.sub(r"/\*.*?\*/", " ", src, flags=re.S)  # block comments
+        src = re.sub(r"//[^\n]*", " ", src)                 # line comments
+        h.update(" ".join(src.split()).encode())
     return h.hexdigest()[:16]
 
 

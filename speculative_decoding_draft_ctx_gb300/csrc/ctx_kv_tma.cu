@@ -14,11 +14,16 @@
 // a ring of shared-memory stages: a producer warp reads the slot and position
 // of its next tokens, skips padding (nothing of a padded token is read), and
 // for each valid (token, layer piece) issues one bulk asynchronous copy
-// (cp.async.bulk, completing on an mbarrier) of the block plus one of the
-// token's cos|sin row.  Eight consumer warps wait on the stage's barrier,
-// compute from shared memory and store straight to the caches, then release
-// the stage.  Bytes in flight per SM are bounded by shared memory, not by
-// registers, so the HBM queue stays full with few warps.
+// (cp.async.bulk, completing on an mbarrier) of the block, plus one of the
+// token's cos|sin row when r is 16, 32 or 64.  Eight consumer warps wait on
+// the stage's barrier, compute from shared memory and store straight to the
+// caches, then release the stage.  Bytes in flight per SM are bounded by
+// shared memory, not by registers, so the HBM queue stays full with few
+// warps.  A slot's (block, offset) comes from a shift and a mask for a
+// power-of-two block size, else from a multiply-high by the host's
+// Granlund-Montgomery magic number.  The kernel is launched with
+// programmatic dependent launch (launch_pdl): it waits for the stream's
+// previous kernel before its first global access.
 //
 // Compute mapping.  A consumer warp handles 4 rows per instruction: 8 lanes
 // per row, each lane holding the D/64 chunks [64k + 8q, 64k + 8q + 8) of K

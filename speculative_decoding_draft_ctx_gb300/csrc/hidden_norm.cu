@@ -13,7 +13,7 @@
 // Sum of squares on mixed bf16 FMAs (fma.rn.f32.bf16 on the register halves,
 // four chains), a 5-step xor shuffle, the hardware reciprocal square root;
 // y = bf16((x * inv) * (1 + w)) in fp32 with (1 + w) read through L1
-// (every row uses the same weight).  Rows 1024 to 4096 wide are shared by
+// (every row uses the same weight).  Rows wider than 1024 (up to 4096) are shared by
 // four warps instead (finer work units: no ragged last wave of whole
 // rows).  A row is read before it is written, so
 // the output may be the input (in place).  Bound: HBM, 2 * hidden * 2 bytes
@@ -124,7 +124,7 @@ __global__ void __launch_bounds__(kThreadsN, kChunks <= 4 ? 4 : (kChunks <= 8 ? 
     }
 }
 
-// Four warps per row (rows 1024 to 4096 wide), so that the work is cut into
+// Four warps per row (rows wider than 1024, up to 4096), so that the work is cut into
 // units four times finer than whole rows; the four partial sums of squares
 // meet in shared memory.
 __global__ void __launch_bounds__(kThreadsN) gemma_norm_split_kernel(const uint16_t *x, const uint16_t *w,
@@ -286,7 +286,7 @@ cudaError_t launch_gemma_norm(const uint16_t *x, const uint16_t *w, uint16_t *ou
                               float eps, cudaStream_t stream)
 {
     const int per_lane = (hidden / 8 + 31) / 32;  // 16-byte chunks per lane
-    // rows 1024 to 4096 wide: each row over four warps (measured faster than
+    // rows wider than 1024 and at most 4096: each row over four warps (faster than
     // a warp per row at every row count: 512, 8192 and 65536 rows)
     static int sms = 0;
     if (sms == 0) {

@@ -45,7 +45,8 @@ namespace {
 
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
-constexpr int kBatch = 2;  // head groups per warp whose loads are issued together
+constexpr int kBatch = 3;  // head groups per warp whose loads are issued together (a 64 + 2 x 8 head
+                           // token: 20 groups, one round of loads for 8 warps)
 constexpr unsigned kFlagSlot = 0x1u;
 constexpr unsigned kFlagPos = 0x2u;
 

@@ -7,7 +7,7 @@
  * rounded to bf16), applies partial NeoX RoPE to the leading rotary_dim dims
  * of K at the token's position, and stores K|V into the layer's paged cache,
  * as raw bf16 or as OCP fp8 e4m3 of x / scale.  Tokens whose slot is < 0 are
- * padding and are neither read nor written.
+ * padding: nothing is written for them and their positions are not used.
  *
  * Defining passages: vLLM DSpark context-KV writer page (module docstring:
  * layouts, norm, RoPE, fp8 rule, padding, cache/scale offset tables;
@@ -96,6 +96,11 @@ typedef enum {
  *  eps           the norm's epsilon (finite, >= 0).
  *  kv_dtype      a dspark_kv_dtype.
  *  stream        the CUDA stream the kernel is enqueued on.
+ *
+ * This entry point has no error word, so it cannot report what the kernel
+ * flags: rows skipped as out of range, and a launch that gave up on one of
+ * its bounded internal waits (DSPARK_FLAG_TIMEOUT) and left rows unwritten,
+ * both pass silently.  dspark_ctx_kv_write_ex reports both.
  */
 int dspark_ctx_kv_write(const void *all_kv, const void *knorm_w, const int64_t *positions,
                         const int64_t *slot_mapping, int64_t num_ctx, const void *cos_sin,

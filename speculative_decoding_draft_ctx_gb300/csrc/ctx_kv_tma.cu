@@ -12,8 +12,10 @@
 // Data movement.  all_kv[t, l0 : l0 + Lp] -- every K and V row of Lp layers of
 // one token -- is one contiguous block of Lp * nkv * 4D bytes.  Each CTA runs
 // a ring of shared-memory stages: a producer warp reads the slot and position
-// of its next tokens, skips padding (nothing of a padded token is read), and
-// for each valid (token, layer piece) issues one bulk asynchronous copy
+// of its next tokens, skips padding (a padded token's K|V is not copied, save
+// among the CTA's first S units, which are copied before their slots are
+// known and dropped if padded), and for each valid (token, layer piece)
+// issues one bulk asynchronous copy
 // (cp.async.bulk, completing on an mbarrier) of the block, plus one of the
 // token's cos|sin row when r is 16, 32 or 64.  Eight consumer warps wait on
 // the stage's barrier, compute from shared memory and store straight to the
@@ -428,7 +430,8 @@ __global__ void __launch_bounds__(kThreads, 2) ctx_kv_tma_kernel(const TmaParams
         // The first S units of the CTA get their K|V block copied before
         // their slots are known (each takes a stage whatever its slot), which
         // hides the slot fetch behind the first copies; a padded one among
-        // them is then released unread.
+        // them has been read all the same and is dropped (its stage released
+        // with no rows).
         auto unit_span = [&](long long u, long long &t, int &l0, uint32_t &slab) {
             t = NP == 1 ? u : u / NP;
             l0 = (NP == 1 ? 0 : (int)(u - t * NP)) * Lp;
@@ -466,7 +469,7 @@ __global__ void __launch_bounds__(kThreads, 2) ctx_kv_tma_kernel(const TmaParams
                 const long long pos = __shfl_sync(0xffffffffu, cur_pos, i);
                 const bool spec = ordinal + i < nspec;
                 if (slot < 0 && !spec)
-                    continue;  // padding (or out of range): nothing read, nothing written
+                    continue;  // padding (or out of range): K|V not copied, nothing written
                 if (lane == 0) {
                     const int s = ps;
                     ok = spec || mbar_wait(empty + s, pph ^ 1u, abort);
@@ -477,7 +480,7 @@ __global__ void __launch_bounds__(kThreads, 2) ctx_kv_tma_kernel(const TmaParams
                         unit_span(u, t, l0, slab);
                         unsigned char *dst = stages + (size_t)s * lay.stage_bytes;
                         if (slot < 0) {
-                            hdr[s].rows = 0;  // a speculatively copied padded unit: release it unread
+                            hdr[s].rows = 0;  // a speculatively copied padded unit: dropped
                             mbar_arrive(full + s);
                         } else {
                             if (PL) {

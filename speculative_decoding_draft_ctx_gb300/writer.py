@@ -14,9 +14,57 @@ from __future__ import annotations
 from ._binding import (
     HEAD_DIM, DSparkError, Tables, cache_desc, dspark_ctx_kv_general_supported, dspark_ctx_kv_rotary_dims_supported,
     dspark_ctx_kv_project, dspark_ctx_kv_project_write, dspark_ctx_kv_validate_layers,
-    dspark_ctx_kv_validate_layers_general, dspark_ctx_kv_write, dspark_ctx_kv_write_ex, dspark_ctx_kv_write_general,
+    dspark_ctx_kv_validate_layers_general, dspark_ctx_kv_write_ex, dspark_ctx_kv_write_general,
     dspark_ctx_kv_write_layer_slots, dspark_gemma_rms_norm, dspark_qknorm_rope_kv_insert, kv_dtype_code,
 )
+
+
+def _need(cond, message: str):
+    if not cond:
+        raise DSparkError(1, message)
+
+
+def _check_tensor(name, x, dtype, device, shape=None, ndim=None):
+    """A tensor argument as the kernels read it: of ``dtype``, on ``device``,
+    contiguous (the library receives only its address), and of ``shape``
+    (``None`` in a shape entry: any extent) or ``ndim`` when given."""
+    import torch
+
+    _need(isinstance(x, torch.Tensor), f"{name} must be a tensor, got {type(x).__name__}")
+    _need(x.dtype == dtype, f"{name} must be {dtype}, got {x.dtype}")
+    _need(x.device == device, f"{name} is on {x.device}, expected {device}")
+    _need(x.is_contiguous(), f"{name} must be contiguous")
+    if ndim is not None:
+        _need(x.dim() == ndim, f"{name} must have {ndim} dims, got shape {tuple(x.shape)}")
+    if shape is not None:
+        _need(x.dim() == len(shape) and all(e is None or int(a) == e for a, e in zip(x.shape, shape)),
+              f"{name} must have shape {tuple('*' if e is None else e for e in shape)}, got {tuple(x.shape)}")
+
+
+def _check_index(name, x, device, count):
+    """positions / slot mappings: int64, contiguous, at least ``count``
+    entries (the kernels read entries 0 .. count - 1)."""
+    import torch
+
+    _check_tensor(name, x, torch.int64, device, ndim=1)
+    _need(x.numel() >= count, f"{name} has {x.numel()} entries, {count} tokens")
+
+
+def _check_cos_sin(x, rotary_dim, device):
+    import torch
+
+    _check_tensor("cos_sin_cache", x, torch.bfloat16, device, ndim=2)
+    _need(int(x.shape[1]) == int(rotary_dim),
+          f"cos_sin_cache rows hold {int(x.shape[1])} values, rotary_dim is {rotary_dim}")
+    _need(x.shape[0] > 0, "cos_sin_cache is empty")
+
+
+def _check_flags(error_flags, device):
+    import torch
+
+    if error_flags is not None:
+        _check_tensor("error_flags", error_flags, torch.int32, device)
+        _need(error_flags.numel() >= 1, "error_flags must hold one int32 word")
 
 
 def rotary_dims_supported(rotary_dim: int, head_dim: int) -> bool:
@@ -57,6 +105,11 @@ class ContextKVWriter:
         self.head_dim = int(c0.shape[3]) // 2
         self._dtype = kv_dtype_code(kv_cache_dtype)
         self._tables = Tables(self.num_layers)
+        # the writer's own error word: every launch reports into it unless the
+        # caller passes one (see error_flags())
+        import torch
+
+        self._flags = torch.zeros(1, dtype=torch.int32, device=c0.device)
 
     def _descs(self):
         return [cache_desc(c, self.kv_cache_dtype, k, v)
@@ -75,6 +128,17 @@ class ContextKVWriter:
     def tables(self) -> Tables:
         return self._tables
 
+    def error_flags(self, clear: bool = True) -> int:
+        """The bits the kernels raised in the writer's own error word since it
+        was last cleared (calls that passed their own ``error_flags`` report
+        there instead): FLAG_SLOT_RANGE / FLAG_POS_RANGE for rows skipped as
+        out of range, FLAG_TIMEOUT when a launch gave up on a bounded wait and
+        left rows unwritten.  Reading it synchronises with the device."""
+        v = int(self._flags.item())
+        if clear and v:
+            self._flags.zero_()
+        return v
+
     def ensure_tables(self, stream=None):
         self._tables.update(self.kv_caches, self.k_scales, self.v_scales, stream)
 
@@ -84,19 +148,33 @@ class ContextKVWriter:
         of one per layer (the same tensor everywhere counts as shared, like
         the pages' _shared_slot_mapping; otherwise each layer's rows go to
         its own slots)."""
+        import torch
+
+        dev = self.kv_caches[0].device
+        _check_tensor("all_kv", all_kv, torch.bfloat16, dev, ndim=5)
         num_ctx, L, two, nkv, hd = all_kv.shape
         if L != self.num_layers or nkv != self.num_kv_heads or two != 2 or hd != self.head_dim:
             raise DSparkError(1, f"all_kv shape {tuple(all_kv.shape)} does not match the layers")
-        if num_ctx == 0:
-            return
+        _check_tensor("k_norm_weight", k_norm_weight, torch.bfloat16, dev, shape=(L, self.head_dim))
+        _check_index("positions", positions, dev, num_ctx)
+        _check_cos_sin(cos_sin_cache, rotary_dim, dev)
+        _check_flags(error_flags, dev)
         per_layer = None
         if isinstance(slot_mapping, (list, tuple)):
             if len(slot_mapping) != L or any(s is None for s in slot_mapping):
                 raise DSparkError(1, "one slot mapping per layer expected")
+            for l, s in enumerate(slot_mapping):
+                _check_index(f"slot_mapping[{l}]", s, dev, num_ctx)
             if all(s.data_ptr() == slot_mapping[0].data_ptr() for s in slot_mapping):
                 slot_mapping = slot_mapping[0]
             else:
                 per_layer = slot_mapping
+        else:
+            _check_index("slot_mapping", slot_mapping, dev, num_ctx)
+        if num_ctx == 0:
+            return
+        if error_flags is None:
+            error_flags = self._flags
         self.ensure_tables(stream)
         t = self._tables
         if per_layer is not None:
@@ -118,21 +196,31 @@ class ContextKVWriter:
         args = (all_kv, k_norm_weight, positions, slot_mapping, num_ctx, cos_sin_cache,
                 cos_sin_cache.shape[0], self.kv_caches[0], self.num_blocks, t.cache_offsets,
                 t.k_scales, t.v_scales, L, nkv, self.block_size, rotary_dim, eps, self._dtype)
-        if error_flags is None:
-            dspark_ctx_kv_write(*args, stream=stream)
-        else:
-            dspark_ctx_kv_write_ex(*args, error_flags, stream=stream)
+        dspark_ctx_kv_write_ex(*args, error_flags, stream=stream)
 
     def project_and_write(self, context_states, w_kv, k_norm_weight, eps, positions, cos_sin_cache, rotary_dim,
                           slot_mapping, stream=None, error_flags=None):
         """Project the (normed) context states with the stacked K/V weights
         ``w_kv`` ``[L * 2 * nkv * 128, hidden]`` and write every layer's
         context K/V in the same launch: all_kv never reaches device memory."""
+        import torch
+
+        dev = self.kv_caches[0].device
+        _need(self.head_dim == HEAD_DIM, "the fused projection takes head_dim 128")
+        _check_tensor("context_states", context_states, torch.bfloat16, dev, ndim=2)
         num_ctx, hidden = context_states.shape
+        _check_tensor("w_kv", w_kv, torch.bfloat16, dev, ndim=2)
         if w_kv.shape[0] != self.num_layers * 2 * self.num_kv_heads * HEAD_DIM or w_kv.shape[1] != hidden:
             raise DSparkError(1, f"w_kv shape {tuple(w_kv.shape)} does not match the layers and hidden {hidden}")
+        _check_tensor("k_norm_weight", k_norm_weight, torch.bfloat16, dev, shape=(self.num_layers, HEAD_DIM))
+        _check_index("positions", positions, dev, num_ctx)
+        _check_index("slot_mapping", slot_mapping, dev, num_ctx)
+        _check_cos_sin(cos_sin_cache, rotary_dim, dev)
+        _check_flags(error_flags, dev)
         if num_ctx == 0:
             return
+        if error_flags is None:
+            error_flags = self._flags
         self.ensure_tables(stream)
         t = self._tables
         dspark_ctx_kv_project_write(context_states, w_kv, num_ctx, hidden, k_norm_weight, positions, slot_mapping,
@@ -158,18 +246,36 @@ def qknorm_rope_kv_insert(qkv, q_norm_weight, k_norm_weight, cos_sin_cache, posi
     """
     import torch
 
+    _need(isinstance(qkv, torch.Tensor), "qkv must be a tensor")
+    dev = qkv.device
+    _check_tensor("qkv", qkv, torch.bfloat16, dev, ndim=2)
     T = qkv.shape[0]
-    if qkv.dim() != 2 or qkv.shape[1] != (num_heads + 2 * num_kv_heads) * HEAD_DIM:
+    if qkv.shape[1] != (num_heads + 2 * num_kv_heads) * HEAD_DIM:
         raise DSparkError(1, f"qkv shape {tuple(qkv.shape)} does not match {num_heads}+2x{num_kv_heads} heads")
+    _check_tensor("q_norm_weight", q_norm_weight, torch.bfloat16, dev, shape=(HEAD_DIM,))
+    _check_tensor("k_norm_weight", k_norm_weight, torch.bfloat16, dev, shape=(HEAD_DIM,))
+    _check_cos_sin(cos_sin_cache, rotary_dim, dev)
+    _check_index("positions", positions, dev, T)
+    _check_flags(error_flags, dev)
     if (slot_mapping is None) != (kv_cache is None):
         raise DSparkError(1, "slot_mapping and kv_cache go together")
     num_blocks = block_size = 0
     dtype = "auto"
     if kv_cache is not None:
+        _check_index("slot_mapping", slot_mapping, dev, T)
+        _need(isinstance(kv_cache, torch.Tensor) and kv_cache.dtype in (torch.bfloat16, torch.uint8),
+              "kv_cache must be a bf16 or uint8 (fp8 e4m3) tensor")
+        _check_tensor("kv_cache", kv_cache, kv_cache.dtype, dev, ndim=4)
         num_blocks, nkv, block_size = (int(x) for x in kv_cache.shape[:3])
         if nkv != num_kv_heads or kv_cache.shape[3] != 2 * HEAD_DIM:
             raise DSparkError(1, f"kv_cache shape {tuple(kv_cache.shape)} does not match {num_kv_heads} KV heads")
         dtype = "fp8" if kv_cache.dtype == torch.uint8 else "auto"
+        for name, sc in (("k_scale", k_scale), ("v_scale", v_scale)):
+            if sc is not None:
+                _check_tensor(name, sc, torch.float32, dev)
+                _need(sc.numel() >= 1, f"{name} must hold one fp32 value")
+    if q_fp8_out is not None:
+        _check_tensor("q_fp8_out", q_fp8_out, torch.uint8, dev, shape=(T, num_heads * HEAD_DIM))
     dspark_qknorm_rope_kv_insert(qkv, q_norm_weight, k_norm_weight, cos_sin_cache, cos_sin_cache.shape[0],
                                  positions, T, num_heads, num_kv_heads, rotary_dim, eps, slot_mapping,
                                  kv_cache, num_blocks, block_size, dtype, k_scale, v_scale, q_fp8_out,
@@ -181,10 +287,16 @@ def project_context_kv(context_states, w_kv, num_layers, num_kv_heads, out=None,
     on the tensor cores (the fused projection the context-KV writer reads)."""
     import torch
 
+    _need(isinstance(context_states, torch.Tensor), "context_states must be a tensor")
+    dev = context_states.device
+    _check_tensor("context_states", context_states, torch.bfloat16, dev, ndim=2)
     num_ctx, hidden = context_states.shape
+    _check_tensor("w_kv", w_kv, torch.bfloat16, dev, shape=(num_layers * 2 * num_kv_heads * HEAD_DIM, hidden))
     if out is None:
-        out = torch.empty((num_ctx, num_layers, 2, num_kv_heads, HEAD_DIM), dtype=torch.bfloat16,
-                          device=context_states.device)
+        out = torch.empty((num_ctx, num_layers, 2, num_kv_heads, HEAD_DIM), dtype=torch.bfloat16, device=dev)
+    _check_tensor("out", out, torch.bfloat16, dev)
+    _need(out.numel() == num_ctx * num_layers * 2 * num_kv_heads * HEAD_DIM,
+          f"out has {out.numel()} elements, the projection {num_ctx} x {num_layers * 2 * num_kv_heads * HEAD_DIM}")
     dspark_ctx_kv_project(context_states, w_kv, out, num_ctx, hidden, num_layers, num_kv_heads, stream)
     return out
 
@@ -195,8 +307,12 @@ def gemma_rms_norm(x, weight, eps, out=None, stream=None):
     of ``x`` (bf16 ``[rows, hidden]``); ``out=x`` works in place."""
     import torch
 
+    _need(isinstance(x, torch.Tensor), "x must be a tensor")
+    _check_tensor("x", x, torch.bfloat16, x.device, ndim=2)
     rows, hidden = x.shape
+    _check_tensor("weight", weight, torch.bfloat16, x.device, shape=(hidden,))
     if out is None:
         out = torch.empty_like(x)
+    _check_tensor("out", out, torch.bfloat16, x.device, shape=(rows, hidden))
     dspark_gemma_rms_norm(x, weight, out, rows, hidden, eps, stream)
     return out

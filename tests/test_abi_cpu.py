@@ -317,3 +317,175 @@ def test_general_layout_rules(L):
     span = 8 * 2 * 24 * 512 * 2
     assert general_status([desc(shape=(8, 2, 24, 512)), desc(data=FAKE + span + 16, shape=(8, 2, 24, 512))]) == \
         "DSPARK_ERR_ALIGNMENT"
+
+
+# ---------------------------------------------------------------- tensor checks of the Python API
+# The library receives only addresses, so the Python layer checks every
+# tensor's dtype, device, contiguity and extent before the call (the pages'
+# writer validates its inputs before the launch).  A writer object is built
+# here around CPU caches without its device tables; reaching the library is
+# replaced by a sentinel, so no test here touches a GPU.
+
+class _Reached(Exception):
+    pass
+
+
+def _stop(*a, **k):
+    raise _Reached()
+
+
+def _cpu_writer(monkeypatch, L=2, H=2, bs=16, nb=4):
+    import torch
+    from speculative_decoding_draft_ctx_gb300 import writer as wr
+
+    w = object.__new__(wr.ContextKVWriter)
+    w.kv_caches = [torch.empty(nb, H, bs, 256, dtype=torch.bfloat16) for _ in range(L)]
+    w.k_scales = w.v_scales = [torch.ones(1) for _ in range(L)]
+    w.kv_cache_dtype, w.general, w._dtype, w._flags = "auto", False, 0, None
+    w.num_layers, w.num_blocks, w.num_kv_heads, w.block_size, w.head_dim = L, nb, H, bs, 128
+    monkeypatch.setattr(w, "ensure_tables", _stop)
+    monkeypatch.setattr(wr, "dspark_ctx_kv_project_write", _stop)
+    return w
+
+
+def _good_write_args(T=4, L=2, H=2, r=32):
+    import torch
+
+    bf = torch.bfloat16
+    return dict(all_kv=torch.zeros(T, L, 2, H, 128, dtype=bf), k_norm_weight=torch.zeros(L, 128, dtype=bf),
+                eps=1e-6, positions=torch.zeros(T, dtype=torch.int64), cos_sin_cache=torch.zeros(64, r, dtype=bf),
+                rotary_dim=r, slot_mapping=torch.zeros(T, dtype=torch.int64))
+
+
+def _bad_write_cases():
+    import torch
+
+    bf = torch.bfloat16
+    return [
+        ("positions", torch.zeros(4, dtype=torch.int32)),           # read as int64: 8T bytes from 4T
+        ("slot_mapping", torch.zeros(4, dtype=torch.int32)),
+        ("positions", torch.zeros(3, dtype=torch.int64)),           # fewer entries than tokens
+        ("slot_mapping", torch.zeros(3, dtype=torch.int64)),
+        ("positions", torch.zeros(8, dtype=torch.int64)[::2]),      # not contiguous
+        ("cos_sin_cache", torch.zeros(64, 16, dtype=bf)),          # narrower than rotary_dim
+        ("cos_sin_cache", torch.zeros(64, 32, dtype=torch.float32)),
+        ("cos_sin_cache", torch.zeros(64, 64, dtype=bf)[:, :32]),  # right width, not contiguous
+        ("k_norm_weight", torch.zeros(128, dtype=bf)),             # [128], not [L, 128]
+        ("k_norm_weight", torch.zeros(2, 128, dtype=torch.float32)),
+        ("all_kv", torch.zeros(4, 2, 2, 2, 256, dtype=bf)[..., :128]),
+        ("all_kv", torch.zeros(4, 2, 2, 2, 128, dtype=torch.float32)),
+        ("all_kv", torch.zeros(4, 2, 2, 2, 128, dtype=bf, device="meta")),  # not on the caches' device
+        ("positions", torch.zeros(4, dtype=torch.int64, device="meta")),
+        ("error_flags", torch.zeros(1, dtype=torch.int64)),
+        ("error_flags", torch.zeros(0, dtype=torch.int32)),
+    ]
+
+
+def test_writer_passes_good_tensors_to_the_library(monkeypatch):
+    w = _cpu_writer(monkeypatch)
+    with pytest.raises(_Reached):
+        w(**_good_write_args())
+    import torch
+
+    a = _good_write_args()
+    a["slot_mapping"] = [torch.zeros(4, dtype=torch.int64), torch.ones(4, dtype=torch.int64)]
+    with pytest.raises(_Reached):
+        w(**a)
+
+
+@pytest.mark.parametrize("case", range(16))
+def test_writer_refuses_bad_tensors(monkeypatch, case):
+    name, bad = _bad_write_cases()[case]
+    w = _cpu_writer(monkeypatch)
+    a = _good_write_args()
+    a[name] = bad
+    with pytest.raises(dk.DSparkError) as ei:
+        w(**a)
+    assert ei.value.name == "DSPARK_ERR_INVALID_ARG"
+
+
+def test_writer_refuses_bad_per_layer_slot_mapping(monkeypatch):
+    import torch
+
+    w = _cpu_writer(monkeypatch)
+    a = _good_write_args()
+    a["slot_mapping"] = [torch.zeros(4, dtype=torch.int64), torch.zeros(4, dtype=torch.int32)]
+    with pytest.raises(dk.DSparkError, match="slot_mapping\\[1\\]"):
+        w(**a)
+
+
+def test_project_and_write_refuses_bad_tensors(monkeypatch):
+    import torch
+
+    bf = torch.bfloat16
+    w = _cpu_writer(monkeypatch)
+    a = _good_write_args()
+    good = dict(context_states=torch.zeros(4, 64, dtype=bf), w_kv=torch.zeros(2 * 2 * 2 * 128, 64, dtype=bf),
+                k_norm_weight=a["k_norm_weight"], eps=1e-6, positions=a["positions"],
+                cos_sin_cache=a["cos_sin_cache"], rotary_dim=32, slot_mapping=a["slot_mapping"])
+    with pytest.raises(_Reached):
+        w.project_and_write(**good)
+    for name, bad in [("context_states", torch.zeros(4, 64)), ("context_states", torch.zeros(4, 128, dtype=bf)[:, ::2]),
+                      ("w_kv", torch.zeros(1024, 64)), ("positions", torch.zeros(4, dtype=torch.int32)),
+                      ("slot_mapping", torch.zeros(2, dtype=torch.int64)),
+                      ("cos_sin_cache", torch.zeros(64, 16, dtype=bf)), ("k_norm_weight", torch.zeros(128, dtype=bf))]:
+        b = dict(good)
+        b[name] = bad
+        with pytest.raises(dk.DSparkError) as ei:
+            w.project_and_write(**b)
+        assert ei.value.name == "DSPARK_ERR_INVALID_ARG", name
+
+
+def test_qk_insert_refuses_bad_tensors(monkeypatch):
+    import torch
+    from speculative_decoding_draft_ctx_gb300 import writer as wr
+
+    monkeypatch.setattr(wr, "dspark_qknorm_rope_kv_insert", _stop)
+    bf = torch.bfloat16
+    T, Hq, Hkv = 3, 4, 1
+    good = dict(qkv=torch.zeros(T, (Hq + 2 * Hkv) * 128, dtype=bf), q_norm_weight=torch.zeros(128, dtype=bf),
+                k_norm_weight=torch.zeros(128, dtype=bf), cos_sin_cache=torch.zeros(64, 64, dtype=bf),
+                positions=torch.zeros(T, dtype=torch.int64), num_heads=Hq, num_kv_heads=Hkv, rotary_dim=64,
+                eps=1e-6, slot_mapping=torch.zeros(T, dtype=torch.int64),
+                kv_cache=torch.zeros(4, Hkv, 16, 256, dtype=torch.uint8), k_scale=torch.ones(1),
+                v_scale=torch.ones(1), q_fp8_out=torch.zeros(T, Hq * 128, dtype=torch.uint8))
+    with pytest.raises(_Reached):
+        wr.qknorm_rope_kv_insert(**good)
+    for name, bad in [("qkv", torch.zeros(T, (Hq + 2 * Hkv) * 128)), ("q_norm_weight", torch.zeros(2, 128, dtype=bf)),
+                      ("k_norm_weight", torch.zeros(128)), ("cos_sin_cache", torch.zeros(64, 32, dtype=bf)),
+                      ("positions", torch.zeros(T, dtype=torch.int32)), ("slot_mapping", torch.zeros(2, dtype=torch.int64)),
+                      ("kv_cache", torch.zeros(4, Hkv, 16, 256, dtype=torch.float16)),
+                      ("kv_cache", torch.zeros(4, Hkv, 16, 512, dtype=torch.uint8)[..., :256]),
+                      ("k_scale", torch.ones(1, dtype=torch.float64)), ("v_scale", torch.ones(0)),
+                      ("q_fp8_out", torch.zeros(T, Hq * 128 - 1, dtype=torch.uint8)),
+                      ("qkv", torch.zeros(T, (Hq + 2 * Hkv) * 128, dtype=bf, device="meta"))]:
+        b = dict(good)
+        b[name] = bad
+        with pytest.raises(dk.DSparkError) as ei:
+            wr.qknorm_rope_kv_insert(**b)
+        assert ei.value.name == "DSPARK_ERR_INVALID_ARG", name
+
+
+def test_projection_and_norm_refuse_bad_tensors(monkeypatch):
+    import torch
+    from speculative_decoding_draft_ctx_gb300 import writer as wr
+
+    monkeypatch.setattr(wr, "dspark_ctx_kv_project", _stop)
+    monkeypatch.setattr(wr, "dspark_gemma_rms_norm", _stop)
+    bf = torch.bfloat16
+    x, w = torch.zeros(4, 64, dtype=bf), torch.zeros(2 * 2 * 2 * 128, 64, dtype=bf)
+    with pytest.raises(_Reached):
+        wr.project_context_kv(x, w, 2, 2)
+    for args in [(torch.zeros(4, 64), w), (x, torch.zeros(1024, 32, dtype=bf)), (x, w.t().contiguous())]:
+        with pytest.raises(dk.DSparkError):
+            wr.project_context_kv(*args, 2, 2)
+    with pytest.raises(dk.DSparkError):
+        wr.project_context_kv(x, w, 2, 2, out=torch.zeros(4, 1000, dtype=bf))
+    with pytest.raises(_Reached):
+        wr.gemma_rms_norm(x, torch.zeros(64, dtype=bf), 1e-6)
+    for args in [(torch.zeros(4, 64), torch.zeros(64, dtype=bf)), (x, torch.zeros(32, dtype=bf)),
+                 (x, torch.zeros(64))]:
+        with pytest.raises(dk.DSparkError):
+            wr.gemma_rms_norm(*args, 1e-6)
+    with pytest.raises(dk.DSparkError):
+        wr.gemma_rms_norm(x, torch.zeros(64, dtype=bf), 1e-6, out=torch.zeros(4, 32, dtype=bf))

@@ -3,9 +3,10 @@ inputs, element by element, through the C ABI.
 
 Small workloads compare whole caches (every byte of every layer); the two
 full-size workloads (prefill batch, long context) run in the same launch
-configuration the benchmark times and compare every written row (prefill)
-or a sample of rows the oracle computes one by one (long context), plus
-whole-cache properties: exactly the addressed rows changed.
+configuration the benchmark times and compare every written row with the
+oracle's, plus whole-cache properties: exactly the addressed rows changed.
+The long-context write is also checked by a placement round trip with
+tagged V rows.
 Tolerance: see tests/parity.py.
 """
 
@@ -80,18 +81,50 @@ def test_parity_prefill_full_size(oracle_lib, kernel):
     _check_rows(inp, caches, row_ids=None)
 
 
-def test_parity_long_context_sampled(oracle_lib):
-    """Long context (65536 tokens, bf16, r=16, bs=128): rows of 4096 sampled
-    tokens, all layers and heads; the whole-cache property check covers the rest."""
+def test_parity_long_context_full_size(oracle_lib, kernel):
+    """Long context (65536 tokens, bf16, r=16, bs=128) at full size: every
+    written row -- all 1,310,720 (token, layer, head) rows -- against the
+    oracle, and exactly the addressed rows changed."""
     wl = wk.WORKLOADS[4]
     inp = wk.generate(wl)
     caches, _, _ = gpu_write(inp)
-    g = torch.Generator().manual_seed(7)
-    toks = torch.randperm(wl.num_ctx, generator=g)[:4096]
-    toks = torch.cat([toks, torch.tensor([0, wl.num_ctx - 1])]).unique()
-    L, H = wl.num_layers, wl.num_kv_heads
-    ids = (toks[:, None] * (L * H) + torch.arange(L * H)[None, :]).flatten().numpy()
-    _check_rows(inp, caches, row_ids=ids)
+    _check_rows(inp, caches, row_ids=None)
+
+
+def test_placement_long_context_tagged(oracle_lib, kernel):
+    """Placement round trip at full size (long context): V of every row
+    carries exact small-integer tags of its own (token, layer, head) -- token
+    low byte, token high byte, layer, head, each an integer below 256 and so
+    exact in bf16 -- and every written row of every layer's cache must
+    decode back to a token whose slot (oracle placement rule) and head give
+    exactly that row, in that layer; every layer holds exactly the valid
+    tokens' rows (writer page: slots < 0 are padding and are not written)."""
+    import oracle
+
+    wl = wk.WORKLOADS[4]
+    inp = wk.generate(wl)
+    T, L, H = wl.num_ctx, wl.num_layers, wl.num_kv_heads
+    t = torch.arange(T)
+    v = inp.all_kv[:, :, 1]  # [T, L, H, 128] view
+    v[..., 0] = (t & 255).to(torch.bfloat16)[:, None, None]
+    v[..., 1] = (t >> 8).to(torch.bfloat16)[:, None, None]
+    v[..., 2] = torch.arange(L, dtype=torch.bfloat16)[None, :, None]
+    v[..., 3] = torch.arange(H, dtype=torch.bfloat16)[None, None, :]
+    caches, _, _ = gpu_write(inp)
+    slots = inp.slot_mapping.numpy()
+    nvalid = int((slots >= 0).sum())
+    for layer, c in enumerate(caches):
+        rows = c.view(-1, 256)
+        written = (rows.view(torch.int16) != -1).any(dim=1).nonzero().flatten()
+        assert written.numel() == nvalid * H, (layer, written.numel(), nvalid * H)
+        tags = rows[written][:, 128:132].float().cpu().numpy().astype(np.int64)
+        tt = tags[:, 0] + 256 * tags[:, 1]
+        assert (tags[:, 2] == layer).all()
+        assert ((tt >= 0) & (tt < T)).all()
+        assert (slots[tt] >= 0).all()
+        dest = np.array([oracle.dest_row(int(s), int(h), H, wl.block_size, wl.num_blocks)
+                         for s, h in zip(slots[tt], tags[:, 3])], np.int64)
+        assert np.array_equal(dest, written.cpu().numpy())
 
 
 def _check_rows(inp, caches, row_ids):
@@ -125,7 +158,14 @@ def _check_rows(inp, caches, row_ids):
             continue
         rows = caches[layer].view(-1, 256)[torch.from_numpy(dest[m]).cuda()].cpu()
         gpu[m] = rows.view(torch.uint8).numpy() if fp8 else rows.view(torch.int16).numpy().view(np.uint16)
-    bad = compare_rows(gpu, ora, alt_index_rows(alts), fp8)
+    # compared in chunks of rows, so that full-size workloads stay within a
+    # few GB of host memory
+    ar, ad, av = alts
+    bad = []
+    chunk = 1 << 17
+    for c0 in range(0, len(row_ids), chunk):
+        m = (ar >= c0) & (ar < c0 + chunk)
+        bad += compare_rows(gpu[c0:c0 + chunk], ora[c0:c0 + chunk], alt_index_rows((ar[m] - c0, ad[m], av[m])), fp8)
     assert not bad, bad[:10]
     # whole caches: exactly the addressed rows differ from the 0xFF prefill
     nvalid = int((slots >= 0).sum())

@@ -42,12 +42,13 @@ int ok()
     return DSPARK_OK;
 }
 
-// Which kernel serves a call: for the pages' layouts the pipelined one where
-// the shape allows, else the generic one; the general kernel for every other
-// layout.  DSPARK_CTX_KV_KERNEL=generic pins the generic kernel for the
-// pages' layouts and =general the general kernel for every layout, for the
-// calls made while it is set (all compute the same result; the tests run
-// each).
+// Which kernel serves a call: the pipelined one where a token's rows fit a
+// stage, else the generic one for the pages' layouts; the general kernel for
+// every other layout.  DSPARK_CTX_KV_KERNEL=warp picks the warp-private
+// pipelines where they apply (the pages' layouts with 4 or 8 KV heads and a
+// shared slot mapping), =generic the generic kernel for the pages' layouts
+// and =general the general kernel for every layout, for the calls made while
+// it is set (all compute the same result; the tests run each).
 bool force_kernel(const char *name)
 {
     const char *e = std::getenv("DSPARK_CTX_KV_KERNEL");
@@ -256,6 +257,8 @@ int write_common(const void *all_kv, const void *knorm_w, const int64_t *positio
         e = dspark::launch_ctx_kv_general(p, head_dim, fp8, stream);
     else if (pages_layout && force_kernel("generic"))
         e = dspark::launch_ctx_kv_write(p, rotary_dim, fp8, stream);
+    else if (pages_layout && force_kernel("warp") && dspark::warp_path_supported(p))
+        e = dspark::launch_ctx_kv_write_warp(p, fp8, stream);
     else if (dspark::tma_path_supported(p, head_dim))
         e = dspark::launch_ctx_kv_write_tma(p, head_dim, fp8, stream);
     else if (pages_layout)

@@ -3,16 +3,18 @@
 //
 // The fp8 store holds e4m3(x / scale) with the division in fp32 (vLLM DSpark
 // context-KV writer page, module docstring: "fp8 e4m3 of x / scale").  The
-// quotient is formed exactly, without a division instruction: with the
-// negated correctly rounded reciprocal n = -RN(1/s), Markstein's FMA
-// correction  p0 = x n,  e = p0 s + x (exact),  p = p0 + e n  gives
-// p = -RN(x / s) whenever |x| and |x / s| are at least 2^-90 (below, the
-// residual underflows and the quotient encodes to a signed zero either way);
-// x is first clamped in magnitude to a bf16 bound just above 512 s, so x n
-// cannot overflow and every clamped quotient still saturates.  The saturating
-// RNE pack of p with every sign bit flipped is the code of the IEEE quotient;
-// a NaN input gives the NaN code 0xFF.  The method is checked against IEEE
-// division for every bf16 input on the CPU.
+// quotient is formed exactly, without a division instruction.  x is first
+// clamped in magnitude to a bf16 bound just above 512 s and negated, in one
+// instruction (min.xorsign.abs against the negated bound): x' = -sign(x)
+// min(|x|, B), so x' n cannot overflow and every clamped quotient still
+// saturates.  With the negated correctly rounded reciprocal n = -RN(1/s),
+// Markstein's FMA correction  p0 = x' n,  e = p0 s + x' (exact),
+// p = p0 + e n  gives p = RN(-x' / s) = RN(x_c / s) whenever |x| and |x / s|
+// are at least 2^-90 (below, the residual underflows and the quotient
+// encodes to a zero of the right sign either way); signed zeros come out
+// with the sign of x.  The saturating RNE pack of p is the code of the IEEE
+// quotient; a NaN input gives the NaN code 0x7F.  The method is checked
+// against IEEE division for every bf16 input on the CPU.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -75,7 +77,8 @@ __device__ __forceinline__ uint32_t f2_to_bf2(uint64_t v)
     return pack_bf16x2(lo, hi);
 }
 
-// |w| clamped to the bf16 pair `bound` per half, sign and NaN kept
+// min(|w|, |bound|) per half with the sign of w XOR the sign of bound (a
+// negative bound negates), NaN kept
 __device__ __forceinline__ uint32_t clamp_bf2(uint32_t w, uint32_t bound)
 {
     uint32_t d;
@@ -84,8 +87,8 @@ __device__ __forceinline__ uint32_t clamp_bf2(uint32_t w, uint32_t bound)
 }
 
 // Four e4m3 codes in one word, element order a b c d from the low byte up,
-// RNE with saturation, every sign bit flipped.
-__device__ __forceinline__ uint32_t neg_e4m3x4(uint64_t ab, uint64_t cd)
+// RNE with saturation.
+__device__ __forceinline__ uint32_t e4m3x4(uint64_t ab, uint64_t cd)
 {
     float a, b, c, d;
     unpr(ab, a, b);
@@ -97,34 +100,41 @@ __device__ __forceinline__ uint32_t neg_e4m3x4(uint64_t ab, uint64_t cd)
         "mov.b32 %0, {lo, hi};\n\t}"
         : "=r"(w)
         : "f"(a), "f"(b), "f"(c), "f"(d));
-    return w ^ 0x80808080u;
+    return w;
 }
 
-// e4m3 codes of x / s for the 8 bf16 values of v (two 4-code words): bound
-// is the clamp bound as a bf16 pair, s2 = (s, s), n2 = (-RN(1/s), -RN(1/s)).
-__device__ __forceinline__ uint2 quantise8(const uint4 &v, uint32_t bound, uint64_t s2, uint64_t n2)
+// -x' / s correctly rounded for an fp32 pair x' (already clamped and
+// negated): s2 = (s, s), n2 = (-RN(1/s), -RN(1/s)).
+__device__ __forceinline__ uint64_t quotient2(uint64_t x, uint64_t s2, uint64_t n2)
 {
-    const uint32_t w[4] = {clamp_bf2(v.x, bound), clamp_bf2(v.y, bound), clamp_bf2(v.z, bound),
-                           clamp_bf2(v.w, bound)};
+    const uint64_t p0 = mul2(x, n2);
+    const uint64_t e = fma2(p0, s2, x);
+    return fma2(e, n2, p0);
+}
+
+// e4m3 codes of x / s for the 8 bf16 values of v (two 4-code words): nbound
+// is the negated clamp bound as a bf16 pair, s2 = (s, s),
+// n2 = (-RN(1/s), -RN(1/s)).
+__device__ __forceinline__ uint2 quantise8(const uint4 &v, uint32_t nbound, uint64_t s2, uint64_t n2)
+{
+    const uint32_t w[4] = {clamp_bf2(v.x, nbound), clamp_bf2(v.y, nbound), clamp_bf2(v.z, nbound),
+                           clamp_bf2(v.w, nbound)};
     uint64_t p[4];
 #pragma unroll
-    for (int j = 0; j < 4; j++) {
-        const uint64_t x = bf2_to_f2(w[j]);
-        const uint64_t p0 = mul2(x, n2);
-        const uint64_t e = fma2(p0, s2, x);
-        p[j] = fma2(e, n2, p0);
-    }
-    return make_uint2(neg_e4m3x4(p[0], p[1]), neg_e4m3x4(p[2], p[3]));
+    for (int j = 0; j < 4; j++)
+        p[j] = quotient2(bf2_to_f2(w[j]), s2, n2);
+    return make_uint2(e4m3x4(p[0], p[1]), e4m3x4(p[2], p[3]));
 }
 
 
-// Clamp bound of a scale: the smallest bf16 >= 512 s, as a bf16 pair.
+// Negated clamp bound of a scale: minus the smallest bf16 >= 512 s, as a
+// bf16 pair.
 __device__ __forceinline__ uint32_t fp8_bound_pair(float s)
 {
     uint32_t u = __float_as_uint(512.0f * s);
     if (u & 0xffffu)
         u = (u & 0xffff0000u) + 0x10000u;
-    return (u >> 16) * 0x10001u;
+    return ((u >> 16) | 0x8000u) * 0x10001u;
 }
 
 // Everything quantise8 needs for one scale.

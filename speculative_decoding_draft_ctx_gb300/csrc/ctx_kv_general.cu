@@ -124,13 +124,9 @@ __device__ __forceinline__ Words<W / 2> quantise(const Words<W> &v, const Fp8Sca
     for (int k = 0; k < W / 2; k++) {
         uint64_t pq[2];
 #pragma unroll
-        for (int j = 0; j < 2; j++) {
-            const uint64_t x = bf2_to_f2(clamp_bf2(v.w[2 * k + j], q.bound));
-            const uint64_t p0 = mul2(x, q.n2);
-            const uint64_t e = fma2(p0, q.s2, x);
-            pq[j] = fma2(e, q.n2, p0);
-        }
-        out.w[k] = neg_e4m3x4(pq[0], pq[1]);
+        for (int j = 0; j < 2; j++)
+            pq[j] = quotient2(bf2_to_f2(clamp_bf2(v.w[2 * k + j], q.bound)), q.s2, q.n2);
+        out.w[k] = e4m3x4(pq[0], pq[1]);
     }
     return out;
 }

@@ -101,6 +101,12 @@ cudaError_t launch_ctx_kv_general(const CtxKvParams &p, int head_dim, bool fp8, 
 bool tma_path_supported(const CtxKvParams &p, int head_dim);
 cudaError_t launch_ctx_kv_write_tma(const CtxKvParams &p, int head_dim, bool fp8, cudaStream_t stream);
 
+// Warp-private pipelines (ctx_kv_warp.cu): head dim 128, rotary dim 16 / 32 /
+// 64, power-of-two block sizes, 4 or 8 KV heads, any layer count, a shared
+// slot mapping.
+bool warp_path_supported(const CtxKvParams &p);
+cudaError_t launch_ctx_kv_write_warp(const CtxKvParams &p, bool fp8, cudaStream_t stream);
+
 // Draft-token fused QK-norm / RoPE / KV insert (qk_insert_kernel.cu).
 struct QkInsertParams {
     uint16_t *qkv;               // bf16 bits [T, (Hq + 2 Hkv) * 128], updated in place

@@ -32,8 +32,16 @@
 // and of V (q = lane % 8), so every 16-byte shared load is conflict-free and
 // every 16-byte (bf16) or 8-byte (fp8) global store of a warp covers 4 whole
 // 128-byte (64-byte) segments.  Sum of squares: paired FMAs + 3 xor shuffles
-// within the row's 8 lanes.  RoPE with r = 16, 32 or 64: the partner of dim
-// d is d +- r/2, r/16 lanes away within the row's 8 lanes (one xor shuffle).
+// within the row's 8 lanes.  RoPE with r = 16 or 64: the partner of dim d is
+// d +- r/2, r/16 lanes away within the row's 8 lanes (one xor shuffle).
+// r = 32 maps K differently: lane q holds dims [32k + 4q, 32k + 4q + 4) for
+// k = 0..3, so the 32 rotated dims are four on every lane of the row and
+// each lane's first segment rotates against lane q ^ 4 (with 8-dim chunks
+// only half the lanes would hold rotated dims, the other half computing a
+// rotation they throw away).  In these three modes (head dim 128) a consumer
+// warp copies its rows of the stage (at most two groups) and the token's
+// cos|sin words into registers and releases the stage before computing, so
+// the producer refills it while the warp computes.
 // Any other even r: the normed row goes to a per-warp shared scratch (rows
 // padded by 4 bytes, so the warp's partner reads hit 32 different banks), and
 // after a __syncwarp each rotated dim reads its partner there; the token's
@@ -63,9 +71,12 @@
 
 #include "ctx_kv_device.cuh"
 #include "ctx_kv_internal.h"
+#include "ctx_kv_pipe.cuh"
 
 namespace dspark {
 namespace {
+
+using namespace pipe;
 
 constexpr int kConsumerWarps = 8;
 constexpr int kThreads = 32 * (kConsumerWarps + 1);  // last warp is the producer
@@ -73,7 +84,6 @@ constexpr int kCsBytes = 128;                        // cos|sin row slot (r <= 6
 constexpr unsigned kFlagSlot = 0x1u;
 constexpr unsigned kFlagPos = 0x2u;
 constexpr unsigned kFlagTimeout = 0x4u;
-constexpr unsigned long long kTimeoutNs = 4000000000ull;  // 4 s
 constexpr int kMaxTmaLayers = 32;
 
 // What the producer tells the consumers about a stage.
@@ -83,144 +93,6 @@ struct StageHdr {
     int l0;         // first layer in the stage
     int rows;       // rows in the stage (layers * nkv); < 0: end of work
 };
-
-// ------------------------------------------------------------------ PTX helpers
-
-__device__ __forceinline__ uint32_t smem_addr(const void *p)
-{
-    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-
-__device__ __forceinline__ unsigned long long globaltimer()
-{
-    unsigned long long t;
-    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-    return t;
-}
-
-__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count)
-{
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count) : "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive(uint64_t *bar)
-{
-    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes)
-{
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)), "r"(bytes)
-                 : "memory");
-}
-
-// One poll of a barrier phase.  A waiting warp is suspended by the hardware
-// (up to kSuspendNs) until the phase completes, so waiting warps do not take
-// issue slots from the warps that compute.
-constexpr uint32_t kSuspendNs = 200000;
-
-// Raises the transaction count the current phase of `bar` waits for,
-// without arriving.
-__device__ __forceinline__ void mbar_expect_tx(uint64_t *bar, uint32_t bytes)
-{
-    asm volatile("mbarrier.expect_tx.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(bytes)
-                 : "memory");
-}
-
-__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity)
-{
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(smem_addr(bar)), "r"(parity), "n"(kSuspendNs)
-        : "memory");
-    return ok != 0;
-}
-
-// Waits for the phase of `bar` with the given parity to complete.  Gives up
-// (and raises the CTA's abort word) after kTimeoutNs, or as soon as another
-// warp of the CTA has given up.
-__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volatile int *abort)
-{
-    if (mbar_try_wait(bar, parity))
-        return true;
-    const unsigned long long t0 = globaltimer();
-    while (true) {
-        if (mbar_try_wait(bar, parity))
-            return true;
-        if (*abort)
-            return false;
-        if (globaltimer() - t0 > kTimeoutNs) {
-            *abort = 1;
-            return false;
-        }
-    }
-}
-
-// Bulk copy global -> shared, completing on `bar`; `policy` is an L2 cache
-// policy (evict-first for data read exactly once).
-__device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t bytes, uint64_t *bar,
-                                         uint64_t policy)
-{
-    asm volatile(
-        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::"r"(
-            smem_addr(dst)),
-        "l"(src), "r"(bytes), "r"(smem_addr(bar)), "l"(policy)
-        : "memory");
-}
-
-__device__ __forceinline__ uint64_t evict_first_policy()
-{
-    uint64_t pol;
-    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
-    return pol;
-}
-
-__device__ __forceinline__ uint64_t evict_last_policy()
-{
-    uint64_t pol;
-    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
-    return pol;
-}
-
-// A plain load (not asm) so the compiler may schedule the loads of a group
-// together; the mbarrier waits carry "memory" clobbers, so none moves above
-// the wait that makes its stage valid.
-__device__ __forceinline__ uint4 lds128(const void *p) { return *reinterpret_cast<const uint4 *>(p); }
-
-__device__ __forceinline__ void st_stream_v4(void *p, uint4 v)
-{
-    asm volatile("st.global.cs.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z),
-                 "r"(v.w)
-                 : "memory");
-}
-
-__device__ __forceinline__ void st_stream_v2(void *p, uint2 v)
-{
-    asm volatile("st.global.cs.v2.u32 [%0], {%1, %2};" ::"l"(p), "r"(v.x), "r"(v.y) : "memory");
-}
-
-// RoPE on a bf16 pair: for each half, y * c + yp * sn with a single rounding
-// (the product yp * sn of two bf16 values is exact in fp32, formed as an FMA
-// with -0 so that a zero product keeps its sign).  The operands stay bf16:
-// the mixed-precision fma.rn.f32.bf16 reads register halves directly.
-__device__ __forceinline__ uint64_t rope_bf2(uint32_t y, uint32_t c, uint32_t yp, uint32_t sn)
-{
-    float lo, hi;
-    asm("{\n\t.reg .b16 y0, y1, c0, c1, p0, p1, s0, s1;\n\t.reg .f32 t0, t1;\n\t"
-        "mov.b32 {y0, y1}, %2;\n\tmov.b32 {c0, c1}, %3;\n\t"
-        "mov.b32 {p0, p1}, %4;\n\tmov.b32 {s0, s1}, %5;\n\t"
-        "fma.rn.f32.bf16 t0, p0, s0, 0f80000000;\n\t"
-        "fma.rn.f32.bf16 t1, p1, s1, 0f80000000;\n\t"
-        "fma.rn.f32.bf16 %0, y0, c0, t0;\n\t"
-        "fma.rn.f32.bf16 %1, y1, c1, t1;\n\t}"
-        : "=f"(lo), "=f"(hi)
-        : "r"(y), "r"(c), "r"(yp), "r"(sn));
-    return pr(lo, hi);
-}
 
 // Shared-memory layout (dynamic): barriers and headers, per-layer tables,
 // then the stages (128-byte aligned).
@@ -300,6 +172,11 @@ __global__ void __launch_bounds__(kThreads, 2) ctx_kv_tma_kernel(const TmaParams
     constexpr uint32_t kRowIn = 4 * D;          // bytes of one K|V row pair in all_kv
     constexpr int kCacheRow = FP8 ? 2 * D : 4 * D;  // bytes of one cache row
     constexpr bool kXor = ROT != 0;
+    // r = 32: K in the segmented mapping -- lane q holds dims 32k + 4q .. + 3
+    // (k = 0..3), so the rotated dims 0..31 are four on every lane of a row
+    // and each lane's first segment rotates with lane q ^ 4 (V keeps the
+    // 16-byte chunks)
+    constexpr bool kSeg = ROT == 32;
     extern __shared__ __align__(128) unsigned char smem[];
     const CtxKvParams &p = tp.p;
     const int L = p.num_layers, H = p.num_kv_heads, S = tp.stages, NP = tp.pieces, Lp = tp.layers_per_piece;
@@ -555,8 +432,10 @@ __global__ void __launch_bounds__(kThreads, 2) ctx_kv_tma_kernel(const TmaParams
         for (int i = tid; i < L * D; i += 32 * kConsumerWarps) {
             const int l = i / D, d = i % D;
             const int c = d / 8, j = d % 8;  // chunk c holds dims 8c .. 8c+7
-            reinterpret_cast<float *>(w1)[w1_slot<D>(l, j / 4, c) * 4 + (j % 4)] =
-                1.0f + __uint_as_float((uint32_t)__ldg(p.knorm_w + i) << 16);
+            // segmented mode (r = 32): dims in natural order, float4 slot
+            // l * D/4 + 8k + q holding the lane's dims 32k + 4q .. + 3
+            const int at = kSeg ? i : w1_slot<D>(l, j / 4, c) * 4 + (j % 4);
+            reinterpret_cast<float *>(w1)[at] = 1.0f + __uint_as_float((uint32_t)__ldg(p.knorm_w + i) << 16);
         }
         for (int l = tid; l < L; l += 32 * kConsumerWarps) {
             layer_base[l] = p.cache0 + __ldg(p.cache_offsets + l) * (FP8 ? 1 : 2);
@@ -604,43 +483,79 @@ __global__ void __launch_bounds__(kThreads, 2) ctx_kv_tma_kernel(const TmaParams
             const int ngroups = (R + 3) >> 2;
             const int first = (warp - gmod) & (kConsumerWarps - 1);  // this warp's first group here
             gmod = (gmod + ngroups) & (kConsumerWarps - 1);
-            if (first < ngroups) {
-                const unsigned char *stage = stages + (size_t)s * lay.stage_bytes;
-                // xor modes: cos and sign * sin (bf16 pairs) of this token for the lane's first 8 dims
+            if constexpr (kXor) {
+                // Early release: the warp copies its rows (at most two groups --
+                // a stage holds at most 64 rows of the pages' head dim) and the
+                // token's cos|sin words into registers, releases the stage so
+                // that the producer can refill it at once, then computes.
+                constexpr int kMaxG = 2;
+                uint4 kd[kMaxG][NC], vd[kMaxG][NC];
+                long long gdst[kMaxG];
+                int gl[kMaxG], gh[kMaxG];
+                bool gact[kMaxG];  // the lane's row exists in the group
                 uint32_t cw[4] = {0, 0, 0, 0}, sw[4] = {0, 0, 0, 0};
-                if constexpr (kXor) {
-                    if (rot_lane) {
+                const unsigned char *stage = stages + (size_t)s * lay.stage_bytes;
+                if (first < ngroups) {
+                    if constexpr (kSeg) {
+                        // the lane's 4 rotated dims 4q .. 4q+3: cos and sin of dims 4 (q & 3) .. + 3
+                        const unsigned char *cs = stage + lay.slab_bytes + 8 * (q & 3);
+                        const uint2 c2 = *reinterpret_cast<const uint2 *>(cs);
+                        const uint2 s2 = *reinterpret_cast<const uint2 *>(cs + ROT);
+                        const uint32_t flip = (q & 4) ? 0u : 0x80008000u;  // lower half subtracts
+                        cw[0] = c2.x, cw[1] = c2.y;
+                        sw[0] = s2.x ^ flip, sw[1] = s2.y ^ flip;
+                    } else if (rot_lane) {
                         const unsigned char *cs = stage + lay.slab_bytes + 16 * (q & (kPartner - 1));
                         const uint4 c4 = lds128(cs), s4 = lds128(cs + ROT);  // sin half: r/2 elements later
                         const uint32_t flip = (q & kPartner) ? 0u : 0x80008000u;  // lower half subtracts
                         cw[0] = c4.x, cw[1] = c4.y, cw[2] = c4.z, cw[3] = c4.w;
                         sw[0] = s4.x ^ flip, sw[1] = s4.y ^ flip, sw[2] = s4.z ^ flip, sw[3] = s4.w ^ flip;
                     }
-                } else {
-                    // the token's cos|sin row into this warp's slot, as 4-byte words (r is even)
-                    const uint32_t *src = reinterpret_cast<const uint32_t *>(p.cos_sin + h_s.pos * rdim);
-                    uint32_t *dst = reinterpret_cast<uint32_t *>(csw);
-                    for (int k = lane; k < half; k += 32)
-                        dst[k] = __ldg(src + k);
-                    __syncwarp();
+#pragma unroll
+                    for (int gi = 0; gi < kMaxG; gi++) {
+                        const int g = first + gi * kConsumerWarps;
+                        gact[gi] = false;
+                        gdst[gi] = -1;
+                        gl[gi] = gh[gi] = 0;
+                        if (g < ngroups) {
+                            const int row = g * 4 + rr;
+                            gact[gi] = row < R;
+                            const int rc = gact[gi] ? row : R - 1;
+                            const int lr = (int)(((uint64_t)(uint32_t)rc * tp.h_magic) >> 32);
+                            gh[gi] = rc - lr * H;
+                            gl[gi] = h_s.l0 + lr;
+                            gdst[gi] = PL ? pdst[s * Lp + lr] : h_s.dst;
+                            const unsigned char *krow = stage + ((size_t)(2 * lr) * H + gh[gi]) * (2 * D);
+                            const unsigned char *vrow = krow + (size_t)H * (2 * D);
+#pragma unroll
+                            for (int k = 0; k < NC; k++) {
+                                if constexpr (kSeg) {  // segments 2k, 2k + 1
+                                    const uint2 a = *reinterpret_cast<const uint2 *>(krow + 128 * k + 8 * q);
+                                    const uint2 b = *reinterpret_cast<const uint2 *>(krow + 128 * k + 64 + 8 * q);
+                                    kd[gi][k] = make_uint4(a.x, a.y, b.x, b.y);
+                                } else {
+                                    kd[gi][k] = lds128(krow + 128 * k + 16 * q);
+                                }
+                                vd[gi][k] = lds128(vrow + 128 * k + 16 * q);
+                            }
+                        }
+                    }
                 }
-                for (int g = first; g < ngroups; g += kConsumerWarps) {
-                    const int row = g * 4 + rr;
-                    const bool active = row < R;
-                    const int rc = active ? row : R - 1;
-                    const int lr = (int)(((uint64_t)(uint32_t)rc * tp.h_magic) >> 32);
-                    const int h = rc - lr * H;
-                    const int l = h_s.l0 + lr;
-                    const unsigned char *krow = stage + ((size_t)(2 * lr) * H + h) * (2 * D);
-                    const unsigned char *vrow = krow + (size_t)H * (2 * D);
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(empty + s);
+#pragma unroll
+                for (int gi = 0; gi < kMaxG; gi++) {
+                    if (first + gi * kConsumerWarps >= ngroups)
+                        break;  // warp-uniform
+                    const int l = gl[gi], h = gh[gi];
                     uint64_t x2[4 * NC];
 #pragma unroll
                     for (int k = 0; k < NC; k++) {
-                        const uint4 a = lds128(krow + 128 * k + 16 * q);
+                        const uint4 a = kd[gi][k];
                         x2[4 * k] = bf2_to_f2(a.x), x2[4 * k + 1] = bf2_to_f2(a.y);
                         x2[4 * k + 2] = bf2_to_f2(a.z), x2[4 * k + 3] = bf2_to_f2(a.w);
                     }
-                    // sum of squares: two accumulator chains of packed FMAs
                     uint64_t a0 = mul2(x2[0], x2[0]), a1 = mul2(x2[1], x2[1]);
 #pragma unroll
                     for (int j = 2; j < 4 * NC; j += 2) {
@@ -656,68 +571,65 @@ __global__ void __launch_bounds__(kThreads, 2) ctx_kv_tma_kernel(const TmaParams
                     float inv;  // ss/D + eps >= eps > 0 (hardware reciprocal square root)
                     asm("rsqrt.approx.ftz.f32 %0, %1;" : "=f"(inv) : "f"(fmaf(ss, 1.0f / D, p.eps)));
                     const uint64_t inv2 = pr(inv, inv);
-                    // y = bf16((k * inv) * (1 + w))
-                    uint32_t y[4 * NC];
+                    uint32_t ko[4 * NC];
 #pragma unroll
                     for (int k = 0; k < NC; k++) {
-                        const float4 wa = w1[w1_slot<D>(l, 0, 8 * k + q)], wb = w1[w1_slot<D>(l, 1, 8 * k + q)];
-                        y[4 * k] = f2_to_bf2(mul2(mul2(x2[4 * k], inv2), pr(wa.x, wa.y)));
-                        y[4 * k + 1] = f2_to_bf2(mul2(mul2(x2[4 * k + 1], inv2), pr(wa.z, wa.w)));
-                        y[4 * k + 2] = f2_to_bf2(mul2(mul2(x2[4 * k + 2], inv2), pr(wb.x, wb.y)));
-                        y[4 * k + 3] = f2_to_bf2(mul2(mul2(x2[4 * k + 3], inv2), pr(wb.z, wb.w)));
+                        float4 wa, wb;
+                        if constexpr (kSeg) {
+                            wa = w1[l * (D / 4) + 16 * k + q];      // dims 64k + 4q .. + 3 (segment 2k)
+                            wb = w1[l * (D / 4) + 16 * k + 8 + q];  // segment 2k + 1
+                        } else {
+                            wa = w1[w1_slot<D>(l, 0, 8 * k + q)], wb = w1[w1_slot<D>(l, 1, 8 * k + q)];
+                        }
+                        ko[4 * k] = f2_to_bf2(mul2(mul2(x2[4 * k], inv2), pr(wa.x, wa.y)));
+                        ko[4 * k + 1] = f2_to_bf2(mul2(mul2(x2[4 * k + 1], inv2), pr(wa.z, wa.w)));
+                        ko[4 * k + 2] = f2_to_bf2(mul2(mul2(x2[4 * k + 2], inv2), pr(wb.x, wb.y)));
+                        ko[4 * k + 3] = f2_to_bf2(mul2(mul2(x2[4 * k + 3], inv2), pr(wb.z, wb.w)));
                     }
-                    uint32_t ko[4 * NC];
-                    if constexpr (kXor) {
-                        // RoPE on the first chunk (dims 8q .. 8q+7); the partner is kPartner lanes away
+                    if constexpr (kSeg) {
+                        // segment 0 (dims 4q .. 4q+3) rotates on every lane; the partner is 4 lanes away
+#pragma unroll
+                        for (int j = 0; j < 2; j++) {
+                            const uint32_t yp = __shfl_xor_sync(0xffffffffu, ko[j], 4);
+                            ko[j] = f2_to_bf2(rope_bf2(ko[j], cw[j], yp, sw[j]));
+                        }
+                    } else {
 #pragma unroll
                         for (int j = 0; j < 4; j++) {
-                            const uint32_t yp = __shfl_xor_sync(0xffffffffu, y[j], kPartner);
-                            const uint32_t rv = f2_to_bf2(rope_bf2(y[j], cw[j], yp, sw[j]));
-                            ko[j] = rot_lane ? rv : y[j];  // both computed: a select, not a branch
-                        }
-#pragma unroll
-                        for (int j = 4; j < 4 * NC; j++)
-                            ko[j] = y[j];
-                    } else {
-                        // the normed row into the warp's scratch (the row's 8 lanes own it; the
-                        // previous group's partner reads are done first), then each rotated dim
-                        // d reads its partner d +- r/2 there
-                        __syncwarp();
-#pragma unroll
-                        for (int k = 0; k < NC; k++)
-#pragma unroll
-                            for (int w = 0; w < 4; w++)  // 4-byte stores: the rows are only 4-byte aligned
-                                reinterpret_cast<uint32_t *>(yrow + 64 * k + 8 * q)[w] = y[4 * k + w];
-                        __syncwarp();
-#pragma unroll
-                        for (int k = 0; k < NC; k++) {
-                            const int d0 = 64 * k + 8 * q;
-#pragma unroll
-                            for (int j = 0; j < 4; j++) {
-                                ko[4 * k + j] = y[4 * k + j];
-                                if (d0 + 2 * j < rdim) {
-                                    float o[2];
-#pragma unroll
-                                    for (int b = 0; b < 2; b++) {
-                                        const int d = d0 + 2 * j + b;  // d < r: r is even
-                                        const bool lower = d < half;
-                                        const int fi = lower ? d : d - half;
-                                        const float yd = __uint_as_float(b ? (y[4 * k + j] & 0xffff0000u)
-                                                                           : (y[4 * k + j] << 16));
-                                        const float c = __uint_as_float((uint32_t)csw[fi] << 16);
-                                        const float sn = __uint_as_float((uint32_t)csw[half + fi] << 16);
-                                        const float yp = __uint_as_float((uint32_t)yrow[lower ? d + half : d - half] << 16);
-                                        o[b] = fmaf(yd, c, lower ? -(yp * sn) : yp * sn);
-                                    }
-                                    ko[4 * k + j] = pack_bf16x2(o[0], o[1]);
-                                }
-                            }
+                            const uint32_t yp = __shfl_xor_sync(0xffffffffu, ko[j], kPartner);
+                            const uint32_t rv = f2_to_bf2(rope_bf2(ko[j], cw[j], yp, sw[j]));
+                            ko[j] = rot_lane ? rv : ko[j];  // both computed: a select, not a branch
                         }
                     }
-                    const long long roff = PL ? pdst[s * Lp + lr] : h_s.dst;
-                    if (!active || roff < 0)
+                    if (!gact[gi] || gdst[gi] < 0)
                         continue;  // past the stage's rows, or a layer padded in its own mapping
-                    unsigned char *dg = layer_base[l] + roff + h * head_bytes;
+                    unsigned char *dg = layer_base[l] + gdst[gi] + h * head_bytes;
+                    if constexpr (kSeg) {
+                        // K: 4 dims per segment, 4 segments; V: 16-byte chunks
+                        if (!FP8) {
+#pragma unroll
+                            for (int k = 0; k < 4; k++)
+                                st_stream_v2(dg + 64 * k + 8 * q, make_uint2(ko[2 * k], ko[2 * k + 1]));
+#pragma unroll
+                            for (int k = 0; k < NC; k++)
+                                st_stream_v4(dg + 2 * D + 128 * k + 16 * q, vd[gi][k]);
+                        } else {
+                            const ulonglong2 sv = reinterpret_cast<const ulonglong2 *>(scl + 12 * l)[0];
+                            const ulonglong2 nv = reinterpret_cast<const ulonglong2 *>(scl + 12 * l)[1];
+                            const uint2 b2 = *reinterpret_cast<const uint2 *>(scl + 12 * l + 8);
+#pragma unroll
+                            for (int k = 0; k < NC; k++) {
+                                const uint2 c = quantise8(
+                                    make_uint4(ko[4 * k], ko[4 * k + 1], ko[4 * k + 2], ko[4 * k + 3]), b2.x, sv.x, nv.x);
+                                st_stream_v1(dg + 64 * k + 4 * q, c.x);
+                                st_stream_v1(dg + 64 * k + 32 + 4 * q, c.y);
+                            }
+#pragma unroll
+                            for (int k = 0; k < NC; k++)
+                                st_stream_v2(dg + D + 64 * k + 8 * q, quantise8(vd[gi][k], b2.y, sv.y, nv.y));
+                        }
+                        continue;
+                    }
                     if (!FP8) {
 #pragma unroll
                         for (int k = 0; k < NC; k++)
@@ -725,26 +637,144 @@ __global__ void __launch_bounds__(kThreads, 2) ctx_kv_tma_kernel(const TmaParams
                                                                           ko[4 * k + 3]));
 #pragma unroll
                         for (int k = 0; k < NC; k++)
-                            st_stream_v4(dg + 2 * D + 128 * k + 16 * q, lds128(vrow + 128 * k + 16 * q));
+                            st_stream_v4(dg + 2 * D + 128 * k + 16 * q, vd[gi][k]);
                     } else {
                         const ulonglong2 sv = reinterpret_cast<const ulonglong2 *>(scl + 12 * l)[0];
                         const ulonglong2 nv = reinterpret_cast<const ulonglong2 *>(scl + 12 * l)[1];
                         const uint2 b2 = *reinterpret_cast<const uint2 *>(scl + 12 * l + 8);
-                        const uint64_t ks2 = sv.x, vs2 = sv.y, kn2 = nv.x, vn2 = nv.y;
 #pragma unroll
                         for (int k = 0; k < NC; k++)
                             st_stream_v2(dg + 64 * k + 8 * q,
                                          quantise8(make_uint4(ko[4 * k], ko[4 * k + 1], ko[4 * k + 2], ko[4 * k + 3]),
-                                                   b2.x, ks2, kn2));
+                                                   b2.x, sv.x, nv.x));
 #pragma unroll
                         for (int k = 0; k < NC; k++)
-                            st_stream_v2(dg + D + 64 * k + 8 * q, quantise8(lds128(vrow + 128 * k + 16 * q), b2.y, vs2, vn2));
+                            st_stream_v2(dg + D + 64 * k + 8 * q, quantise8(vd[gi][k], b2.y, sv.y, nv.y));
                     }
                 }
+            } else {
+                if (first < ngroups) {
+                    // any other even rotary dim: partners through the warp's shared row
+                    const unsigned char *stage = stages + (size_t)s * lay.stage_bytes;
+                    {
+                        // the token's cos|sin row into this warp's slot, as 4-byte words (r is even)
+                        const uint32_t *src = reinterpret_cast<const uint32_t *>(p.cos_sin + h_s.pos * rdim);
+                        uint32_t *dst = reinterpret_cast<uint32_t *>(csw);
+                        for (int k = lane; k < half; k += 32)
+                            dst[k] = __ldg(src + k);
+                        __syncwarp();
+                    }
+                    for (int g = first; g < ngroups; g += kConsumerWarps) {
+                        const int row = g * 4 + rr;
+                        const bool active = row < R;
+                        const int rc = active ? row : R - 1;
+                        const int lr = (int)(((uint64_t)(uint32_t)rc * tp.h_magic) >> 32);
+                        const int h = rc - lr * H;
+                        const int l = h_s.l0 + lr;
+                        const unsigned char *krow = stage + ((size_t)(2 * lr) * H + h) * (2 * D);
+                        const unsigned char *vrow = krow + (size_t)H * (2 * D);
+                        uint64_t x2[4 * NC];
+#pragma unroll
+                        for (int k = 0; k < NC; k++) {
+                            const uint4 a = lds128(krow + 128 * k + 16 * q);
+                            x2[4 * k] = bf2_to_f2(a.x), x2[4 * k + 1] = bf2_to_f2(a.y);
+                            x2[4 * k + 2] = bf2_to_f2(a.z), x2[4 * k + 3] = bf2_to_f2(a.w);
+                        }
+                        // sum of squares: two accumulator chains of packed FMAs
+                        uint64_t a0 = mul2(x2[0], x2[0]), a1 = mul2(x2[1], x2[1]);
+#pragma unroll
+                        for (int j = 2; j < 4 * NC; j += 2) {
+                            a0 = fma2(x2[j], x2[j], a0);
+                            a1 = fma2(x2[j + 1], x2[j + 1], a1);
+                        }
+                        float slo, shi;
+                        unpr(add2(a0, a1), slo, shi);
+                        float ss = slo + shi;
+                        ss += __shfl_xor_sync(0xffffffffu, ss, 4);
+                        ss += __shfl_xor_sync(0xffffffffu, ss, 2);
+                        ss += __shfl_xor_sync(0xffffffffu, ss, 1);
+                        float inv;  // ss/D + eps >= eps > 0 (hardware reciprocal square root)
+                        asm("rsqrt.approx.ftz.f32 %0, %1;" : "=f"(inv) : "f"(fmaf(ss, 1.0f / D, p.eps)));
+                        const uint64_t inv2 = pr(inv, inv);
+                        // y = bf16((k * inv) * (1 + w))
+                        uint32_t y[4 * NC];
+#pragma unroll
+                        for (int k = 0; k < NC; k++) {
+                            const float4 wa = w1[w1_slot<D>(l, 0, 8 * k + q)], wb = w1[w1_slot<D>(l, 1, 8 * k + q)];
+                            y[4 * k] = f2_to_bf2(mul2(mul2(x2[4 * k], inv2), pr(wa.x, wa.y)));
+                            y[4 * k + 1] = f2_to_bf2(mul2(mul2(x2[4 * k + 1], inv2), pr(wa.z, wa.w)));
+                            y[4 * k + 2] = f2_to_bf2(mul2(mul2(x2[4 * k + 2], inv2), pr(wb.x, wb.y)));
+                            y[4 * k + 3] = f2_to_bf2(mul2(mul2(x2[4 * k + 3], inv2), pr(wb.z, wb.w)));
+                        }
+                        uint32_t ko[4 * NC];
+                        {
+                            // the normed row into the warp's scratch (the row's 8 lanes own it; the
+                            // previous group's partner reads are done first), then each rotated dim
+                            // d reads its partner d +- r/2 there
+                            __syncwarp();
+#pragma unroll
+                            for (int k = 0; k < NC; k++)
+#pragma unroll
+                                for (int w = 0; w < 4; w++)  // 4-byte stores: the rows are only 4-byte aligned
+                                    reinterpret_cast<uint32_t *>(yrow + 64 * k + 8 * q)[w] = y[4 * k + w];
+                            __syncwarp();
+#pragma unroll
+                            for (int k = 0; k < NC; k++) {
+                                const int d0 = 64 * k + 8 * q;
+#pragma unroll
+                                for (int j = 0; j < 4; j++) {
+                                    ko[4 * k + j] = y[4 * k + j];
+                                    if (d0 + 2 * j < rdim) {
+                                        float o[2];
+#pragma unroll
+                                        for (int b = 0; b < 2; b++) {
+                                            const int d = d0 + 2 * j + b;  // d < r: r is even
+                                            const bool lower = d < half;
+                                            const int fi = lower ? d : d - half;
+                                            const float yd = __uint_as_float(b ? (y[4 * k + j] & 0xffff0000u)
+                                                                               : (y[4 * k + j] << 16));
+                                            const float c = __uint_as_float((uint32_t)csw[fi] << 16);
+                                            const float sn = __uint_as_float((uint32_t)csw[half + fi] << 16);
+                                            const float yp = __uint_as_float((uint32_t)yrow[lower ? d + half : d - half] << 16);
+                                            o[b] = fmaf(yd, c, lower ? -(yp * sn) : yp * sn);
+                                        }
+                                        ko[4 * k + j] = pack_bf16x2(o[0], o[1]);
+                                    }
+                                }
+                            }
+                        }
+                        const long long roff = PL ? pdst[s * Lp + lr] : h_s.dst;
+                        if (!active || roff < 0)
+                            continue;  // past the stage's rows, or a layer padded in its own mapping
+                        unsigned char *dg = layer_base[l] + roff + h * head_bytes;
+                        if (!FP8) {
+#pragma unroll
+                            for (int k = 0; k < NC; k++)
+                                st_stream_v4(dg + 128 * k + 16 * q, make_uint4(ko[4 * k], ko[4 * k + 1], ko[4 * k + 2],
+                                                                              ko[4 * k + 3]));
+#pragma unroll
+                            for (int k = 0; k < NC; k++)
+                                st_stream_v4(dg + 2 * D + 128 * k + 16 * q, lds128(vrow + 128 * k + 16 * q));
+                        } else {
+                            const ulonglong2 sv = reinterpret_cast<const ulonglong2 *>(scl + 12 * l)[0];
+                            const ulonglong2 nv = reinterpret_cast<const ulonglong2 *>(scl + 12 * l)[1];
+                            const uint2 b2 = *reinterpret_cast<const uint2 *>(scl + 12 * l + 8);
+                            const uint64_t ks2 = sv.x, vs2 = sv.y, kn2 = nv.x, vn2 = nv.y;
+#pragma unroll
+                            for (int k = 0; k < NC; k++)
+                                st_stream_v2(dg + 64 * k + 8 * q,
+                                             quantise8(make_uint4(ko[4 * k], ko[4 * k + 1], ko[4 * k + 2], ko[4 * k + 3]),
+                                                       b2.x, ks2, kn2));
+#pragma unroll
+                            for (int k = 0; k < NC; k++)
+                                st_stream_v2(dg + D + 64 * k + 8 * q, quantise8(lds128(vrow + 128 * k + 16 * q), b2.y, vs2, vn2));
+                        }
+                    }
+                }
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(empty + s);
             }
-            __syncwarp();
-            if (lane == 0)
-                mbar_arrive(empty + s);
         }
         __syncwarp();
         __syncthreads();

@@ -21,14 +21,15 @@ from parity import (alt_index_rows, compare_caches, compare_rows, device_inputs,
 pytestmark = pytest.mark.gpu
 
 
-@pytest.fixture(params=["pipelined", "generic"])
+@pytest.fixture(params=["default", "warp", "generic"])
 def kernel(request, monkeypatch):
-    """Run the test on the pipelined bulk-copy kernel (the default where the
-    shape allows) and on the generic kernel."""
-    if request.param == "generic":
-        monkeypatch.setenv("DSPARK_CTX_KV_KERNEL", "generic")
-    else:
+    """Run the test on the kernel the library picks (the pipelined bulk-copy
+    kernel where the shape allows), on the warp-private pipelines (where
+    they apply; elsewhere the default) and on the generic kernel."""
+    if request.param == "default":
         monkeypatch.delenv("DSPARK_CTX_KV_KERNEL", raising=False)
+    else:
+        monkeypatch.setenv("DSPARK_CTX_KV_KERNEL", request.param)
     return request.param
 
 

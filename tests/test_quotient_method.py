@@ -1,21 +1,20 @@
 """The fp8 path's quotient method against IEEE division, on the CPU.
 
-The pipelined kernel forms x / scale (the fp8 store's "x / scale", vLLM
+The pipelined kernels form x / scale (the fp8 store's "x / scale", vLLM
 DSpark context-KV writer page, module docstring) with Markstein's FMA
-correction of a reciprocal-multiplied quotient, on the negated reciprocal
-n = -RN(1/s) and on x clamped in magnitude to a bound X >= 448 s (the bf16
-value just above 512 s; sign and NaN kept, so every clamped quotient still
-saturates):
-    x' = clamp(x),  p0 = x' * n,  e = p0*s + x'  (exact by FMA),
-    p = p0 + e*n  = -(x'/s) correctly rounded,  code = e4m3(p) ^ 0x80.
+correction of a reciprocal-multiplied quotient.  x is clamped in magnitude to
+a bound B >= 448 s (the bf16 value just above 512 s, so every clamped
+quotient still saturates) and negated in the same instruction (min.xorsign.abs
+against -B; NaN kept); with the negated reciprocal n = -RN(1/s):
+    x' = -sign(x) min(|x|, B),  p0 = x' * n,  e = p0*s + x'  (exact by FMA),
+    p = p0 + e*n  = -(x'/s) correctly rounded,  code = e4m3(p).
 This test runs the same operations in C (the C library's correctly rounded
 fmaf) for every bf16 value x, including +-0, subnormals, +-inf and NaN, and
 many fp32 scales, and checks that
   * that code equals the e4m3 code (RNE, saturating, the oracle's encoder)
-    of the IEEE quotient x / s -- so the kernel's fp8 codes can be bit-exact
-    with the oracle's true division (NaN inputs excepted: they give the
-    negative NaN code 0xFF rather than 0x7F; both are e4m3 NaN);
-  * -p is the correctly rounded quotient wherever |x| and |x / s| are at
+    of the IEEE quotient x / s -- so the kernels' fp8 codes can be bit-exact
+    with the oracle's true division, signed zeros and NaN included;
+  * p is the correctly rounded quotient wherever |x| and |x / s| are at
     least 2^-90 and x is not clamped (below, the FMA residual underflows;
     those quotients are far below e4m3's smallest step and encode to a zero
     of the right sign either way).
@@ -38,9 +37,9 @@ SRC = r"""
 uint8_t dspark_oracle_e4m3_rne_sat(float xf);
 static float bf(uint16_t b) { uint32_t u = (uint32_t)b << 16; float f; memcpy(&f, &u, 4); return f; }
 static uint32_t bits(float f) { uint32_t u; memcpy(&u, &f, 4); return u; }
-static float clamp_mag(float v, float bound) {   /* min.NaN.xorsign.abs(v, bound) */
+static float clamp_neg(float v, float bound) {   /* min.NaN.xorsign.abs(v, -bound) */
     if (isnan(v)) return v;
-    return copysignf(fminf(fabsf(v), bound), v);
+    return copysignf(fminf(fabsf(v), bound), -v);
 }
 static float bf16_up(float v) {  /* smallest bf16 >= v > 0 */
     uint32_t u = bits(v);
@@ -59,14 +58,13 @@ void check(const float *scales, int ns, long long *bad_code, long long *bad_q, l
             const float x = bf((uint16_t)b);
             const volatile float xv = x;
             const float want = xv / s;
-            const float xc = clamp_mag(x, bound);
+            const float xc = clamp_neg(x, bound);
             const float p0 = xc * n;
             const float e = fmaf(p0, s, xc);
-            const float p = fmaf(e, n, p0);
-            const float q = -p;
-            const uint8_t code = dspark_oracle_e4m3_rne_sat(p) ^ 0x80;
+            const float q = fmaf(e, n, p0);
+            const uint8_t code = dspark_oracle_e4m3_rne_sat(q);
             const uint8_t want_code = dspark_oracle_e4m3_rne_sat(want);
-            if (code != want_code && !(isnan(x) && code == 0xFF && want_code == 0x7F)) {
+            if (code != want_code) {
                 if (*first < 0) *first = (long long)j << 16 | b;
                 (*bad_code)++;
             }

@@ -44,8 +44,8 @@ METRIC = "context-KV write GB/s and rows/s on 1 GB300; % of HBM roofline"
 UNIT = "GB/s"
 # sources of the write kernels and of the host layer that picks one
 KERNEL_SRCS = [os.path.join(ROOT, "speculative_decoding_draft_ctx_gb300", "csrc", f)
-               for f in ("ctx_kv_tma.cu", "ctx_kv_kernel.cu", "ctx_kv_general.cu", "ctx_kv_api.cpp",
-                         "ctx_kv_internal.h", "ctx_kv_device.cuh")]
+               for f in ("ctx_kv_tma.cu", "ctx_kv_kernel.cu", "ctx_kv_general.cu", "ctx_kv_warp.cu",
+                         "ctx_kv_api.cpp", "ctx_kv_internal.h", "ctx_kv_device.cuh", "ctx_kv_pipe.cuh")]
 QK_METRIC = "draft-token QK-norm/RoPE/KV-insert GB/s on 1 GB300; % of HBM roofline"
 PROJ_METRIC = "fused context-KV projection + write TFLOP/s on 1 GB300; % of bf16 tensor roofline"
 NORM_METRIC = "context-state Gemma RMSNorm GB/s on 1 GB300; % of HBM roofline"
@@ -73,8 +73,11 @@ def parse_args(argv=None):
     ap.add_argument("--num-ctx", type=int, default=None,
                     help="run a smaller case of the workload (profiling captures): fewer tokens")
     ap.add_argument("--num-blocks", type=int, default=None, help="with --num-ctx: fewer cache blocks")
-    ap.add_argument("--graph", action="store_true",
-                    help="replay the timed steps from one CUDA graph (launch-bound small workloads)")
+    ap.add_argument("--events", action="store_true",
+                    help="context write: time each launch on its own between two CUDA events (isolated "
+                         "launches, each paying its own ramp-up and drain) instead of replaying the timed "
+                         "steps back to back from one CUDA graph")
+    ap.add_argument("--graph", action="store_true", help="accepted for compatibility: the default")
     ap.add_argument("--layer-slots", type=int, default=0, metavar="G",
                     help="context write: layers split over G KV-cache groups, one slot mapping per group")
     return ap.parse_args(argv)
@@ -469,8 +472,10 @@ def run_ours(args):
     t_begin = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
     graph = None
-    if args.graph:
-        # the timed steps as one graph: one launch per step, no host gaps
+    if not args.events:
+        # the timed steps as one graph: one launch per step back to back, no
+        # host gaps (each launch's prologue overlaps the previous one's drain,
+        # as in a serving step); --events times isolated launches instead
         side = torch.cuda.Stream()
         side.wait_stream(stream)
         graph = torch.cuda.CUDAGraph()
@@ -519,37 +524,64 @@ def run_ours(args):
         h_kv = host.all_kv.pin_memory()
         h_pos = host.positions.pin_memory()
         h_slot = host.slot_mapping.pin_memory()
-        d = sets[0]
+        # two device input sets: step i+1's host-to-device copies (on a copy
+        # stream) run while step i's write runs on the compute stream
+        s0 = sets[0]
+        bufs = [s0, sets[1] if n_sets > 1 else
+                wk.Inputs(wl, s0.all_kv.clone(), s0.knorm_w, s0.positions.clone(), s0.slot_mapping.clone(),
+                          s0.cos_sin, s0.k_scale, s0.v_scale, s0.eps)]
+        copy_stream = torch.cuda.Stream()
+        copied = [torch.cuda.Event() for _ in range(2)]
+        consumed = [torch.cuda.Event() for _ in range(2)]
         flags = torch.zeros(1, dtype=torch.int32, device=dev)
         h_flags = torch.zeros(1, dtype=torch.int32).pin_memory()
         ne = max(1, args.e2e_steps)
+        h2d_bytes = h_kv.numel() * 2 + h_pos.numel() * 8 + h_slot.numel() * 8
 
-        def e2e_step():
-            d.all_kv.copy_(h_kv, non_blocking=True)
-            d.positions.copy_(h_pos, non_blocking=True)
-            d.slot_mapping.copy_(h_slot, non_blocking=True)
+        def e2e_step(i):
+            d = bufs[i % 2]
+            with torch.cuda.stream(copy_stream):
+                copy_stream.wait_event(consumed[i % 2])  # the write two steps back is done with this set
+                d.all_kv.copy_(h_kv, non_blocking=True)
+                d.positions.copy_(h_pos, non_blocking=True)
+                d.slot_mapping.copy_(h_slot, non_blocking=True)
+                copied[i % 2].record(copy_stream)
+            stream.wait_event(copied[i % 2])
             writer(d.all_kv, d.knorm_w, d.eps, d.positions, d.cos_sin, wl.rotary_dim, d.slot_mapping,
                    error_flags=flags)
+            consumed[i % 2].record(stream)
             h_flags.copy_(flags, non_blocking=True)
 
-        for _ in range(3):
-            e2e_step()
+        for e in consumed:
+            e.record(stream)
+        for i in range(3):
+            e2e_step(i)
         torch.cuda.synchronize()
+        # the host-to-device rate alone, for context
+        c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        c0.record(stream)
+        for i in range(3):
+            bufs[i % 2].all_kv.copy_(h_kv, non_blocking=True)
+        c1.record(stream)
+        torch.cuda.synchronize()
+        h2d_gbs = 3 * h_kv.numel() * 2 / (c0.elapsed_time(c1) * 1e-3) / 1e9
         if pg:
             pg.barrier()
         e0 = torch.cuda.Event(enable_timing=True)
         e1 = torch.cuda.Event(enable_timing=True)
         e0.record(stream)
-        for _ in range(ne):
-            e2e_step()
+        copy_stream.wait_event(e0)
+        for i in range(ne):
+            e2e_step(i)
+        stream.wait_stream(copy_stream)
         e1.record(stream)
         torch.cuda.synchronize()
         e_ms = max_over_ranks(e0.elapsed_time(e1), pg, dev)
         if int(h_flags.item()) != 0:
             raise RuntimeError(f"write reported error flags {int(h_flags.item())}")
         e2e = {"value": whole_job_rate(step_bytes, ne, ws, e_ms) / 1e9, "unit": UNIT,
-               "h2d_bytes_per_step": h_kv.numel() * 2 + h_pos.numel() * 8 + h_slot.numel() * 8,
-               "d2h_bytes_per_step": 4, "steps": ne, "ms_per_step": e_ms / ne}
+               "h2d_bytes_per_step": h2d_bytes, "d2h_bytes_per_step": 4, "steps": ne, "ms_per_step": e_ms / ne,
+               "h2d_gbs_alone": h2d_gbs, "overlap": "step i+1's copies on a copy stream during step i's write"}
 
     cpu = None
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:

@@ -13,6 +13,7 @@
 // the write fused into it).
 #include "../../include/dspark_ctx_kv.h"
 
+#include <algorithm>
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
@@ -53,6 +54,18 @@ bool force_kernel(const char *name)
 {
     const char *e = std::getenv("DSPARK_CTX_KV_KERNEL");
     return e && std::strcmp(e, name) == 0;
+}
+
+// DSPARK_TEST_HOLD_NS=<ns> (tests of the timeout path only): the pipelined
+// kernel's producer first waits that long on a device word that nothing
+// sets, then stops as on any expired wait and reports DSPARK_FLAG_TIMEOUT.
+uint64_t test_hold_ns()
+{
+    const char *e = std::getenv("DSPARK_TEST_HOLD_NS");
+    if (!e)
+        return 0;
+    const long long v = std::atoll(e);
+    return v > 0 ? (uint64_t)std::min(v, 1000000000LL) : 0;
 }
 
 bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
@@ -247,6 +260,7 @@ int write_common(const void *all_kv, const void *knorm_w, const int64_t *positio
     p.block_size = block_size;
     if (!pow2(block_size))
         block_divisor(block_size, &p.bs_magic, &p.bs_magic_shift);
+    p.test_hold_ns = test_hold_ns();
     const bool fp8 = kv_dtype == DSPARK_KV_FP8_E4M3;
     // the pipelined kernel where its stage holds a token's rows; else the
     // generic kernel (the pages' layouts) or the general one (any other)

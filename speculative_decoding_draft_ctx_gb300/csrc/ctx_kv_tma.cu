@@ -86,6 +86,10 @@ constexpr unsigned kFlagPos = 0x2u;
 constexpr unsigned kFlagTimeout = 0x4u;
 constexpr int kMaxTmaLayers = 32;
 
+// A device word that nothing ever sets: the test hook's wait (test_hold_ns)
+// runs out on it.
+__device__ unsigned g_never_set = 0;
+
 // What the producer tells the consumers about a stage.
 struct StageHdr {
     long long dst;  // byte offset of the token's row for head 0 within a layer's cache
@@ -317,6 +321,19 @@ __global__ void __launch_bounds__(kThreads, 2) ctx_kv_tma_kernel(const TmaParams
         int nspec = 0;
         for (long long u = u_first; u < u_end && nspec < S; u += step)
             nspec++;
+        if (p.test_hold_ns) {
+            // test hook: a bounded wait on a word nothing sets, which runs out;
+            // the CTA then stops before issuing anything
+            if (lane == 0) {
+                const unsigned long long t0 = globaltimer();
+                while (*reinterpret_cast<volatile unsigned *>(&g_never_set) == 0 &&
+                       globaltimer() - t0 < p.test_hold_ns) {
+                }
+                *abort = 1;
+            }
+            ok = false;
+            nspec = 0;
+        }
         if (lane == 0) {
             for (int i = 0; i < nspec; i++) {
                 long long t;
@@ -331,7 +348,8 @@ __global__ void __launch_bounds__(kThreads, 2) ctx_kv_tma_kernel(const TmaParams
         long long base = u_first;
         long long ordinal = 0;  // index of unit `base` in this CTA's sequence
         int buf = 0;            // prefetch-table buffer of the batch at `base`
-        fetch(base, cur_slot, cur_pos, buf);
+        if (ok)
+            fetch(base, cur_slot, cur_pos, buf);
         for (; base < u_end && ok; base += 32 * step, ordinal += 32, buf ^= 1) {
             const long long nbase = base + 32 * step;
             if (nbase < u_end)

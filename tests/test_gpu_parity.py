@@ -353,3 +353,33 @@ def test_writer_validation_on_device_tensors(oracle_lib):
     nc = [torch.empty(8, 16, 2, 256, dtype=torch.bfloat16, device="cuda").transpose(1, 2) for _ in range(2)]
     assert not dk.ContextKVWriter.supported(nc, ks, ks, "auto")
     del wl
+
+
+def test_expired_wait_reports_timeout_and_leaves_the_context_usable(oracle_lib, monkeypatch):
+    """The timeout path of the pipelined kernel, exercised without a fault:
+    with the test hook DSPARK_TEST_HOLD_NS set, each CTA's producer first
+    waits 2 ms on a device word that nothing sets; the wait runs out, the CTA
+    stops before issuing any copy (its consumers see the abort and leave),
+    nothing is written, and DSPARK_FLAG_TIMEOUT reaches the caller's error
+    word -- or the writer's own word when the caller passes none.  The next
+    launch, hook off, matches the oracle: the context is still usable."""
+    import speculative_decoding_draft_ctx_gb300 as dk
+
+    wl = wk.WORKLOADS[2].with_(num_ctx=256, pad_count=12)
+    inp = wk.generate(wl)
+    monkeypatch.delenv("DSPARK_CTX_KV_KERNEL", raising=False)
+    monkeypatch.setenv("DSPARK_TEST_HOLD_NS", "2000000")
+    flags = torch.zeros(1, dtype=torch.int32, device="cuda")
+    caches, w, d = gpu_write(inp, error_flags=flags)
+    assert int(flags.item()) == dk.FLAG_TIMEOUT
+    for c in caches:
+        assert bool((c.view(torch.uint8) == 0xFF).all())
+    w(d.all_kv, d.knorm_w, d.eps, d.positions, d.cos_sin, wl.rotary_dim, d.slot_mapping)
+    assert w.error_flags() == dk.FLAG_TIMEOUT
+    assert w.error_flags() == 0  # read and cleared
+    monkeypatch.delenv("DSPARK_TEST_HOLD_NS")
+    flags.zero_()
+    caches, _, _ = gpu_write(inp, error_flags=flags)
+    assert int(flags.item()) == 0
+    _, o, alts = oracle_full(inp)
+    assert not compare_caches(to_numpy_caches(caches, True), o, alts, True)

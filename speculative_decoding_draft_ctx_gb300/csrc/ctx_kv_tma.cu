@@ -54,10 +54,12 @@
 //
 // Per-layer slot mappings (drafts whose layers span several KV-cache
 // groups): the producer prefetches each unit's per-layer slots one batch
-// ahead into a double-buffered shared table and writes a row offset per
-// layer into the stage (< 0: that layer is padding); a unit is copied when
-// any of its layers has a slot, and the consumers skip the padded layers'
-// rows.
+// ahead into a double-buffered shared table, where each lane turns its
+// unit's slots into row offsets (< 0: that layer is padding); when the unit
+// is issued, one lane per layer copies them into the stage, and only the
+// runs of layers that have a slot are copied from all_kv (a layer padded in
+// its own mapping is neither read nor written; the consumers skip its
+// rows).
 //
 // Every wait on an mbarrier is bounded (globaltimer); on expiry the CTA sets
 // DSPARK_FLAG_TIMEOUT, stops, waits (bounded) for its own copies in flight
@@ -101,7 +103,7 @@ struct StageHdr {
 // Shared-memory layout (dynamic): barriers and headers, per-layer tables,
 // then the stages (128-byte aligned).
 struct Layout {
-    uint32_t full, empty, hdr, abort, w1, off, scl, pls, pdst, csw, stages, stage_bytes, slab_bytes, total;
+    uint32_t full, empty, hdr, abort, w1, off, scl, pls, lsp, pdst, csw, stages, stage_bytes, slab_bytes, total;
 };
 
 __host__ __device__ inline uint32_t align_up(uint32_t v, uint32_t a) { return (v + a - 1) / a * a; }
@@ -132,6 +134,8 @@ __host__ __device__ inline Layout make_layout(int L, int S, uint32_t slab_bytes,
     o = y.scl + 48 * L;
     y.pls = align_up(o, 16);
     o = y.pls + 2 * 32 * 8 * pl;
+    y.lsp = align_up(o, 16);  // per layer: its slot mapping's address (per-layer mappings)
+    o = y.lsp + (pl ? 8 * L : 0);
     y.pdst = align_up(o, 16);
     o = y.pdst + 8 * S * pl;
     // per consumer warp (rotary dims other than 16/32/64): the token's cos|sin
@@ -195,6 +199,7 @@ __global__ void __launch_bounds__(kThreads, 2) ctx_kv_tma_kernel(const TmaParams
     unsigned char *stages = smem + lay.stages;
     long long *pls = reinterpret_cast<long long *>(smem + lay.pls);    // [2][32][Lp] prefetched per-layer slots
     long long *pdst = reinterpret_cast<long long *>(smem + lay.pdst);  // [S][Lp] per-layer row offsets (< 0: none)
+    const int64_t **lsp = reinterpret_cast<const int64_t **>(smem + lay.lsp);  // [L] per-layer slot mappings
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     if (tid == 0) {
@@ -254,19 +259,17 @@ __global__ void __launch_bounds__(kThreads, 2) ctx_kv_tma_kernel(const TmaParams
                 const long long t = NP == 1 ? u : u / NP;
                 pos = __ldg(p.positions + t);
                 if (PL) {
+                    // the unit's per-layer slots land in the prefetch table by
+                    // asynchronous copies (no register waits on them here);
+                    // vet() waits for them a batch later
                     const int l0 = (NP == 1 ? 0 : (int)(u - t * NP)) * Lp;
                     const int n = min(Lp, L - l0);
                     long long *e = pls + (buf * 32 + lane) * Lp;
-                    bool any = false;
-                    for (int j = 0; j < n; j++) {
-                        const long long sj = __ldg(reinterpret_cast<const int64_t *>(__ldg(
-                                                       reinterpret_cast<const unsigned long long *>(p.layer_slots) +
-                                                       l0 + j)) +
-                                                   t);
-                        e[j] = sj;
-                        any |= sj >= 0;
-                    }
-                    slot = any ? 0 : -1;
+                    for (int j = 0; j < n; j++)
+                        asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(smem_addr(e + j)),
+                                     "l"(lsp[l0 + j] + t)
+                                     : "memory");
+                    slot = 0;  // vet() decides
                 } else {
                     slot = __ldg(p.slot_mapping + t);
                 }
@@ -284,14 +287,17 @@ __global__ void __launch_bounds__(kThreads, 2) ctx_kv_tma_kernel(const TmaParams
             } else if (PL) {
                 const long long t = NP == 1 ? u : u / NP;
                 const int n = min(Lp, L - (NP == 1 ? 0 : (int)(u - t * NP)) * Lp);
-                long long *e = pls + (buf * 32 + lane) * Lp;
+                long long *e = pls + (buf * 32 + lane) * Lp;  // this lane's own copies (waited for below)
                 bool any = false;
+                // each layer's slot becomes its row offset here, one unit per
+                // lane, so the issuing lane only copies them
                 for (int j = 0; j < n; j++) {
                     if (e[j] >= p.capacity) {
                         flags |= kFlagSlot;
                         e[j] = -1;
                     }
                     any |= e[j] >= 0;
+                    e[j] = e[j] >= 0 ? row_off(e[j]) : -1;
                 }
                 if (!any)
                     slot = -1;
@@ -348,12 +354,28 @@ __global__ void __launch_bounds__(kThreads, 2) ctx_kv_tma_kernel(const TmaParams
         long long base = u_first;
         long long ordinal = 0;  // index of unit `base` in this CTA's sequence
         int buf = 0;            // prefetch-table buffer of the batch at `base`
-        if (ok)
+        if (PL) {  // the layers' slot mapping addresses, once
+            for (int j = lane; j < L; j += 32)
+                lsp[j] = reinterpret_cast<const int64_t *>(
+                    __ldg(reinterpret_cast<const unsigned long long *>(p.layer_slots) + j));
+            __syncwarp();
+        }
+        if (ok) {
             fetch(base, cur_slot, cur_pos, buf);
+            if (PL)
+                asm volatile("cp.async.commit_group;" ::: "memory");
+        }
         for (; base < u_end && ok; base += 32 * step, ordinal += 32, buf ^= 1) {
             const long long nbase = base + 32 * step;
-            if (nbase < u_end)
+            if (nbase < u_end) {
                 fetch(nbase, nxt_slot, nxt_pos, buf ^ 1);
+                if (PL) {
+                    asm volatile("cp.async.commit_group;" ::: "memory");
+                    asm volatile("cp.async.wait_group 1;" ::: "memory");  // this batch's, not the next one's
+                }
+            } else if (PL) {
+                asm volatile("cp.async.wait_group 0;" ::: "memory");
+            }
             vet(base, cur_slot, cur_pos, buf);
             __syncwarp();  // lane 0 reads the other lanes' prefetched slots below
             for (int i = 0; i < 32; i++) {
@@ -365,9 +387,29 @@ __global__ void __launch_bounds__(kThreads, 2) ctx_kv_tma_kernel(const TmaParams
                 const bool spec = ordinal + i < nspec;
                 if (slot < 0 && !spec)
                     continue;  // padding (or out of range): K|V not copied, nothing written
+                bool ready = true;
+                uint32_t vmask = 0;  // per-layer mappings: the unit's layers that have a slot
+                if constexpr (PL) {
+                    // the stage is free before its per-layer row offsets are
+                    // rewritten, one lane per layer; the ballot gives the mask of
+                    // the unit's layers that have a slot
+                    if (lane == 0)
+                        ready = spec || mbar_wait(empty + ps, pph ^ 1u, abort);
+                    ready = __shfl_sync(0xffffffffu, ready, 0);
+                    long long t_;
+                    int l0_;
+                    uint32_t slab_;
+                    unit_span(u, t_, l0_, slab_);
+                    const int n = (int)(slab_ / kRowIn) / H;
+                    const long long off = lane < n ? pls[(buf * 32 + i) * Lp + lane] : -1;
+                    if (ready && slot >= 0 && lane < n)
+                        pdst[ps * Lp + lane] = off;
+                    vmask = __ballot_sync(0xffffffffu, off >= 0);
+                    __syncwarp();
+                }
                 if (lane == 0) {
                     const int s = ps;
-                    ok = spec || mbar_wait(empty + s, pph ^ 1u, abort);
+                    ok = PL ? ready : spec || mbar_wait(empty + s, pph ^ 1u, abort);
                     if (ok) {
                         long long t;
                         int l0;
@@ -378,13 +420,8 @@ __global__ void __launch_bounds__(kThreads, 2) ctx_kv_tma_kernel(const TmaParams
                             hdr[s].rows = 0;  // a speculatively copied padded unit: dropped
                             mbar_arrive(full + s);
                         } else {
-                            if (PL) {
-                                const long long *e = pls + (buf * 32 + i) * Lp;
-                                for (int j = 0; j < (int)(slab / kRowIn) / H; j++)
-                                    pdst[s * Lp + j] = e[j] >= 0 ? row_off(e[j]) : -1;
-                            } else {
+                            if (!PL)
                                 hdr[s].dst = row_off(slot);
-                            }
                             hdr[s].l0 = l0;
                             hdr[s].pos = pos;
                             hdr[s].rows = (int)(slab / kRowIn);
@@ -396,6 +433,19 @@ __global__ void __launch_bounds__(kThreads, 2) ctx_kv_tma_kernel(const TmaParams
                                     mbar_arrive_expect_tx(full + s, cs_bytes);
                                 else
                                     mbar_arrive(full + s);
+                            } else if (PL) {
+                                // only the runs of layers that have a slot (bits of vmask): a
+                                // layer padded in its own mapping is neither read nor written
+                                const uint32_t layer_bytes = (uint32_t)H * kRowIn;
+                                mbar_arrive_expect_tx(full + s, (uint32_t)__popc(vmask) * layer_bytes + cs_bytes);
+                                for (uint32_t m = vmask; m;) {
+                                    const int j = __ffs(m) - 1;
+                                    // the run of set bits from j (64-bit: a run may hold all 32 layers)
+                                    const int len = __ffsll((long long)~((unsigned long long)m >> j)) - 1;
+                                    bulk_g2s(dst + (size_t)j * layer_bytes, p.all_kv + (t * L + l0 + j) * 2LL * H * D,
+                                             (uint32_t)len * layer_bytes, full + s, stream_once);
+                                    m &= ~(uint32_t)(((1ull << len) - 1ull) << j);
+                                }
                             } else {
                                 mbar_arrive_expect_tx(full + s, slab + cs_bytes);
                                 bulk_g2s(dst, p.all_kv + (t * L + l0) * 2LL * H * D, slab, full + s, stream_once);
@@ -417,6 +467,8 @@ __global__ void __launch_bounds__(kThreads, 2) ctx_kv_tma_kernel(const TmaParams
             cur_slot = nxt_slot;
             cur_pos = nxt_pos;
         }
+        if (PL)
+            asm volatile("cp.async.wait_group 0;" ::: "memory");  // no prefetch copy outlives the CTA
         uint32_t rounds = k;  // barrier rounds used, the sentinel included
         if (lane == 0) {
             if (ok) {

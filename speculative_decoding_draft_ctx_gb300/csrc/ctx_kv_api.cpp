@@ -43,13 +43,18 @@ int ok()
     return DSPARK_OK;
 }
 
-// Which kernel serves a call: the pipelined one where a token's rows fit a
-// stage, else the generic one for the pages' layouts; the general kernel for
-// every other layout.  DSPARK_CTX_KV_KERNEL=warp picks the warp-private
-// pipelines where they apply (the pages' layouts with 4 or 8 KV heads and a
-// shared slot mapping), =generic the generic kernel for the pages' layouts
-// and =general the general kernel for every layout, for the calls made while
-// it is set (all compute the same result; the tests run each).
+// Which kernel serves a call: for small calls (at most kWarpPathMaxTokens
+// tokens: draft steps) in the pages' layouts with 4 or 8 KV heads and a
+// shared slot mapping, the warp-private pipelines (every warp starts on its
+// own 4 KB unit at once: shorter chains than the shared stages give when a
+// CTA gets one or two tokens); otherwise the pipelined one where a token's
+// rows fit a stage, else the generic one for the pages' layouts; the general
+// kernel for every other layout.  DSPARK_CTX_KV_KERNEL=warp picks the
+// warp-private pipelines wherever they apply, =tma the pipelined kernel,
+// =generic the generic kernel for the pages' layouts and =general the
+// general kernel for every layout, for the calls made while it is set (all
+// compute the same result; the tests run each).
+constexpr int64_t kWarpPathMaxTokens = 1024;
 bool force_kernel(const char *name)
 {
     const char *e = std::getenv("DSPARK_CTX_KV_KERNEL");
@@ -271,7 +276,8 @@ int write_common(const void *all_kv, const void *knorm_w, const int64_t *positio
         e = dspark::launch_ctx_kv_general(p, head_dim, fp8, stream);
     else if (pages_layout && force_kernel("generic"))
         e = dspark::launch_ctx_kv_write(p, rotary_dim, fp8, stream);
-    else if (pages_layout && force_kernel("warp") && dspark::warp_path_supported(p))
+    else if (pages_layout && dspark::warp_path_supported(p) &&
+             (force_kernel("warp") || (num_ctx <= kWarpPathMaxTokens && !force_kernel("tma"))))
         e = dspark::launch_ctx_kv_write_warp(p, fp8, stream);
     else if (dspark::tma_path_supported(p, head_dim))
         e = dspark::launch_ctx_kv_write_tma(p, head_dim, fp8, stream);

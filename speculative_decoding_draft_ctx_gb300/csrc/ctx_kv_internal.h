@@ -83,9 +83,10 @@ struct CtxKvParams {
     int32_t block_size;
     int32_t bs_magic_shift;      // block = umulhi(slot, bs_magic) >> bs_magic_shift
     uint64_t bs_magic;           //   when block_size_log2 < 0
-    // test hook of the pipelined kernel (0: off): the producer first waits
-    // this many ns on a device word that nothing sets, then gives up as on
-    // any expired wait (DSPARK_FLAG_TIMEOUT, nothing written)
+    // test hook of the pipelined and warp-private kernels (0: off): the
+    // producer (every warp) first waits this many ns on a device word that
+    // nothing sets, then gives up as on any expired wait
+    // (DSPARK_FLAG_TIMEOUT, nothing written)
     uint64_t test_hold_ns;
 };
 

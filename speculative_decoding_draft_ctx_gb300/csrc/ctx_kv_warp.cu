@@ -71,6 +71,10 @@ struct WarpParams {
     CtxKvParams p;
 };
 
+// A device word that nothing ever sets: the test hook's wait (test_hold_ns)
+// runs out on it.
+__device__ unsigned g_never_set_w = 0;
+
 __device__ __forceinline__ void fence_proxy_async_shared()
 {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -124,6 +128,19 @@ __global__ void __launch_bounds__(32 * kWarps, 4) ctx_kv_warp_kernel(const WarpP
     const uint64_t stream_once = evict_first_policy();  // all_kv: read exactly once
     const uint64_t keep = evict_last_policy();          // cos|sin rows: shared by many tokens
     unsigned flags = 0;
+
+    if (p.test_hold_ns) {
+        // test hook: a bounded wait on a word nothing sets, which runs out;
+        // the warp then stops before issuing anything
+        if (lane == 0) {
+            const unsigned long long t0 = globaltimer();
+            while (*reinterpret_cast<volatile unsigned *>(&g_never_set_w) == 0 && globaltimer() - t0 < p.test_hold_ns) {
+            }
+            if (p.error_flags)
+                atomicOr(p.error_flags, kFlagTimeoutW);
+        }
+        return;
+    }
 
     // ---- first S units: copied before their slots are known
     const int nspec = (int)min((long long)S, n_my);

@@ -21,10 +21,11 @@ from parity import (alt_index_rows, compare_caches, compare_rows, device_inputs,
 pytestmark = pytest.mark.gpu
 
 
-@pytest.fixture(params=["default", "warp", "generic"])
+@pytest.fixture(params=["default", "tma", "warp", "generic"])
 def kernel(request, monkeypatch):
-    """Run the test on the kernel the library picks (the pipelined bulk-copy
-    kernel where the shape allows), on the warp-private pipelines (where
+    """Run the test on the kernel the library picks (warp-private pipelines
+    for small calls, else the pipelined bulk-copy kernel where the shape
+    allows), on the pipelined kernel, on the warp-private pipelines (where
     they apply; elsewhere the default) and on the generic kernel."""
     if request.param == "default":
         monkeypatch.delenv("DSPARK_CTX_KV_KERNEL", raising=False)
@@ -355,19 +356,21 @@ def test_writer_validation_on_device_tensors(oracle_lib):
     del wl
 
 
-def test_expired_wait_reports_timeout_and_leaves_the_context_usable(oracle_lib, monkeypatch):
-    """The timeout path of the pipelined kernel, exercised without a fault:
-    with the test hook DSPARK_TEST_HOLD_NS set, each CTA's producer first
-    waits 2 ms on a device word that nothing sets; the wait runs out, the CTA
-    stops before issuing any copy (its consumers see the abort and leave),
-    nothing is written, and DSPARK_FLAG_TIMEOUT reaches the caller's error
-    word -- or the writer's own word when the caller passes none.  The next
-    launch, hook off, matches the oracle: the context is still usable."""
+@pytest.mark.parametrize("which", ["tma", "warp"])
+def test_expired_wait_reports_timeout_and_leaves_the_context_usable(oracle_lib, monkeypatch, which):
+    """The timeout path of the pipelined and the warp-private kernels,
+    exercised without a fault: with the test hook DSPARK_TEST_HOLD_NS set,
+    each CTA's producer (each warp) first waits 2 ms on a device word that
+    nothing sets; the wait runs out, it stops before issuing any copy (the
+    pipelined kernel's consumers see the abort and leave), nothing is
+    written, and DSPARK_FLAG_TIMEOUT reaches the caller's error word -- or
+    the writer's own word when the caller passes none.  The next launch,
+    hook off, matches the oracle: the context is still usable."""
     import speculative_decoding_draft_ctx_gb300 as dk
 
     wl = wk.WORKLOADS[2].with_(num_ctx=256, pad_count=12)
     inp = wk.generate(wl)
-    monkeypatch.delenv("DSPARK_CTX_KV_KERNEL", raising=False)
+    monkeypatch.setenv("DSPARK_CTX_KV_KERNEL", which)
     monkeypatch.setenv("DSPARK_TEST_HOLD_NS", "2000000")
     flags = torch.zeros(1, dtype=torch.int32, device="cuda")
     caches, w, d = gpu_write(inp, error_flags=flags)

@@ -184,7 +184,7 @@ __global__ void __launch_bounds__(kThreads, 2) ctx_kv_tma_kernel(const TmaParams
     // (k = 0..3), so the rotated dims 0..31 are four on every lane of a row
     // and each lane's first segment rotates with lane q ^ 4 (V keeps the
     // 16-byte chunks)
-    constexpr bool kSeg = ROT == 32;
+    constexpr bool kSeg = ROT == 32 && D == 128;
     extern __shared__ __align__(128) unsigned char smem[];
     const CtxKvParams &p = tp.p;
     const int L = p.num_layers, H = p.num_kv_heads, S = tp.stages, NP = tp.pieces, Lp = tp.layers_per_piece;
@@ -554,11 +554,11 @@ __global__ void __launch_bounds__(kThreads, 2) ctx_kv_tma_kernel(const TmaParams
             const int first = (warp - gmod) & (kConsumerWarps - 1);  // this warp's first group here
             gmod = (gmod + ngroups) & (kConsumerWarps - 1);
             if constexpr (kXor) {
-                // Early release: the warp copies its rows (at most two groups --
-                // a stage holds at most 64 rows of the pages' head dim) and the
+                // Early release: the warp copies its rows (a 32 KB stage holds at
+                // most 8192 / D rows, so at most 256 / D groups per warp) and the
                 // token's cos|sin words into registers, releases the stage so
                 // that the producer can refill it at once, then computes.
-                constexpr int kMaxG = 2;
+                constexpr int kMaxG = 256 / D;
                 uint4 kd[kMaxG][NC], vd[kMaxG][NC];
                 long long gdst[kMaxG];
                 int gl[kMaxG], gh[kMaxG];
@@ -863,11 +863,13 @@ struct Plan {
     Layout lay;
 };
 
-// xor modes (r = 16, 32, 64) are built for the pages' head dim 128; every
-// other layout takes the shared-memory RoPE (ROT = 0).
+// xor modes: r = 16, 32 or 64 (the rotated dims all in each lane's first
+// chunk, partners r/16 lanes away) for every head dim; any other rotary dim
+// takes the shared-memory RoPE (ROT = 0).
 bool xor_mode(int head_dim, int rotary_dim)
 {
-    return head_dim == 128 && (rotary_dim == 16 || rotary_dim == 32 || rotary_dim == 64);
+    return (head_dim == 64 || head_dim == 128 || head_dim == 256) &&
+           (rotary_dim == 16 || rotary_dim == 32 || rotary_dim == 64);
 }
 
 bool plan_for(const CtxKvParams &p, int head_dim, Plan &pl)
@@ -937,25 +939,34 @@ cudaError_t launch_dtype(const TmaParams &tp, bool fp8, uint32_t smem, cudaStrea
                : launch_tma_variant<D, ROT, false, PL>(tp, smem, stream);
 }
 
+template <int D, bool PL>
+cudaError_t launch_rot(const TmaParams &tp, int rotary_dim, bool fp8, uint32_t smem, cudaStream_t stream)
+{
+    switch (xor_mode(D, rotary_dim) ? rotary_dim : 0) {
+    case 16:
+        return launch_dtype<D, 16, PL>(tp, fp8, smem, stream);
+    case 32:
+        return launch_dtype<D, 32, PL>(tp, fp8, smem, stream);
+    case 64:
+        return launch_dtype<D, 64, PL>(tp, fp8, smem, stream);
+    default:
+        return launch_dtype<D, 0, PL>(tp, fp8, smem, stream);
+    }
+}
+
 template <bool PL>
 cudaError_t launch_layout(const TmaParams &tp, int head_dim, int rotary_dim, bool fp8, uint32_t smem,
                           cudaStream_t stream)
 {
-    if (head_dim == 64)
-        return launch_dtype<64, 0, PL>(tp, fp8, smem, stream);
-    if (head_dim == 256)
-        return launch_dtype<256, 0, PL>(tp, fp8, smem, stream);
-    if (head_dim != 128)
-        return cudaErrorInvalidValue;
-    switch (xor_mode(head_dim, rotary_dim) ? rotary_dim : 0) {
-    case 16:
-        return launch_dtype<128, 16, PL>(tp, fp8, smem, stream);
-    case 32:
-        return launch_dtype<128, 32, PL>(tp, fp8, smem, stream);
+    switch (head_dim) {
     case 64:
-        return launch_dtype<128, 64, PL>(tp, fp8, smem, stream);
+        return launch_rot<64, PL>(tp, rotary_dim, fp8, smem, stream);
+    case 128:
+        return launch_rot<128, PL>(tp, rotary_dim, fp8, smem, stream);
+    case 256:
+        return launch_rot<256, PL>(tp, rotary_dim, fp8, smem, stream);
     default:
-        return launch_dtype<128, 0, PL>(tp, fp8, smem, stream);
+        return cudaErrorInvalidValue;
     }
 }
 

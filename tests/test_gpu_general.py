@@ -32,6 +32,12 @@ LAYOUTS = [
     layout(128, 24, 16), layout(128, 128, 48, fp8=True), layout(128, 2, 7), layout(128, 96, 12, fp8=True),
     layout(128, 64, 100, H=4),
     layout(256, 64, 32, fp8=True), layout(256, 256, 48), layout(256, 50, 100), layout(256, 2, 5, fp8=True, H=7),
+    # rotary dims 16 / 32 / 64 at head dims 64 and 256: the pipelined kernel's
+    # xor-shuffle RoPE; 16 heads x 8 layers of head dim 64 fill a 32 KB stage
+    # with 128 rows (four row groups per consumer warp), 8 heads of head dim
+    # 256 give one group per warp
+    layout(64, 16, 8, fp8=True), layout(64, 32, 5), layout(64, 64, 16, H=16, L=8, T=120, fp8=True),
+    layout(256, 16, 16), layout(256, 32, 12, fp8=True), layout(256, 32, 16, H=8, L=4, T=100),
 ]
 
 

@@ -121,6 +121,33 @@ int dspark_ctx_kv_write_ex(const void *all_kv, const void *knorm_w, const int64_
                            cudaStream_t stream);
 
 /*
+ * dspark_ctx_kv_write_sched -- the write with a dynamic tail: as
+ * dspark_ctx_kv_write_ex (one shared slot_mapping) or
+ * dspark_ctx_kv_write_layer_slots (a device table of per-layer mappings) --
+ * exactly one of the two non-NULL -- plus a work counter through which the
+ * pipelined kernel hands the last tenth of a large call's units (a unit: a
+ * token's rows of up to 8 layers) in runs of 4 to whichever CTA is free,
+ * instead of a fixed CTA (a fixed split waits for its slowest CTA).  The
+ * vLLM DSpark context-KV writer page has no counterpart: its kernel runs one
+ * fixed grid.  Calls below 64 units per CTA (the grid is two CTAs per SM:
+ * about 19.5k units on a 152-SM GPU), and layouts the pipelined kernel does
+ * not take, keep the fixed split and leave the counter untouched.
+ *
+ *  work_counter  device, 2 x uint64, 8-byte aligned, owned by the caller:
+ *                zero before its first use; every call leaves it zero
+ *                again.  Calls that can run at the same time on the GPU
+ *                (different streams without an order between them) need
+ *                their own counters; NULL gives the fixed split.
+ */
+int dspark_ctx_kv_write_sched(const void *all_kv, const void *knorm_w, const int64_t *positions,
+                              const int64_t *slot_mapping, const int64_t *const *layer_slot_mappings,
+                              int64_t num_ctx, const void *cos_sin, int64_t max_pos, void *layer0_cache,
+                              int64_t num_blocks, const int64_t *cache_offsets, const float *const *k_scales,
+                              const float *const *v_scales, int L, int nkv, int block_size, int rotary_dim,
+                              float eps, int kv_dtype, unsigned int *error_flags, unsigned long long *work_counter,
+                              cudaStream_t stream);
+
+/*
  * dspark_gemma_rms_norm -- the hidden-state Gemma RMSNorm of the context
  * states (DSpark draft model page: hidden_norm = _gemma_rms_norm(hidden_size,
  * eps), _normalize_context_states): for every row,

@@ -40,6 +40,7 @@ EXPORTS = (
     "dspark_ctx_kv_project", "dspark_ctx_kv_project_write", "dspark_gemma_rms_norm",
     "dspark_ctx_kv_write_layer_slots", "dspark_ctx_kv_tables_update_slots", "dspark_ctx_kv_tables_layer_slots",
     "dspark_ctx_kv_write_general", "dspark_ctx_kv_general_supported", "dspark_ctx_kv_validate_layers_general",
+    "dspark_ctx_kv_write_sched",
 )
 
 
@@ -117,6 +118,8 @@ def lib() -> ctypes.CDLL:
         L.dspark_gemma_rms_norm.restype = I
         L.dspark_ctx_kv_write_layer_slots.argtypes = write_args[:3] + [P] + write_args[4:] + [P, P]
         L.dspark_ctx_kv_write_layer_slots.restype = I
+        L.dspark_ctx_kv_write_sched.argtypes = write_args[:4] + [P] + write_args[4:] + [P, P, P]
+        L.dspark_ctx_kv_write_sched.restype = I
         L.dspark_ctx_kv_tables_update_slots.argtypes = [P, P, P]
         L.dspark_ctx_kv_tables_update_slots.restype = I
         L.dspark_ctx_kv_tables_layer_slots.argtypes = [P]
@@ -186,6 +189,20 @@ def dspark_ctx_kv_write_ex(all_kv, knorm_w, positions, slot_mapping, num_ctx, co
         _addr(cos_sin), int(max_pos), _addr(layer0_cache), int(num_blocks), _addr(cache_offsets),
         _addr(k_scales), _addr(v_scales), int(L), int(nkv), int(block_size), int(rotary_dim),
         float(eps), kv_dtype_code(kv_dtype), _addr(error_flags), _stream(stream)))
+
+
+def dspark_ctx_kv_write_sched(all_kv, knorm_w, positions, slot_mapping, layer_slot_mappings, num_ctx, cos_sin,
+                              max_pos, layer0_cache, num_blocks, cache_offsets, k_scales, v_scales, L, nkv,
+                              block_size, rotary_dim, eps, kv_dtype, error_flags, work_counter, stream=None):
+    """``dspark_ctx_kv_write_sched``: the write with a shared ``slot_mapping``
+    or a per-layer ``layer_slot_mappings`` table (exactly one given), the
+    error word, and ``work_counter`` (two zeroed int64 words on the device,
+    or ``None`` for the fixed split)."""
+    check(lib().dspark_ctx_kv_write_sched(
+        _addr(all_kv), _addr(knorm_w), _addr(positions), _addr(slot_mapping), _addr(layer_slot_mappings),
+        int(num_ctx), _addr(cos_sin), int(max_pos), _addr(layer0_cache), int(num_blocks), _addr(cache_offsets),
+        _addr(k_scales), _addr(v_scales), int(L), int(nkv), int(block_size), int(rotary_dim), float(eps),
+        kv_dtype_code(kv_dtype), _addr(error_flags), _addr(work_counter), _stream(stream)))
 
 
 def dspark_qknorm_rope_kv_insert(qkv, q_norm_w, k_norm_w, cos_sin, max_pos, positions, num_tokens,

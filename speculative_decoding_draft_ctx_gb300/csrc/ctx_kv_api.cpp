@@ -94,7 +94,8 @@ int write_common(const void *all_kv, const void *knorm_w, const int64_t *positio
                  const int64_t *const *layer_slots, int64_t num_ctx, const void *cos_sin, int64_t max_pos,
                  void *layer0_cache, int64_t num_blocks, const int64_t *cache_offsets, const float *const *k_scales,
                  const float *const *v_scales, int L, int nkv, int head_dim, int block_size, int rotary_dim,
-                 float eps, int kv_dtype, unsigned int *error_flags, cudaStream_t stream, Rules rules);
+                 float eps, int kv_dtype, unsigned int *error_flags, cudaStream_t stream, Rules rules,
+                 unsigned long long *work_counter = nullptr);
 
 }  // namespace
 
@@ -151,6 +152,23 @@ int dspark_ctx_kv_write_layer_slots(const void *all_kv, const void *knorm_w, con
                         block_size, rotary_dim, eps, kv_dtype, error_flags, stream, Rules::pages);
 }
 
+int dspark_ctx_kv_write_sched(const void *all_kv, const void *knorm_w, const int64_t *positions,
+                              const int64_t *slot_mapping, const int64_t *const *layer_slot_mappings,
+                              int64_t num_ctx, const void *cos_sin, int64_t max_pos, void *layer0_cache,
+                              int64_t num_blocks, const int64_t *cache_offsets, const float *const *k_scales,
+                              const float *const *v_scales, int L, int nkv, int block_size, int rotary_dim,
+                              float eps, int kv_dtype, unsigned int *error_flags, unsigned long long *work_counter,
+                              cudaStream_t stream)
+{
+    if (num_ctx > 0 && (slot_mapping == nullptr) == (layer_slot_mappings == nullptr))
+        return fail(DSPARK_ERR_INVALID_ARG, "give exactly one of slot_mapping and layer_slot_mappings");
+    if (num_ctx > 0 && layer_slot_mappings && !aligned(layer_slot_mappings, 8))
+        return fail(DSPARK_ERR_ALIGNMENT, "layer_slot_mappings must be 8-byte aligned");
+    return write_common(all_kv, knorm_w, positions, slot_mapping, layer_slot_mappings, num_ctx, cos_sin, max_pos,
+                        layer0_cache, num_blocks, cache_offsets, k_scales, v_scales, L, nkv, DSPARK_HEAD_DIM,
+                        block_size, rotary_dim, eps, kv_dtype, error_flags, stream, Rules::pages, work_counter);
+}
+
 int dspark_ctx_kv_general_supported(int head_dim, int rotary_dim, int block_size)
 {
     return (head_dim == 64 || head_dim == 128 || head_dim == 256) && rotary_dim >= 2 && rotary_dim <= head_dim &&
@@ -193,7 +211,8 @@ int write_common(const void *all_kv, const void *knorm_w, const int64_t *positio
                  const int64_t *const *layer_slots, int64_t num_ctx, const void *cos_sin, int64_t max_pos,
                  void *layer0_cache, int64_t num_blocks, const int64_t *cache_offsets, const float *const *k_scales,
                  const float *const *v_scales, int L, int nkv, int head_dim, int block_size, int rotary_dim,
-                 float eps, int kv_dtype, unsigned int *error_flags, cudaStream_t stream, Rules rules)
+                 float eps, int kv_dtype, unsigned int *error_flags, cudaStream_t stream, Rules rules,
+                 unsigned long long *work_counter)
 {
     // Scalar checks first: they need no device and no pointer.
     if (num_ctx < 0)
@@ -241,8 +260,11 @@ int write_common(const void *all_kv, const void *knorm_w, const int64_t *positio
         return fail(DSPARK_ERR_ALIGNMENT, "int64 and pointer tables must be 8-byte aligned");
     if (error_flags && !aligned(error_flags, 4))
         return fail(DSPARK_ERR_ALIGNMENT, "error_flags must be 4-byte aligned");
+    if (work_counter && !aligned(work_counter, 8))
+        return fail(DSPARK_ERR_ALIGNMENT, "work_counter must be 8-byte aligned");
 
     dspark::CtxKvParams p{};
+    p.work_counter = work_counter;
     p.all_kv = static_cast<const uint16_t *>(all_kv);
     p.knorm_w = static_cast<const uint16_t *>(knorm_w);
     p.positions = positions;

@@ -88,6 +88,9 @@ struct CtxKvParams {
     // nothing sets, then gives up as on any expired wait
     // (DSPARK_FLAG_TIMEOUT, nothing written)
     uint64_t test_hold_ns;
+    // pipelined kernel: a device pair {claimed, finished} (zero between
+    // launches) for handing out the tail of the units dynamically, or null
+    unsigned long long *work_counter;
 };
 
 // Generic kernel (any layer count and head count): enqueues the write on

@@ -156,7 +156,13 @@ struct TmaParams {
     int32_t pieces;            // ceil(L / Lp)
     int32_t stages;            // S
     uint64_t h_magic;          // ceil(2^32 / nkv): row / nkv = (row * h_magic) >> 32 for row < 2^16
-    int32_t contiguous;        // 1: each CTA takes one contiguous run of units; 0: grid stride
+    // dynamic tail (work_counter != null): units [0, static_units) go to the
+    // CTAs in grid-stride order, the rest in runs of claim_units to whichever
+    // CTA claims the next run from work_counter[0]; work_counter[1] counts
+    // finished CTAs, and the last one leaves both at zero for the next launch
+    unsigned long long *work_counter;
+    long long static_units;
+    int32_t claim_units;       // consecutive units per claim (1..32)
 };
 
 // w1 table: float4 slot of (layer l, half jj of an 8-dim chunk, chunk c of
@@ -219,21 +225,43 @@ __global__ void __launch_bounds__(kThreads, 2) ctx_kv_tma_kernel(const TmaParams
 
     if (warp == kConsumerWarps) {
         // ---------------------------------------------------------- producer
-        // Starts at once: the consumers build their tables meanwhile.  Slots
-        // and positions of the next 32 units are fetched one batch ahead.
-        // This CTA's units: u_first, u_first + step, ... below u_end (grid
-        // stride, or one contiguous run per CTA).
-        long long u_first, u_end, step;
-        if (tp.contiguous) {
-            const long long per = (units + G - 1) / G;
-            u_first = blockIdx.x * per;
-            u_end = min(units, u_first + per);
-            step = 1;
-        } else {
-            u_first = blockIdx.x;
-            u_end = units;
-            step = G;
-        }
+        // Starts at once: the consumers build their tables meanwhile.  The
+        // CTA's units come in batches: its static units in grid-stride order
+        // (32 per batch), then, with a work counter, runs of consecutive units
+        // claimed from the shared tail until the counter runs past the end.  Slots
+        // and positions of the next batch are fetched while the current one
+        // is issued.
+        struct Batch {
+            long long first, stride;  // units first + j * stride, j < count
+            int count;
+            bool dyn;
+        };
+        const long long u_first = blockIdx.x, step = G;
+        const long long u_static = tp.work_counter ? tp.static_units : units;
+        auto static_batch = [&](long long base) {
+            Batch b{base, step, 0, false};
+            if (base < u_static)
+                b.count = (int)min(32LL, (u_static - base + step - 1) / step);
+            return b;
+        };
+        auto claim = [&]() {  // the whole warp; lane 0 takes the next run of units
+            unsigned long long c = 0;
+            if (lane == 0)
+                c = atomicAdd(tp.work_counter, 1ull);
+            c = __shfl_sync(0xffffffffu, c, 0);
+            Batch b{u_static + (long long)c * tp.claim_units, 1, 0, true};
+            if (b.first < units)
+                b.count = (int)min((long long)tp.claim_units, units - b.first);
+            return b;
+        };
+        auto next_batch = [&](const Batch &b) {
+            if (!b.dyn) {
+                const Batch n = static_batch(b.first + 32 * step);
+                if (n.count > 0 || !tp.work_counter)
+                    return n;
+            }
+            return claim();
+        };
         // byte offset of a slot's (block, offset) row for head 0 within a
         // layer's cache: a power-of-two block size shifts, any other divides
         // by a multiply-high with the host's magic number
@@ -251,11 +279,11 @@ __global__ void __launch_bounds__(kThreads, 2) ctx_kv_tma_kernel(const TmaParams
         // Slot and position of unit base + lane * step.  With per-layer
         // mappings the unit's layers' slots go to the prefetch table (buffer
         // buf) and `slot` only says whether any of them is valid.
-        auto fetch = [&](long long base, long long &slot, long long &pos, int buf) {
-            const long long u = base + (long long)lane * step;
+        auto fetch = [&](const Batch &b, long long &slot, long long &pos, int buf) {
+            const long long u = b.first + (long long)lane * b.stride;
             slot = -1;
             pos = 0;
-            if (u < u_end) {
+            if (lane < b.count) {
                 const long long t = NP == 1 ? u : u / NP;
                 pos = __ldg(p.positions + t);
                 if (PL) {
@@ -275,10 +303,10 @@ __global__ void __launch_bounds__(kThreads, 2) ctx_kv_tma_kernel(const TmaParams
                 }
             }
         };
-        auto vet = [&](long long base, long long &slot, long long pos, int buf) {
+        auto vet = [&](const Batch &b, long long &slot, long long pos, int buf) {
             if (slot < 0)
                 return;
-            const long long u = base + (long long)lane * step;
+            const long long u = b.first + (long long)lane * b.stride;
             const bool first_piece = NP == 1 || u % NP == 0;  // a token is reported once
             if (pos < 0 || pos >= p.max_pos) {
                 if (first_piece)
@@ -325,7 +353,7 @@ __global__ void __launch_bounds__(kThreads, 2) ctx_kv_tma_kernel(const TmaParams
             slab = (uint32_t)min(Lp, L - l0) * H * kRowIn;
         };
         int nspec = 0;
-        for (long long u = u_first; u < u_end && nspec < S; u += step)
+        for (long long u = u_first; u < u_static && nspec < S; u += step)
             nspec++;
         if (p.test_hold_ns) {
             // test hook: a bounded wait on a word nothing sets, which runs out;
@@ -351,24 +379,26 @@ __global__ void __launch_bounds__(kThreads, 2) ctx_kv_tma_kernel(const TmaParams
                          full + i, stream_once);
             }
         }
-        long long base = u_first;
-        long long ordinal = 0;  // index of unit `base` in this CTA's sequence
-        int buf = 0;            // prefetch-table buffer of the batch at `base`
+        long long ordinal = 0;  // index of the batch's first unit in this CTA's sequence
+        int buf = 0;            // prefetch-table buffer of the current batch
         if (PL) {  // the layers' slot mapping addresses, once
             for (int j = lane; j < L; j += 32)
                 lsp[j] = reinterpret_cast<const int64_t *>(
                     __ldg(reinterpret_cast<const unsigned long long *>(p.layer_slots) + j));
             __syncwarp();
         }
-        if (ok) {
-            fetch(base, cur_slot, cur_pos, buf);
+        Batch cur = static_batch(u_first);
+        if (cur.count == 0 && tp.work_counter && ok)
+            cur = claim();
+        if (ok && cur.count > 0) {
+            fetch(cur, cur_slot, cur_pos, buf);
             if (PL)
                 asm volatile("cp.async.commit_group;" ::: "memory");
         }
-        for (; base < u_end && ok; base += 32 * step, ordinal += 32, buf ^= 1) {
-            const long long nbase = base + 32 * step;
-            if (nbase < u_end) {
-                fetch(nbase, nxt_slot, nxt_pos, buf ^ 1);
+        for (; cur.count > 0 && ok; buf ^= 1) {
+            const Batch nxt = next_batch(cur);
+            if (nxt.count > 0) {
+                fetch(nxt, nxt_slot, nxt_pos, buf ^ 1);
                 if (PL) {
                     asm volatile("cp.async.commit_group;" ::: "memory");
                     asm volatile("cp.async.wait_group 1;" ::: "memory");  // this batch's, not the next one's
@@ -376,12 +406,10 @@ __global__ void __launch_bounds__(kThreads, 2) ctx_kv_tma_kernel(const TmaParams
             } else if (PL) {
                 asm volatile("cp.async.wait_group 0;" ::: "memory");
             }
-            vet(base, cur_slot, cur_pos, buf);
+            vet(cur, cur_slot, cur_pos, buf);
             __syncwarp();  // lane 0 reads the other lanes' prefetched slots below
-            for (int i = 0; i < 32; i++) {
-                const long long u = base + (long long)i * step;
-                if (u >= u_end)
-                    break;
+            for (int i = 0; i < cur.count; i++) {
+                const long long u = cur.first + (long long)i * cur.stride;
                 const long long slot = __shfl_sync(0xffffffffu, cur_slot, i);
                 const long long pos = __shfl_sync(0xffffffffu, cur_pos, i);
                 const bool spec = ordinal + i < nspec;
@@ -464,8 +492,10 @@ __global__ void __launch_bounds__(kThreads, 2) ctx_kv_tma_kernel(const TmaParams
                     pph ^= 1u;
                 }
             }
+            ordinal += cur.count;
             cur_slot = nxt_slot;
             cur_pos = nxt_pos;
+            cur = nxt;
         }
         if (PL)
             asm volatile("cp.async.wait_group 0;" ::: "memory");  // no prefetch copy outlives the CTA
@@ -852,6 +882,17 @@ __global__ void __launch_bounds__(kThreads, 2) ctx_kv_tma_kernel(const TmaParams
     flags = __reduce_or_sync(0xffffffffu, flags);
     if (lane == 0 && flags && p.error_flags)
         atomicOr(p.error_flags, flags);
+    if (tp.work_counter) {
+        // every claim of this CTA is done (its producer has left its loop);
+        // the last CTA to finish leaves the counter at zero for the next launch
+        __syncthreads();
+        __threadfence();
+        if (threadIdx.x == 0 && atomicAdd(tp.work_counter + 1, 1ull) == gridDim.x - 1) {
+            tp.work_counter[0] = 0;
+            tp.work_counter[1] = 0;
+            __threadfence();
+        }
+    }
 }
 
 constexpr int kMaxSlabBytes = 32 * 1024;
@@ -895,6 +936,24 @@ bool plan_for(const CtxKvParams &p, int head_dim, Plan &pl)
     pl.S = S;
     pl.lay = make_layout(L, S, (uint32_t)pl.Lp * row_bytes, pl_tab, head_dim, xr);
     return pl.lay.total <= 113 * 1024;
+}
+
+int tma_sms(cudaError_t &e)
+{
+    static std::mutex mu;
+    static int sms_cache[64];
+    int dev = 0;
+    e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return 0;
+    if (dev < 0 || dev >= 64) {
+        e = cudaErrorInvalidDevice;
+        return 0;
+    }
+    std::lock_guard<std::mutex> lock(mu);
+    if (sms_cache[dev] == 0)
+        e = cudaDeviceGetAttribute(&sms_cache[dev], cudaDevAttrMultiProcessorCount, dev);
+    return sms_cache[dev];
 }
 
 template <int D, int ROT, bool FP8, bool PL>
@@ -989,7 +1048,29 @@ cudaError_t launch_ctx_kv_write_tma(const CtxKvParams &p, int head_dim, bool fp8
     tp.pieces = pl.NP;
     tp.stages = pl.S;
     tp.h_magic = (0x100000000ull + p.num_kv_heads - 1) / (uint64_t)p.num_kv_heads;
-    tp.contiguous = 0;
+    tp.work_counter = nullptr;
+    tp.static_units = 0;
+    tp.claim_units = 1;
+    if (p.work_counter) {
+        // CTAs of a static launch end up to 6% apart and the slowest one ends
+        // it, so on large calls the last tenth of the units is handed out in
+        // runs of 4 to whichever CTA is free (long context 211.8 -> 209.5 us,
+        // per-layer mappings 222.8 -> 220.4 us).  Below 64 units per CTA the
+        // claims cost more than they recover (prefill, 27 units per CTA: 1-3
+        // us slower with any tail share and run length tried), so those calls
+        // keep the static order.
+        cudaError_t e = cudaSuccess;
+        const int sms = tma_sms(e);
+        if (e != cudaSuccess)
+            return e;
+        const long long units = p.num_ctx * (long long)pl.NP;
+        const long long G = 2LL * sms;
+        if (units >= 64 * G) {
+            tp.work_counter = p.work_counter;
+            tp.static_units = units * 9 / 10 / G * G;
+            tp.claim_units = 4;
+        }
+    }
     const uint32_t smem = pl.lay.total;
     if (p.layer_slots)
         return launch_layout<true>(tp, head_dim, p.rotary_dim, fp8, smem, stream);

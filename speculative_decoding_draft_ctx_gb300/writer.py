@@ -14,9 +14,10 @@ from __future__ import annotations
 from ._binding import (
     HEAD_DIM, DSparkError, Tables, cache_desc, dspark_ctx_kv_general_supported, dspark_ctx_kv_rotary_dims_supported,
     dspark_ctx_kv_project, dspark_ctx_kv_project_write, dspark_ctx_kv_validate_layers,
-    dspark_ctx_kv_validate_layers_general, dspark_ctx_kv_write_ex, dspark_ctx_kv_write_general,
-    dspark_ctx_kv_write_layer_slots, dspark_gemma_rms_norm, dspark_qknorm_rope_kv_insert, kv_dtype_code,
+    dspark_ctx_kv_validate_layers_general, dspark_ctx_kv_write_general, dspark_ctx_kv_write_sched,
+    dspark_gemma_rms_norm, dspark_qknorm_rope_kv_insert, kv_dtype_code,
 )
+from ._binding import _stream as _stream_handle
 
 
 def _need(cond, message: str):
@@ -110,6 +111,10 @@ class ContextKVWriter:
         import torch
 
         self._flags = torch.zeros(1, dtype=torch.int32, device=c0.device)
+        # work counters of the dynamic tail, one per stream the writer has
+        # launched on: calls on one stream run in order and share a counter,
+        # calls on different streams may overlap and must not
+        self._work = {}
 
     def _descs(self):
         return [cache_desc(c, self.kv_cache_dtype, k, v)
@@ -187,16 +192,28 @@ class ContextKVWriter:
                                         t.k_scales, t.v_scales, L, nkv, self.head_dim, self.block_size, rotary_dim,
                                         eps, self._dtype, error_flags, stream)
             return
-        if per_layer is not None:
-            dspark_ctx_kv_write_layer_slots(all_kv, k_norm_weight, positions, t.layer_slots, num_ctx,
-                                            cos_sin_cache, cos_sin_cache.shape[0], self.kv_caches[0],
-                                            self.num_blocks, t.cache_offsets, t.k_scales, t.v_scales, L, nkv,
-                                            self.block_size, rotary_dim, eps, self._dtype, error_flags, stream)
-            return
-        args = (all_kv, k_norm_weight, positions, slot_mapping, num_ctx, cos_sin_cache,
-                cos_sin_cache.shape[0], self.kv_caches[0], self.num_blocks, t.cache_offsets,
-                t.k_scales, t.v_scales, L, nkv, self.block_size, rotary_dim, eps, self._dtype)
-        dspark_ctx_kv_write_ex(*args, error_flags, stream=stream)
+        dspark_ctx_kv_write_sched(all_kv, k_norm_weight, positions, slot_mapping if per_layer is None else None,
+                                  t.layer_slots if per_layer is not None else None, num_ctx, cos_sin_cache,
+                                  cos_sin_cache.shape[0], self.kv_caches[0], self.num_blocks, t.cache_offsets,
+                                  t.k_scales, t.v_scales, L, nkv, self.block_size, rotary_dim, eps, self._dtype,
+                                  error_flags, self._work_counter(stream), stream)
+
+    def _work_counter(self, stream):
+        import torch
+
+        h = _stream_handle(stream)
+        c = self._work.get(h)
+        if c is None:
+            dev = self.kv_caches[0].device
+            capturing = torch.cuda.is_current_stream_capturing()
+            if capturing and h != torch.cuda.current_stream(dev).cuda_stream:
+                return None  # its zeros could not be ordered before the launch: the fixed split
+            c = torch.zeros(2, dtype=torch.int64, device=dev)
+            if not capturing:
+                # zeroed on the current stream: land before a launch on another
+                torch.cuda.current_stream(dev).synchronize()
+            self._work[h] = c
+        return c
 
     def project_and_write(self, context_states, w_kv, k_norm_weight, eps, positions, cos_sin_cache, rotary_dim,
                           slot_mapping, stream=None, error_flags=None):

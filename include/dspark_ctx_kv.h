@@ -148,6 +148,42 @@ int dspark_ctx_kv_write_sched(const void *all_kv, const void *knorm_w, const int
                               cudaStream_t stream);
 
 /*
+ * dspark_ctx_kv_write_noalloc -- dspark_ctx_kv_write_sched with no memory
+ * allocated by the caller or by the library: the per-layer tables are given
+ * in HOST memory and the call keeps them, with the dynamic tail's work
+ * counter, in one fixed device array of the library (16 + 32 *
+ * DSPARK_NOALLOC_MAX_LAYERS bytes).  The DSpark pages have no counterpart
+ * (their tables are framework tensors).
+ *
+ *  layer_slot_mappings_host  host array of L device pointers (per-layer
+ *                   [num_ctx] int64 mappings), or NULL with slot_mapping
+ *                   (exactly one of the two)
+ *  cache_offsets_host  host int64[L], element offsets of each layer's cache
+ *                   from layer0_cache (multiples of 16 elements)
+ *  k_scales_host, v_scales_host  host arrays of L device float pointers
+ *                   (fp8; NULL for bf16 caches)
+ *  Other arguments as dspark_ctx_kv_write_sched.
+ *
+ * Each call copies its tables and the counter's zeros from host memory
+ * into the array on `stream` (the host arrays may be reused as soon as the
+ * call returns) and launches after that copy.  The first call on a device
+ * also sets up: it looks up the array's device address once; make that call
+ * before any stream capture.  There is one array per device, so calls whose
+ * executions can overlap on the GPU (different streams with no order
+ * between them, or threads issuing at the same time) race on it: order
+ * them on one stream.  L above DSPARK_NOALLOC_MAX_LAYERS returns
+ * DSPARK_ERR_INVALID_ARG before any CUDA call.
+ */
+#define DSPARK_NOALLOC_MAX_LAYERS 64
+int dspark_ctx_kv_write_noalloc(const void *all_kv, const void *knorm_w, const int64_t *positions,
+                                const int64_t *slot_mapping, const int64_t *const *layer_slot_mappings_host,
+                                int64_t num_ctx, const void *cos_sin, int64_t max_pos, void *layer0_cache,
+                                int64_t num_blocks, const int64_t *cache_offsets_host,
+                                const float *const *k_scales_host, const float *const *v_scales_host, int L,
+                                int nkv, int block_size, int rotary_dim, float eps, int kv_dtype,
+                                unsigned int *error_flags, cudaStream_t stream);
+
+/*
  * dspark_gemma_rms_norm -- the hidden-state Gemma RMSNorm of the context
  * states (DSpark draft model page: hidden_norm = _gemma_rms_norm(hidden_size,
  * eps), _normalize_context_states): for every row,

@@ -14,7 +14,7 @@ from ._binding import (  # noqa: F401
     dspark_ctx_kv_write, dspark_ctx_kv_write_ex, dspark_qknorm_rope_kv_insert, dspark_ctx_kv_project,
     dspark_ctx_kv_project_write, dspark_gemma_rms_norm, dspark_ctx_kv_write_layer_slots, kv_dtype_code, lib,
     library_path, dspark_ctx_kv_write_general, dspark_ctx_kv_general_supported,
-    dspark_ctx_kv_validate_layers_general, dspark_ctx_kv_write_sched,
+    dspark_ctx_kv_validate_layers_general, dspark_ctx_kv_write_sched, dspark_ctx_kv_write_noalloc,
 )
 from .writer import (  # noqa: F401
     ContextKVWriter, gemma_rms_norm, general_layout_supported, project_context_kv, qknorm_rope_kv_insert,

@@ -40,7 +40,7 @@ EXPORTS = (
     "dspark_ctx_kv_project", "dspark_ctx_kv_project_write", "dspark_gemma_rms_norm",
     "dspark_ctx_kv_write_layer_slots", "dspark_ctx_kv_tables_update_slots", "dspark_ctx_kv_tables_layer_slots",
     "dspark_ctx_kv_write_general", "dspark_ctx_kv_general_supported", "dspark_ctx_kv_validate_layers_general",
-    "dspark_ctx_kv_write_sched",
+    "dspark_ctx_kv_write_sched", "dspark_ctx_kv_write_noalloc",
 )
 
 
@@ -120,6 +120,8 @@ def lib() -> ctypes.CDLL:
         L.dspark_ctx_kv_write_layer_slots.restype = I
         L.dspark_ctx_kv_write_sched.argtypes = write_args[:4] + [P] + write_args[4:] + [P, P, P]
         L.dspark_ctx_kv_write_sched.restype = I
+        L.dspark_ctx_kv_write_noalloc.argtypes = write_args[:4] + [P] + write_args[4:] + [P, P]
+        L.dspark_ctx_kv_write_noalloc.restype = I
         L.dspark_ctx_kv_tables_update_slots.argtypes = [P, P, P]
         L.dspark_ctx_kv_tables_update_slots.restype = I
         L.dspark_ctx_kv_tables_layer_slots.argtypes = [P]
@@ -203,6 +205,25 @@ def dspark_ctx_kv_write_sched(all_kv, knorm_w, positions, slot_mapping, layer_sl
         int(num_ctx), _addr(cos_sin), int(max_pos), _addr(layer0_cache), int(num_blocks), _addr(cache_offsets),
         _addr(k_scales), _addr(v_scales), int(L), int(nkv), int(block_size), int(rotary_dim), float(eps),
         kv_dtype_code(kv_dtype), _addr(error_flags), _addr(work_counter), _stream(stream)))
+
+
+def dspark_ctx_kv_write_noalloc(all_kv, knorm_w, positions, slot_mapping, layer_slot_mappings, num_ctx, cos_sin,
+                                max_pos, layer0_cache, num_blocks, cache_offsets, k_scales, v_scales, L, nkv,
+                                block_size, rotary_dim, eps, kv_dtype, error_flags=None, stream=None):
+    """``dspark_ctx_kv_write_noalloc``: the per-layer tables as Python
+    sequences (host memory): ``cache_offsets`` L ints (element offsets from
+    ``layer0_cache``), ``k_scales`` / ``v_scales`` L device scalars (or
+    ``None`` for bf16), ``layer_slot_mappings`` L int64 device tensors (or
+    ``None`` with ``slot_mapping``)."""
+    def ptrs(xs):
+        return None if xs is None else (ctypes.c_void_p * len(xs))(*[_addr(x) for x in xs])
+
+    offs = (ctypes.c_int64 * len(cache_offsets))(*[int(o) for o in cache_offsets])
+    check(lib().dspark_ctx_kv_write_noalloc(
+        _addr(all_kv), _addr(knorm_w), _addr(positions), _addr(slot_mapping), ptrs(layer_slot_mappings),
+        int(num_ctx), _addr(cos_sin), int(max_pos), _addr(layer0_cache), int(num_blocks), offs, ptrs(k_scales),
+        ptrs(v_scales), int(L), int(nkv), int(block_size), int(rotary_dim), float(eps), kv_dtype_code(kv_dtype),
+        _addr(error_flags), _stream(stream)))
 
 
 def dspark_qknorm_rope_kv_insert(qkv, q_norm_w, k_norm_w, cos_sin, max_pos, positions, num_tokens,

@@ -27,7 +27,8 @@ PROJ_SRC = os.path.join(CSRC, "proj_gemm.cu")
 NORM_SRC = os.path.join(CSRC, "hidden_norm.cu")
 GENERAL_SRC = os.path.join(CSRC, "ctx_kv_general.cu")
 WARP_SRC = os.path.join(CSRC, "ctx_kv_warp.cu")
-CU_SRCS = (KERNEL_SRC, TMA_SRC, QK_SRC, PROJ_SRC, NORM_SRC, GENERAL_SRC, WARP_SRC)
+NOALLOC_SRC = os.path.join(CSRC, "ctx_kv_noalloc.cu")
+CU_SRCS = (KERNEL_SRC, TMA_SRC, QK_SRC, PROJ_SRC, NORM_SRC, GENERAL_SRC, WARP_SRC, NOALLOC_SRC)
 API_SRC = os.path.join(CSRC, "ctx_kv_api.cpp")
 HEADERS = [os.path.join(CSRC, "ctx_kv_internal.h"), os.path.join(CSRC, "ctx_kv_device.cuh"),
            os.path.join(CSRC, "ctx_kv_pipe.cuh"),

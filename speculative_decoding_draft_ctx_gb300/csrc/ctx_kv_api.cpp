@@ -99,6 +99,8 @@ int write_common(const void *all_kv, const void *knorm_w, const int64_t *positio
 
 }  // namespace
 
+int dspark::api_fail(int status, const char *message) { return fail(status, "%s", message); }
+
 extern "C" {
 
 const char *dspark_ctx_kv_last_error(void) { return g_last_error; }

@@ -53,6 +53,11 @@ __device__ __forceinline__ void pdl_enter()
 }
 #endif
 
+// Records `message` as the calling thread's last error (what
+// dspark_ctx_kv_last_error returns) and returns `status`: for entry points
+// defined outside the host layer.
+int api_fail(int status, const char *message);
+
 constexpr int kHeadDim = 128;
 constexpr int kRowElems = 256;
 

@@ -289,6 +289,34 @@ def test_general_write_argument_checks(L):
     assert gcall(num_ctx=0, slot_mapping=None, expect_ok=True) == "DSPARK_OK"
 
 
+def test_no_alloc_write_argument_checks(L):
+    """dspark_ctx_kv_write_noalloc refuses a layer count beyond its fixed
+    device array, and its host-table rules, before any CUDA call."""
+    def ncall(expect_ok=False, **over):
+        a = dict(all_kv=FAKE, knorm_w=FAKE, positions=FAKE, slot_mapping=FAKE, layer_slot_mappings=None, num_ctx=4,
+                 cos_sin=FAKE, max_pos=64, layer0_cache=FAKE, num_blocks=4, cache_offsets=[0, 4096],
+                 k_scales=[FAKE, FAKE], v_scales=[FAKE, FAKE], L=2, nkv=2, block_size=16, rotary_dim=32,
+                 eps=1e-6, kv_dtype=0)
+        a.update(over)
+        if expect_ok:
+            dk.dspark_ctx_kv_write_noalloc(**a, stream=0)
+            return "DSPARK_OK"
+        with pytest.raises(dk.DSparkError) as ei:
+            dk.dspark_ctx_kv_write_noalloc(**a, stream=0)
+        return ei.value.name, str(ei.value)
+
+    name, msg = ncall(L=65, cache_offsets=[0] * 65, k_scales=[FAKE] * 65, v_scales=[FAKE] * 65)
+    assert name == "DSPARK_ERR_INVALID_ARG" and "1 to 64 layers" in msg
+    assert ncall(L=0, cache_offsets=[0], k_scales=None, v_scales=None)[0] == "DSPARK_ERR_INVALID_ARG"
+    assert ncall(slot_mapping=None)[0] == "DSPARK_ERR_INVALID_ARG"  # no slot source
+    assert ncall(layer_slot_mappings=[FAKE, FAKE])[0] == "DSPARK_ERR_INVALID_ARG"  # two
+    assert ncall(slot_mapping=None, layer_slot_mappings=[FAKE, None])[0] == "DSPARK_ERR_INVALID_ARG"
+    assert ncall(kv_dtype=1, k_scales=None)[0] == "DSPARK_ERR_INVALID_ARG"  # fp8 needs scales
+    assert ncall(cache_offsets=[0, 4100])[0] == "DSPARK_ERR_ALIGNMENT"  # not 16 elements apart
+    assert ncall(num_ctx=-1)[0] == "DSPARK_ERR_INVALID_ARG"
+    assert ncall(num_ctx=0, expect_ok=True) == "DSPARK_OK"  # nothing to store, no CUDA call
+
+
 def test_general_supported_rule(L):
     for hd in (64, 128, 256):
         for r in range(2, hd + 1, 2):

@@ -101,6 +101,22 @@ __device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t by
         : "memory");
 }
 
+// Hints that bring global memory into L2 and hand no data to the program.
+// L2 is the point of coherence of every SM's global accesses, so they may be
+// issued before griddepcontrol.wait even on bytes the previous kernel is
+// still writing: the copies made after the wait read the lines as that
+// kernel leaves them.  Bulk form: 16-byte aligned address, size a multiple
+// of 16.
+__device__ __forceinline__ void prefetch_l2_bulk(const void *src, uint32_t bytes)
+{
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
+__device__ __forceinline__ void prefetch_l2(const void *p)
+{
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+}
+
 __device__ __forceinline__ uint64_t evict_first_policy()
 {
     uint64_t pol;

@@ -217,6 +217,23 @@ __global__ void __launch_bounds__(kThreads, 2) ctx_kv_tma_kernel(const TmaParams
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     __syncthreads();
+    if (warp == kConsumerWarps) {
+        // While the previous kernel drains: the K|V slabs of this CTA's first
+        // S units, and the slots and positions of its first 32, into L2 (hints
+        // only; every copy below still follows griddepcontrol.wait).
+        const long long u_end = tp.work_counter ? tp.static_units : p.num_ctx * (long long)NP;
+        const long long u = blockIdx.x + (long long)lane * gridDim.x;
+        if (u < u_end) {
+            const long long t = NP == 1 ? u : u / NP;
+            if (lane < S) {
+                const int l0 = (NP == 1 ? 0 : (int)(u - t * NP)) * Lp;
+                prefetch_l2_bulk(p.all_kv + (t * L + l0) * 2LL * H * D, (uint32_t)min(Lp, L - l0) * H * kRowIn);
+            }
+            if (!PL)
+                prefetch_l2(p.slot_mapping + t);
+            prefetch_l2(p.positions + t);
+        }
+    }
     pdl_enter();  // launched with launch_pdl: the barriers above need no global memory
 
     const long long units = p.num_ctx * (long long)NP;

@@ -108,23 +108,36 @@ __global__ void __launch_bounds__(32 * kWarps, 4) ctx_kv_warp_kernel(const WarpP
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     __syncwarp();
-    pdl_enter();  // launched with launch_pdl: the barriers above need no global memory
 
     const long long T = p.num_ctx;
     const long long U = (T + P - 1) / P;            // token units
     const long long NS = (long long)gridDim.x * kWarps / L;  // token streams
     const long long gw = (long long)blockIdx.x * kWarps + warp;
-    if (gw >= NS * L)
-        return;  // a warp beyond the last whole set of L streams: idle
     const int l = (int)(gw % L);
     const long long ts = gw / L;
-    const long long n_my = ts < U ? (U - ts + NS - 1) / NS : 0;  // units of this warp
-    if (n_my == 0)
-        return;
+    const long long n_my = gw < NS * L && ts < U ? (U - ts + NS - 1) / NS : 0;  // units of this warp
     auto unit_of = [&](long long o) { return ts + o * NS; };
     auto unit_tokens = [&](long long u) { return (int)min((long long)P, T - u * P); };
     const unsigned char *kv_layer = reinterpret_cast<const unsigned char *>(p.all_kv) + (size_t)l * kTokRows;
     const size_t tok_stride = (size_t)L * kTokRows;  // bytes between consecutive tokens in all_kv
+    // While the previous kernel drains: this warp's first S units' K|V rows,
+    // and the slots and positions of its first 32 units, into L2 (hints
+    // only; the copies below still follow griddepcontrol.wait).
+    if (n_my > 0) {
+        if (lane < S && lane < n_my) {
+            const long long u = unit_of(lane);
+            for (int j = 0; j < unit_tokens(u); j++)
+                prefetch_l2_bulk(kv_layer + (size_t)(u * P + j) * tok_stride, kTokRows);
+        }
+        if (lane < n_my) {
+            const long long t = unit_of(lane) * P;
+            prefetch_l2(p.slot_mapping + t);
+            prefetch_l2(p.positions + t);
+        }
+    }
+    pdl_enter();  // launched with launch_pdl: the barriers above need no global memory
+    if (n_my == 0)
+        return;  // no units (or a warp beyond the last whole set of L streams): idle
     const uint64_t stream_once = evict_first_policy();  // all_kv: read exactly once
     const uint64_t keep = evict_last_policy();          // cos|sin rows: shared by many tokens
     unsigned flags = 0;

@@ -25,6 +25,7 @@
 
 #include "ctx_kv_device.cuh"
 #include "ctx_kv_internal.h"
+#include "ctx_kv_pipe.cuh"
 
 namespace dspark {
 namespace {
@@ -71,6 +72,15 @@ __device__ __forceinline__ uint4 ld_stream(const void *p)
     return r;
 }
 
+// While the previous kernel drains: row r of x into L2 (a hint only; the
+// loads still follow griddepcontrol.wait).  Rows are a multiple of 16 bytes
+// and x is 16-byte aligned.
+__device__ __forceinline__ void prefetch_row(const uint16_t *x, int64_t r, int64_t rows, int hidden)
+{
+    if (r < rows && (threadIdx.x & 31) == 0)
+        pipe::prefetch_l2_bulk(x + r * hidden, (uint32_t)hidden * 2u);
+}
+
 // Widths up to 32 * 8 * kChunks elements; rows wider than 4096 take the
 // two-pass variant (kChunks 0): the sum of squares first, then the row is
 // read again (an L2 hit) to be normed, so no lane holds more than it must.
@@ -78,6 +88,7 @@ template <int kChunks>
 __global__ void __launch_bounds__(kThreadsN, kChunks <= 4 ? 4 : (kChunks <= 8 ? 3 : 2))
     gemma_norm_kernel(const uint16_t *x, const uint16_t *w, uint16_t *out, int64_t rows, int hidden, float eps)
 {
+    prefetch_row(x, (int64_t)blockIdx.x * kWarpsN + (threadIdx.x >> 5), rows, hidden);
     pdl_enter();
     const int lane = threadIdx.x & 31;
     const int chunks = hidden >> 3;
@@ -131,8 +142,10 @@ __global__ void __launch_bounds__(kThreadsN) gemma_norm_split_kernel(const uint1
                                                                      uint16_t *out, int64_t rows, int hidden,
                                                                      float eps)
 {
-    pdl_enter();
     constexpr int kRowsPerCta = kWarpsN / 4, kChunksS = 4;  // 128 threads x 4 chunks = 4096 elements
+    if (((threadIdx.x >> 5) & 3) == 0)
+        prefetch_row(x, (int64_t)blockIdx.x * kRowsPerCta + (threadIdx.x >> 7), rows, hidden);
+    pdl_enter();
     __shared__ float part[kWarpsN];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int sub = warp & 3, slot = warp >> 2;  // warp within its row, row within the CTA
@@ -193,6 +206,7 @@ __global__ void __launch_bounds__(kThreadsN, 4)
     gemma_norm_two_pass_kernel(const uint16_t *x, const uint16_t *w, uint16_t *out, int64_t rows, int hidden,
                                float eps)
 {
+    prefetch_row(x, (int64_t)blockIdx.x * kWarpsN + (threadIdx.x >> 5), rows, hidden);
     pdl_enter();
     const int lane = threadIdx.x & 31;
     const int chunks = hidden >> 3;

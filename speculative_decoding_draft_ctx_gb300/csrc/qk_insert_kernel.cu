@@ -39,6 +39,7 @@
 
 #include "ctx_kv_device.cuh"
 #include "ctx_kv_internal.h"
+#include "ctx_kv_pipe.cuh"
 
 namespace dspark {
 namespace {
@@ -81,6 +82,16 @@ __device__ __forceinline__ int w1_slot(int norm, int jj, int c) { return norm * 
 template <int ROT, bool FP8>
 __global__ void __launch_bounds__(kThreads, 3) qk_insert_kernel(const QkInsertParams p)
 {
+    if (threadIdx.x == 0 && blockIdx.x < p.num_tokens) {
+        // While the previous kernel drains: this CTA's first token -- its
+        // qkv row, position and slot -- into L2 (hints only; every load below
+        // still follows griddepcontrol.wait).
+        const int64_t t = blockIdx.x, W = p.num_heads + 2 * p.num_kv_heads;
+        pipe::prefetch_l2_bulk(p.qkv + t * W * kHeadDim, (uint32_t)(W * kHeadDim * 2));
+        pipe::prefetch_l2(p.positions + t);
+        if (p.slot_mapping)
+            pipe::prefetch_l2(p.slot_mapping + t);
+    }
     pdl_enter();
     constexpr int kPartner = ROT / 16;  // lane distance of a rotated pair
     constexpr int kRotLanes = ROT / 8;  // lanes whose first word holds rotary dims

@@ -52,7 +52,7 @@ namespace {
 
 using namespace pipe;
 
-constexpr int kWarps = 4;      // warps per CTA
+constexpr int kWarps = 4;      // warps per CTA (8 or 16 measured slower on the draft steps)
 constexpr int kStagesW = 3;    // stages per warp
 constexpr int kCsSlotW = 128;  // one token's cos|sin row (2r <= 128 bytes)
 constexpr unsigned kFlagSlotW = 0x1u, kFlagPosW = 0x2u, kFlagTimeoutW = 0x4u;
@@ -155,49 +155,6 @@ __global__ void __launch_bounds__(32 * kWarps, 4) ctx_kv_warp_kernel(const WarpP
         return;
     }
 
-    // ---- first S units: copied before their slots are known
-    const int nspec = (int)min((long long)S, n_my);
-    if (lane == 0) {
-        for (int i = 0; i < nspec; i++) {
-            const long long u = unit_of(i);
-            const int n = unit_tokens(u);
-            mbar_expect_tx(full + i, (uint32_t)n * kTokRows);
-            for (int j = 0; j < n; j++)
-                bulk_g2s(stages + (size_t)i * Sm::kStage + j * kTokRows, kv_layer + (size_t)(u * P + j) * tok_stride,
-                         kTokRows, full + i, stream_once);
-        }
-    }
-
-    // ---- per-layer constants, in registers for the whole launch
-    const int q = lane & 7;    // 8-dim chunk of each 64-dim half of the row
-    const int rr = lane >> 3;  // row of the 4-row group
-    const bool rot_lane = q < kRotLanes;
-    uint64_t w1[8];  // (1 + w[l, d]) in fp32 for the lane's dims, as pairs
-#pragma unroll
-    for (int c = 0; c < 2; c++) {
-        const uint4 wr = __ldg(reinterpret_cast<const uint4 *>(p.knorm_w + l * 128 + 64 * c + 8 * q));
-        const uint32_t ww[4] = {wr.x, wr.y, wr.z, wr.w};
-#pragma unroll
-        for (int j = 0; j < 4; j++)
-            w1[4 * c + j] = pr(1.0f + __uint_as_float(ww[j] << 16), 1.0f + __uint_as_float(ww[j] & 0xffff0000u));
-    }
-    unsigned char *const lbase = p.cache0 + __ldg(p.cache_offsets + l) * (FP8 ? 1 : 2);
-    Fp8Scale kq{}, vq{};
-    if (FP8) {
-        kq = fp8_scale(__ldg(reinterpret_cast<const float *>(
-            __ldg(reinterpret_cast<const unsigned long long *>(p.k_scales) + l))));
-        vq = fp8_scale(__ldg(reinterpret_cast<const float *>(
-            __ldg(reinterpret_cast<const unsigned long long *>(p.v_scales) + l))));
-    }
-    const long long head_bytes = (long long)kCacheRow << p.block_size_log2;
-    // the two row groups of a unit: token tg[g], head hh[g]
-    constexpr int tg[2] = {0, P - 1};
-    const int hh[2] = {rr, P == 1 ? 4 + rr : rr};
-    uint32_t koff[2];  // byte offset of the group's K row in a stage
-#pragma unroll
-    for (int g = 0; g < 2; g++)
-        koff[g] = (uint32_t)(tg[g] * kTokRows + hh[g] * 256);
-
     // ---- slots and positions, one batch of 32 units ahead
     auto row_off = [&](long long slot) {
         return ((slot >> p.block_size_log2) * H * ((long long)1 << p.block_size_log2) +
@@ -236,7 +193,59 @@ __global__ void __launch_bounds__(32 * kWarps, 4) ctx_kv_warp_kernel(const WarpP
         }
     };
     long long cur_s[P], cur_p[P], nxt_s[P], nxt_p[P];
-    fetch(0, cur_s, cur_p);
+    fetch(0, cur_s, cur_p);  // first: the cos|sin copies wait on these positions
+    // the layer's norm weights, cache offset and scales: issued now, used below
+    const int q = lane & 7;    // 8-dim chunk of each 64-dim half of the row
+    uint4 wraw[2];
+#pragma unroll
+    for (int c = 0; c < 2; c++)
+        wraw[c] = __ldg(reinterpret_cast<const uint4 *>(p.knorm_w + l * 128 + 64 * c + 8 * q));
+    const long long loff = __ldg(p.cache_offsets + l);
+    float ksf = 1.0f, vsf = 1.0f;
+    if (FP8) {
+        ksf = __ldg(reinterpret_cast<const float *>(__ldg(reinterpret_cast<const unsigned long long *>(p.k_scales) + l)));
+        vsf = __ldg(reinterpret_cast<const float *>(__ldg(reinterpret_cast<const unsigned long long *>(p.v_scales) + l)));
+    }
+
+    // ---- first S units: copied before their slots are known
+    const int nspec = (int)min((long long)S, n_my);
+    if (lane == 0) {
+        for (int i = 0; i < nspec; i++) {
+            const long long u = unit_of(i);
+            const int n = unit_tokens(u);
+            mbar_expect_tx(full + i, (uint32_t)n * kTokRows);
+            for (int j = 0; j < n; j++)
+                bulk_g2s(stages + (size_t)i * Sm::kStage + j * kTokRows, kv_layer + (size_t)(u * P + j) * tok_stride,
+                         kTokRows, full + i, stream_once);
+        }
+    }
+
+    // ---- per-layer constants, in registers for the whole launch
+    const int rr = lane >> 3;  // row of the 4-row group
+    const bool rot_lane = q < kRotLanes;
+    uint64_t w1[8];  // (1 + w[l, d]) in fp32 for the lane's dims, as pairs
+#pragma unroll
+    for (int c = 0; c < 2; c++) {
+        const uint32_t ww[4] = {wraw[c].x, wraw[c].y, wraw[c].z, wraw[c].w};
+#pragma unroll
+        for (int j = 0; j < 4; j++)
+            w1[4 * c + j] = pr(1.0f + __uint_as_float(ww[j] << 16), 1.0f + __uint_as_float(ww[j] & 0xffff0000u));
+    }
+    unsigned char *const lbase = p.cache0 + loff * (FP8 ? 1 : 2);
+    Fp8Scale kq{}, vq{};
+    if (FP8) {
+        kq = fp8_scale(ksf);
+        vq = fp8_scale(vsf);
+    }
+    const long long head_bytes = (long long)kCacheRow << p.block_size_log2;
+    // the two row groups of a unit: token tg[g], head hh[g]
+    constexpr int tg[2] = {0, P - 1};
+    const int hh[2] = {rr, P == 1 ? 4 + rr : rr};
+    uint32_t koff[2];  // byte offset of the group's K row in a stage
+#pragma unroll
+    for (int g = 0; g < 2; g++)
+        koff[g] = (uint32_t)(tg[g] * kTokRows + hh[g] * 256);
+
     vet(cur_s, cur_p);
     if (n_my > 32) {
         fetch(32, nxt_s, nxt_p);

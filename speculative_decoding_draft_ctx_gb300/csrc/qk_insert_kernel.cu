@@ -105,6 +105,36 @@ __global__ void __launch_bounds__(kThreads, 3) qk_insert_kernel(const QkInsertPa
     const int bsl = p.block_size_log2;
     const int64_t head_stride = (int64_t)kRowElems << bsl;  // cache elements between kv heads of one slot
 
+    // The first token's position, slot and first head groups are loaded
+    // before anything else, so that their latency overlaps the weight
+    // table's set-up; value heads are read whenever an insert is asked for,
+    // and dropped for padded tokens.
+    uint16_t *trow = p.qkv + (int64_t)blockIdx.x * W * kHeadDim;
+    uint4 xa[kBatch], xb[kBatch];
+    int hd[kBatch];
+    bool live[kBatch];
+    auto load_batch = [&](int g0) {
+#pragma unroll
+        for (int i = 0; i < kBatch; i++) {
+            const int g = g0 + i * kWarps;
+            const int hh = 4 * g + sub;
+            hd[i] = hh;
+            live[i] = g < groups && hh < W && (hh < Hq + Hkv || p.slot_mapping != nullptr);
+            if (live[i]) {
+                const uint16_t *src = trow + hh * kHeadDim;
+                xa[i] = ld16(src + 8 * q);
+                xb[i] = ld16(src + 64 + 8 * q);
+            }
+        }
+    };
+    int64_t pos_first = 0, slot_first = -1;
+    if (blockIdx.x < p.num_tokens) {
+        pos_first = __ldg(p.positions + blockIdx.x);
+        slot_first = p.slot_mapping ? __ldg(p.slot_mapping + blockIdx.x) : -1;
+        if (warp < groups)
+            load_batch(warp);
+    }
+
     __shared__ float4 w1[64];  // (1 + w) of the query norm (slots 0..31) and the key norm (32..63)
     {
         const int i = threadIdx.x;  // kThreads == 2 * 128: one weight element per thread
@@ -123,32 +153,15 @@ __global__ void __launch_bounds__(kThreads, 3) qk_insert_kernel(const QkInsertPa
     unsigned flags = 0;
 
     for (int64_t t = blockIdx.x; t < p.num_tokens; t += gridDim.x) {
-        uint16_t *trow = p.qkv + t * W * kHeadDim;
-        const int64_t pos = __ldg(p.positions + t);
-        int64_t slot = p.slot_mapping ? __ldg(p.slot_mapping + t) : -1;
-        // The first groups' loads go out with the position and slot loads:
-        // value heads are read whenever an insert is asked for, and dropped
-        // for padded tokens.
-        uint4 xa[kBatch], xb[kBatch];
-        int hd[kBatch];
-        bool live[kBatch];
-        auto load_batch = [&](int g0) {
-#pragma unroll
-            for (int i = 0; i < kBatch; i++) {
-                const int g = g0 + i * kWarps;
-                const int hh = 4 * g + sub;
-                hd[i] = hh;
-                live[i] = g < groups && hh < W && (hh < Hq + Hkv || p.slot_mapping != nullptr);
-                if (live[i]) {
-                    const uint16_t *src = trow + hh * kHeadDim;
-                    xa[i] = ld16(src + 8 * q);
-                    xb[i] = ld16(src + 64 + 8 * q);
-                }
-            }
-        };
         int g0 = warp;
-        if (g0 < groups)
-            load_batch(g0);
+        int64_t pos = pos_first, slot = slot_first;
+        if (t != blockIdx.x) {
+            trow = p.qkv + t * W * kHeadDim;
+            pos = __ldg(p.positions + t);
+            slot = p.slot_mapping ? __ldg(p.slot_mapping + t) : -1;
+            if (g0 < groups)
+                load_batch(g0);
+        }
         if (pos < 0 || pos >= p.max_pos) {
             flags |= kFlagPos;  // untouched, and not inserted either
             continue;

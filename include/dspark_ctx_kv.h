@@ -60,6 +60,7 @@ typedef enum {
 #define DSPARK_FLAG_SLOT_RANGE 0x1u /* slot >= num_blocks * block_size */
 #define DSPARK_FLAG_POS_RANGE 0x2u  /* position < 0 or >= max_pos (valid slot) */
 #define DSPARK_FLAG_TIMEOUT 0x4u    /* an internal wait gave up and the kernel stopped early */
+#define DSPARK_FLAG_COUNTER 0x8u    /* dspark_ctx_kv_write_sched: the work counter was not zero at launch */
 
 /*
  * dspark_ctx_kv_write -- the fused write (writer page, module docstring and
@@ -137,7 +138,11 @@ int dspark_ctx_kv_write_ex(const void *all_kv, const void *knorm_w, const int64_
  *                zero before its first use; every call leaves it zero
  *                again.  Calls that can run at the same time on the GPU
  *                (different streams without an order between them) need
- *                their own counters; NULL gives the fixed split.
+ *                their own counters; NULL gives the fixed split.  A counter
+ *                found far from zero raises DSPARK_FLAG_COUNTER and hands
+ *                out nothing (rows of the tail stay unwritten; the call
+ *                leaves it zero again); a small nonzero value skips that
+ *                many runs unreported.
  */
 int dspark_ctx_kv_write_sched(const void *all_kv, const void *knorm_w, const int64_t *positions,
                               const int64_t *slot_mapping, const int64_t *const *layer_slot_mappings,

@@ -8,7 +8,7 @@ K/V insert.  The compute runs in ``libdspark_ctx_kv.so`` (C ABI declared in
 """
 
 from ._binding import (  # noqa: F401
-    CACHE_ROW, EXPORTS, FLAG_POS_RANGE, FLAG_SLOT_RANGE, FLAG_TIMEOUT, HEAD_DIM, KV_BF16, KV_FP8_E4M3, STATUS,
+    CACHE_ROW, EXPORTS, FLAG_COUNTER, FLAG_POS_RANGE, FLAG_SLOT_RANGE, FLAG_TIMEOUT, HEAD_DIM, KV_BF16, KV_FP8_E4M3, STATUS,
     STATUS_CODE, CacheDesc, DSparkError, Tables, cache_desc, check, dspark_ctx_kv_last_error,
     dspark_ctx_kv_rotary_dims_supported, dspark_ctx_kv_status_string, dspark_ctx_kv_validate_layers,
     dspark_ctx_kv_write, dspark_ctx_kv_write_ex, dspark_qknorm_rope_kv_insert, dspark_ctx_kv_project,

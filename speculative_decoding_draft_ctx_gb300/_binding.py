@@ -29,6 +29,7 @@ STATUS_CODE = {v: k for k, v in STATUS.items()}
 FLAG_SLOT_RANGE = 0x1
 FLAG_POS_RANGE = 0x2
 FLAG_TIMEOUT = 0x4
+FLAG_COUNTER = 0x8
 
 # every function the header declares
 EXPORTS = (

@@ -86,6 +86,7 @@ constexpr int kCsBytes = 128;                        // cos|sin row slot (r <= 6
 constexpr unsigned kFlagSlot = 0x1u;
 constexpr unsigned kFlagPos = 0x2u;
 constexpr unsigned kFlagTimeout = 0x4u;
+constexpr unsigned kFlagCounter = 0x8u;
 constexpr int kMaxTmaLayers = 32;
 
 // A device word that nothing ever sets: the test hook's wait (test_hold_ns)
@@ -263,14 +264,24 @@ __global__ void __launch_bounds__(kThreads, 2) ctx_kv_tma_kernel(const TmaParams
                 b.count = (int)min(32LL, (u_static - base + step - 1) / step);
             return b;
         };
+        // runs of the shared tail; a launch makes at most runs + G claims
+        // (every CTA's last one finds the tail empty), so a larger claim
+        // number means the counter was not zero at launch: no unit is taken
+        // from it and the call is flagged
+        const unsigned long long runs =
+            tp.work_counter ? (unsigned long long)((units - u_static + tp.claim_units - 1) / tp.claim_units) : 0;
         auto claim = [&]() {  // the whole warp; lane 0 takes the next run of units
             unsigned long long c = 0;
             if (lane == 0)
                 c = atomicAdd(tp.work_counter, 1ull);
             c = __shfl_sync(0xffffffffu, c, 0);
-            Batch b{u_static + (long long)c * tp.claim_units, 1, 0, true};
-            if (b.first < units)
+            Batch b{0, 1, 0, true};
+            if (c < runs) {
+                b.first = u_static + (long long)c * tp.claim_units;
                 b.count = (int)min((long long)tp.claim_units, units - b.first);
+            } else if (c >= runs + (unsigned long long)G) {
+                flags |= kFlagCounter;
+            }
             return b;
         };
         auto next_batch = [&](const Batch &b) {

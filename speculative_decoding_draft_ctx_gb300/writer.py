@@ -138,7 +138,9 @@ class ContextKVWriter:
         was last cleared (calls that passed their own ``error_flags`` report
         there instead): FLAG_SLOT_RANGE / FLAG_POS_RANGE for rows skipped as
         out of range, FLAG_TIMEOUT when a launch gave up on a bounded wait and
-        left rows unwritten.  Reading it synchronises with the device."""
+        left rows unwritten, FLAG_COUNTER when a work counter was found not
+        zero (rows of the tail unwritten).  Reading it synchronises with the
+        device."""
         v = int(self._flags.item())
         if clear and v:
             self._flags.zero_()

@@ -101,6 +101,22 @@ def test_out_of_range_rows_are_skipped_and_flagged_with_a_counter(oracle_lib):
     check_parity(oracle_lib, ref, caches)
 
 
+def test_a_dirty_counter_is_flagged_and_left_zero(oracle_lib):
+    # a counter far from zero hands out no unit (nothing is read past the
+    # tail), raises its flag, and is zero again after the call; the next call
+    # on it is exact
+    import speculative_decoding_draft_ctx_gb300 as dk
+
+    inp = wk.generate(BIG)
+    counter = torch.tensor([1 << 40, 0], dtype=torch.int64, device="cuda")
+    _, flags = write_sched(inp, counter)
+    assert flags == dk.FLAG_COUNTER
+    assert counter.tolist() == [0, 0]
+    caches, flags = write_sched(inp, counter)
+    assert flags == 0
+    check_parity(oracle_lib, inp, caches)
+
+
 def test_null_counter_is_the_fixed_split(oracle_lib):
     inp = wk.generate(PREFILL)
     caches, _ = write_sched(inp, None)

@@ -30,6 +30,11 @@
 // contiguous bytes per (token, head) into the layer's paged cache.  all_kv
 // never reaches HBM.
 //
+// Tall tiles (calls of at most 2,048 tokens where they save a wave): 256
+// tokens x 256 columns, two x boxes per k-block against the same weight
+// boxes, eight MMAs per k-block into both accumulators, three 64 KB stages;
+// the epilogue runs the same code over the two 128-row halves.
+//
 // Every mbarrier wait is bounded (globaltimer); on expiry the CTA raises
 // DSPARK_FLAG_TIMEOUT, stops issuing, waits (bounded) for its own copies and
 // MMAs in flight, frees its tensor memory and returns.
@@ -38,6 +43,8 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <cstdlib>
+#include <cstring>
 #include <mutex>
 
 #include "ctx_kv_device.cuh"
@@ -54,8 +61,22 @@ constexpr uint32_t kStageBytes = kABytes + 2 * kBoxBytes;  // 48 KB
 constexpr uint32_t kTmemCols = 512;  // two 256-column accumulators: the epilogue of one tile overlaps the next
 constexpr int kMaxLayersProj = 32;   // the (1 + w) table of every layer lives in shared memory
 constexpr int kGroupN = 16;          // column tiles per rasterisation group
-constexpr uint32_t kSmemBytes = kStages * kStageBytes + 1024 /* alignment pad */ + 256 /* barriers */ +
-                                kMaxLayersProj * 128 * 4 /* (1 + w) table */;
+// Tile shape.  Short tiles (128 tokens) keep the two accumulators apart, so
+// the epilogue of one tile overlaps the MMAs of the next.  Tall tiles (256
+// tokens: two 128-row A boxes per k-block against the same two weight boxes,
+// one accumulator each) hold 64 KB of operands per k-block for twice the
+// flops of a short tile's 48 KB, and halve the tile count; their epilogue
+// does not overlap the next tile's MMAs (both accumulators are in use).
+template <bool TALL>
+struct TileCfg {
+    static constexpr int kRows = TALL ? 256 : BM;                       // tokens per tile
+    static constexpr int kStagesC = TALL ? 3 : kStages;                 // k-blocks in flight
+    static constexpr uint32_t kAPart = TALL ? 2 * kABytes : kABytes;    // x boxes of a stage
+    static constexpr uint32_t kStage = kAPart + 2 * kBoxBytes;          // 64 KB / 48 KB
+    static constexpr uint32_t kSmem = kStagesC * kStage + 1024 /* alignment pad */ + 256 /* barriers */ +
+                                      kMaxLayersProj * 128 * 4 /* (1 + w) table */;
+};
+static_assert(TileCfg<true>::kSmem <= 227 * 1024 && TileCfg<false>::kSmem <= 227 * 1024, "shared memory");
 constexpr unsigned kFlagSlot = 0x1u, kFlagPos = 0x2u, kFlagTimeout = 0x4u;
 constexpr unsigned long long kTimeoutNs = 4000000000ull;
 constexpr uint32_t kSuspendNs = 200000;
@@ -232,18 +253,21 @@ __device__ __forceinline__ void tile_coords(int tile, int num_m, int num_n, int 
     n = g * kGroupN + (r - m * gn);
 }
 
-template <int MODE, int ROT, bool FP8>
+template <int MODE, int ROT, bool FP8, bool TALL>
 __global__ void __launch_bounds__(kThreadsG, 1)
     proj_gemm_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant__ CUtensorMap tmw,
                      const GemmParams p)
 {
+    using C = TileCfg<TALL>;
+    constexpr int KS = C::kStagesC;
+    constexpr int NH = TALL ? 2 : 1;  // 128-row accumulators per tile
     extern __shared__ unsigned char smem_raw[];
     unsigned char *smem = smem_raw + ((1024u - (saddr(smem_raw) & 1023u)) & 1023u);  // 1024-aligned for the swizzle
     unsigned char *stages = smem;
-    unsigned char *ctl = smem + kStages * kStageBytes;
+    unsigned char *ctl = smem + KS * C::kStage;
     uint64_t *full = reinterpret_cast<uint64_t *>(ctl);  // TMA -> MMA, per stage
-    uint64_t *empty = full + kStages;                      // MMA -> TMA, per stage
-    uint64_t *acc_full = empty + kStages;                  // MMA -> epilogue, per accumulator
+    uint64_t *empty = full + KS;                           // MMA -> TMA, per stage
+    uint64_t *acc_full = empty + KS;                       // MMA -> epilogue, per accumulator (tall: the pair)
     uint64_t *acc_empty = acc_full + 2;                    // epilogue -> MMA, per accumulator
     uint64_t *done = acc_empty + 2;                        // every MMA of the CTA has completed
     volatile uint32_t *tmem_slot = reinterpret_cast<volatile uint32_t *>(done + 1);
@@ -251,11 +275,11 @@ __global__ void __launch_bounds__(kThreadsG, 1)
     float *w1 = reinterpret_cast<float *>(ctl + 256);      // (1 + w) of every layer, [L][128]
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int num_m = (int)((p.T + BM - 1) / BM), num_n = p.L * p.nkv;
+    const int num_m = (int)((p.T + C::kRows - 1) / C::kRows), num_n = p.L * p.nkv;
     const int num_tiles = num_m * num_n;
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kStages; s++) {
+        for (int s = 0; s < KS; s++) {
             mbar_init(full + s, 1);
             mbar_init(empty + s, 1);
         }
@@ -297,23 +321,25 @@ __global__ void __launch_bounds__(kThreadsG, 1)
                 const int l = n / p.nkv, h = n - l * p.nkv;
                 const int nk = ((l * 2 + 0) * p.nkv + h) * 128, nv = ((l * 2 + 1) * p.nkv + h) * 128;
                 for (int kb = 0; kb < p.num_kb; kb++) {
-                    const int s = issued % kStages;
-                    if (!mbar_wait(empty + s, ((uint32_t)(issued / kStages) & 1u) ^ 1u, abort)) {
+                    const int s = issued % KS;
+                    if (!mbar_wait(empty + s, ((uint32_t)(issued / KS) & 1u) ^ 1u, abort)) {
                         ok = false;
                         break;
                     }
-                    unsigned char *st = stages + s * kStageBytes;
-                    mbar_expect_arrive(full + s, kStageBytes);
-                    tma_load(st, &tmx, kb * BK, m * BM, full + s);
-                    tma_load(st + kABytes, &tmw, kb * BK, nk, full + s);
-                    tma_load(st + kABytes + kBoxBytes, &tmw, kb * BK, nv, full + s);
+                    unsigned char *st = stages + s * C::kStage;
+                    mbar_expect_arrive(full + s, C::kStage);
+                    tma_load(st, &tmx, kb * BK, m * C::kRows, full + s);
+                    if (TALL)  // rows past the end of x arrive as zeros
+                        tma_load(st + kABytes, &tmx, kb * BK, m * C::kRows + BM, full + s);
+                    tma_load(st + C::kAPart, &tmw, kb * BK, nk, full + s);
+                    tma_load(st + C::kAPart + kBoxBytes, &tmw, kb * BK, nv, full + s);
                     issued++;
                 }
             }
             // the copies of the last rounds may still be landing: wait (bounded)
-            for (int it = issued > kStages ? issued - kStages : 0; it < issued; it++) {
+            for (int it = issued > KS ? issued - KS : 0; it < issued; it++) {
                 const unsigned long long t0 = gtimer();
-                while (!mbar_try(full + it % kStages, (uint32_t)(it / kStages) & 1u) && gtimer() - t0 < kTimeoutNs) {
+                while (!mbar_try(full + it % KS, (uint32_t)(it / KS) & 1u) && gtimer() - t0 < kTimeoutNs) {
                 }
             }
         }
@@ -324,24 +350,28 @@ __global__ void __launch_bounds__(kThreadsG, 1)
             int it = 0;  // k-blocks consumed over all tiles
             bool ok = true;
             for (int tile = blockIdx.x, i = 0; tile < num_tiles && ok; tile += gridDim.x, i++) {
-                const int b = i & 1;
+                const int b = TALL ? 0 : i & 1;            // tall: the pair, every tile
+                const uint32_t use = TALL ? i : (i >> 1);  // earlier uses of this accumulator
                 // the epilogue has drained this accumulator (its previous use)
-                if (!mbar_wait(acc_empty + b, ((uint32_t)(i >> 1) & 1u) ^ 1u, abort))
+                if (!mbar_wait(acc_empty + b, (use & 1u) ^ 1u, abort))
                     break;
                 tc_fence_after();
                 const uint32_t d = tmem + (uint32_t)(b * BN);
                 for (int kb = 0; kb < p.num_kb; kb++, it++) {
-                    const int s = it % kStages;
-                    if (!mbar_wait(full + s, (uint32_t)(it / kStages) & 1u, abort)) {
+                    const int s = it % KS;
+                    if (!mbar_wait(full + s, (uint32_t)(it / KS) & 1u, abort)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t a = saddr(stages + s * kStageBytes);
-                    const uint32_t bb = a + kABytes;
+                    const uint32_t a = saddr(stages + s * C::kStage);
+                    const uint32_t bb = a + C::kAPart;
 #pragma unroll
-                    for (int k = 0; k < BK / 16; k++)  // 16 bf16 = 32 bytes per step along K
+                    for (int k = 0; k < BK / 16; k++) {  // 16 bf16 = 32 bytes per step along K
                         mma_bf16(d, sw128_desc(a + 32 * k), sw128_desc(bb + 32 * k), (kb | k) != 0);
+                        if (TALL)  // rows 128..255 of the tile into the second accumulator
+                            mma_bf16(d + BN, sw128_desc(a + kABytes + 32 * k), sw128_desc(bb + 32 * k), (kb | k) != 0);
+                    }
                     mma_commit(empty + s);
                 }
                 if (ok)
@@ -355,150 +385,163 @@ __global__ void __launch_bounds__(kThreadsG, 1)
         const int q4 = warp & 3;  // the TMEM lane quarter this warp may access
         const int row = q4 * 32 + lane;
         for (int tile = blockIdx.x, i = 0; tile < num_tiles; tile += gridDim.x, i++) {
-            const int b = i & 1;
+            const int b = TALL ? 0 : i & 1;            // tall: the pair, every tile
+            const uint32_t use = TALL ? i : (i >> 1);  // earlier uses of this accumulator
             int m, n;
             tile_coords(tile, num_m, num_n, m, n);
             const int l = n / p.nkv, h = n - l * p.nkv;
-            const int64_t t = (int64_t)m * BM + row;
-            int64_t slot = -1, pos = 0;
-            if (MODE == kModeWrite && t < p.T) {
-                slot = __ldg(p.slot_mapping + t);
-                if (slot >= 0) {
-                    pos = __ldg(p.positions + t);
-                    if (slot >= p.capacity) {
-                        if (n == 0)
-                            flags |= kFlagSlot;
-                        slot = -1;
-                    } else if (pos < 0 || pos >= p.max_pos) {
-                        if (n == 0)
-                            flags |= kFlagPos;
-                        slot = -1;
+            // this thread's token in each 128-row half of the tile, with its
+            // slot and position (loaded before the accumulator is ready)
+            int64_t t_h[NH], slot_h[NH], pos_h[NH];
+#pragma unroll
+            for (int hf = 0; hf < NH; hf++) {
+                const int64_t t = (int64_t)m * C::kRows + hf * BM + row;
+                int64_t slot = -1, pos = 0;
+                if (MODE == kModeWrite && t < p.T) {
+                    slot = __ldg(p.slot_mapping + t);
+                    if (slot >= 0) {
+                        pos = __ldg(p.positions + t);
+                        if (slot >= p.capacity) {
+                            if (n == 0)
+                                flags |= kFlagSlot;
+                            slot = -1;
+                        } else if (pos < 0 || pos >= p.max_pos) {
+                            if (n == 0)
+                                flags |= kFlagPos;
+                            slot = -1;
+                        }
                     }
                 }
+                t_h[hf] = t, slot_h[hf] = slot, pos_h[hf] = pos;
             }
-            bool ok = mbar_wait(acc_full + b, (uint32_t)(i >> 1) & 1u, abort);
+            bool ok = mbar_wait(acc_full + b, use & 1u, abort);
             ok = __all_sync(0xffffffffu, ok) && !*abort;
             if (!ok)
                 break;
             tc_fence_after();
-            const uint32_t trow = tmem + (uint32_t)(b * BN) + ((uint32_t)(q4 * 32) << 16);
-            if (MODE == kModeProject) {
-                const int64_t N = (int64_t)p.L * 2 * p.nkv * 128;
-                const int nk = ((l * 2 + 0) * p.nkv + h) * 128, nv = ((l * 2 + 1) * p.nkv + h) * 128;
 #pragma unroll 1
-                for (int c = 0; c < 8; c++) {
+            for (int hf = 0; hf < NH; hf++) {
+                const int64_t t = t_h[hf], slot = slot_h[hf], pos = pos_h[hf];
+                const bool last = hf == NH - 1;  // the tile's last read hands its accumulator(s) back
+                const uint32_t trow = tmem + (uint32_t)((b + hf) * BN) + ((uint32_t)(q4 * 32) << 16);
+                if (MODE == kModeProject) {
+                    const int64_t N = (int64_t)p.L * 2 * p.nkv * 128;
+                    const int nk = ((l * 2 + 0) * p.nkv + h) * 128, nv = ((l * 2 + 1) * p.nkv + h) * 128;
+#pragma unroll 1
+                    for (int c = 0; c < 8; c++) {
+                        uint32_t r[32];
+                        tmem_ld32(trow + 32 * c, r);  // every lane: the load is warp-wide
+                        if (c == 7 && last) {                 // the accumulator is read: hand it back
+                            tc_fence_before();
+                            __syncwarp();
+                            if (lane == 0)
+                                asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(saddr(acc_empty + b))
+                                             : "memory");
+                        }
+                        if (t < p.T) {
+                            uint32_t pk[16];
+#pragma unroll
+                            for (int j = 0; j < 16; j++)
+                                pk[j] = pack_bf16x2(__uint_as_float(r[2 * j]), __uint_as_float(r[2 * j + 1]));
+                            uint16_t *dst = p.all_kv_out + t * N + (c < 4 ? nk + 32 * c : nv + 32 * (c - 4));
+#pragma unroll
+                            for (int k = 0; k < 4; k++)
+                                st16(dst + 8 * k, pk[4 * k], pk[4 * k + 1], pk[4 * k + 2], pk[4 * k + 3]);
+                        }
+                    }
+                    continue;
+                }
+                // K: bf16 as the projection materialises it, then the Gemma norm in fp32
+                uint32_t kw[64];
+                float ss = 0.0f;
+#pragma unroll
+                for (int c = 0; c < 4; c++) {
                     uint32_t r[32];
-                    tmem_ld32(trow + 32 * c, r);  // every lane: the load is warp-wide
-                    if (c == 7) {                 // the accumulator is read: hand it back
+                    tmem_ld32(trow + 32 * c, r);
+#pragma unroll
+                    for (int j = 0; j < 16; j++) {
+                        const uint32_t pk = pack_bf16x2(__uint_as_float(r[2 * j]), __uint_as_float(r[2 * j + 1]));
+                        kw[16 * c + j] = pk;
+                        ss = fmaf(bfl(pk), bfl(pk), ss);
+                        ss = fmaf(bfh(pk), bfh(pk), ss);
+                    }
+                }
+                float inv;  // ss/128 + eps >= eps > 0 (hardware reciprocal square root)
+                asm("rsqrt.approx.ftz.f32 %0, %1;" : "=f"(inv) : "f"(fmaf(ss, 1.0f / kHeadDim, p.eps)));
+                const float *wl = w1 + l * 128;
+#pragma unroll
+                for (int j = 0; j < 64; j++)
+                    kw[j] = pack_bf16x2((bfl(kw[j]) * inv) * wl[2 * j], (bfh(kw[j]) * inv) * wl[2 * j + 1]);
+                unsigned char *dst = nullptr;
+                Fp8Scale vq;
+                if (slot >= 0) {
+                    // RoPE: dims j and j + r/2 (both in this thread), cos|sin of the token's position
+                    uint32_t cs[ROT / 2];
+                    const uint4 *src = reinterpret_cast<const uint4 *>(p.cos_sin + pos * ROT);
+#pragma unroll
+                    for (int k = 0; k < ROT / 8; k++) {
+                        const uint4 v = __ldg(src + k);
+                        cs[4 * k] = v.x, cs[4 * k + 1] = v.y, cs[4 * k + 2] = v.z, cs[4 * k + 3] = v.w;
+                    }
+#pragma unroll
+                    for (int j = 0; j < ROT / 4; j++) {
+                        const uint32_t a = kw[j], bb = kw[j + ROT / 4], c = cs[j], s = cs[ROT / 4 + j];
+                        kw[j] = rope_pair(a, c, bb, s ^ 0x80008000u);  // a c - b s
+                        kw[j + ROT / 4] = rope_pair(bb, c, a, s);      // b c + a s
+                    }
+                    const int64_t rowel =
+                        ((((slot >> p.bsl) * p.nkv + h) << p.bsl) + (slot & ((int64_t(1) << p.bsl) - 1))) * kRowElems;
+                    dst = p.cache0 + (__ldg(p.cache_offsets + l) + rowel) * (FP8 ? 1 : 2);
+                    if (FP8) {
+                        const Fp8Scale kq = fp8_scale(__ldg(reinterpret_cast<const float *>(
+                            __ldg(reinterpret_cast<const unsigned long long *>(p.k_scales) + l))));
+                        vq = fp8_scale(__ldg(reinterpret_cast<const float *>(
+                            __ldg(reinterpret_cast<const unsigned long long *>(p.v_scales) + l))));
+#pragma unroll
+                        for (int k = 0; k < 8; k++) {
+                            const uint2 lo =
+                                quantise8(make_uint4(kw[8 * k], kw[8 * k + 1], kw[8 * k + 2], kw[8 * k + 3]), kq);
+                            const uint2 hi =
+                                quantise8(make_uint4(kw[8 * k + 4], kw[8 * k + 5], kw[8 * k + 6], kw[8 * k + 7]), kq);
+                            st16(dst + 16 * k, lo.x, lo.y, hi.x, hi.y);
+                        }
+                    } else {
+#pragma unroll
+                        for (int k = 0; k < 16; k++)
+                            st16(dst + 16 * k, kw[4 * k], kw[4 * k + 1], kw[4 * k + 2], kw[4 * k + 3]);
+                    }
+                }
+                // V: bf16 as materialised, stored as it is (or encoded); after its
+                // last read the accumulator is handed back to the MMA warp
+#pragma unroll
+                for (int c = 0; c < 4; c++) {
+                    uint32_t r[32];
+                    tmem_ld32(trow + 128 + 32 * c, r);
+                    if (c == 3 && last) {
                         tc_fence_before();
                         __syncwarp();
                         if (lane == 0)
-                            asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(saddr(acc_empty + b))
-                                         : "memory");
+                            asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(saddr(acc_empty + b)) : "memory");
                     }
-                    if (t < p.T) {
+                    if (slot >= 0) {
                         uint32_t pk[16];
 #pragma unroll
                         for (int j = 0; j < 16; j++)
                             pk[j] = pack_bf16x2(__uint_as_float(r[2 * j]), __uint_as_float(r[2 * j + 1]));
-                        uint16_t *dst = p.all_kv_out + t * N + (c < 4 ? nk + 32 * c : nv + 32 * (c - 4));
+                        if (FP8) {
 #pragma unroll
-                        for (int k = 0; k < 4; k++)
-                            st16(dst + 8 * k, pk[4 * k], pk[4 * k + 1], pk[4 * k + 2], pk[4 * k + 3]);
-                    }
-                }
-                continue;
-            }
-            // K: bf16 as the projection materialises it, then the Gemma norm in fp32
-            uint32_t kw[64];
-            float ss = 0.0f;
+                            for (int k = 0; k < 2; k++) {
+                                const uint2 lo =
+                                    quantise8(make_uint4(pk[8 * k], pk[8 * k + 1], pk[8 * k + 2], pk[8 * k + 3]), vq);
+                                const uint2 hi =
+                                    quantise8(make_uint4(pk[8 * k + 4], pk[8 * k + 5], pk[8 * k + 6], pk[8 * k + 7]), vq);
+                                st16(dst + 128 + 32 * c + 16 * k, lo.x, lo.y, hi.x, hi.y);
+                            }
+                        } else {
 #pragma unroll
-            for (int c = 0; c < 4; c++) {
-                uint32_t r[32];
-                tmem_ld32(trow + 32 * c, r);
-#pragma unroll
-                for (int j = 0; j < 16; j++) {
-                    const uint32_t pk = pack_bf16x2(__uint_as_float(r[2 * j]), __uint_as_float(r[2 * j + 1]));
-                    kw[16 * c + j] = pk;
-                    ss = fmaf(bfl(pk), bfl(pk), ss);
-                    ss = fmaf(bfh(pk), bfh(pk), ss);
-                }
-            }
-            float inv;  // ss/128 + eps >= eps > 0 (hardware reciprocal square root)
-            asm("rsqrt.approx.ftz.f32 %0, %1;" : "=f"(inv) : "f"(fmaf(ss, 1.0f / kHeadDim, p.eps)));
-            const float *wl = w1 + l * 128;
-#pragma unroll
-            for (int j = 0; j < 64; j++)
-                kw[j] = pack_bf16x2((bfl(kw[j]) * inv) * wl[2 * j], (bfh(kw[j]) * inv) * wl[2 * j + 1]);
-            unsigned char *dst = nullptr;
-            Fp8Scale vq;
-            if (slot >= 0) {
-                // RoPE: dims j and j + r/2 (both in this thread), cos|sin of the token's position
-                uint32_t cs[ROT / 2];
-                const uint4 *src = reinterpret_cast<const uint4 *>(p.cos_sin + pos * ROT);
-#pragma unroll
-                for (int k = 0; k < ROT / 8; k++) {
-                    const uint4 v = __ldg(src + k);
-                    cs[4 * k] = v.x, cs[4 * k + 1] = v.y, cs[4 * k + 2] = v.z, cs[4 * k + 3] = v.w;
-                }
-#pragma unroll
-                for (int j = 0; j < ROT / 4; j++) {
-                    const uint32_t a = kw[j], bb = kw[j + ROT / 4], c = cs[j], s = cs[ROT / 4 + j];
-                    kw[j] = rope_pair(a, c, bb, s ^ 0x80008000u);  // a c - b s
-                    kw[j + ROT / 4] = rope_pair(bb, c, a, s);      // b c + a s
-                }
-                const int64_t rowel =
-                    ((((slot >> p.bsl) * p.nkv + h) << p.bsl) + (slot & ((int64_t(1) << p.bsl) - 1))) * kRowElems;
-                dst = p.cache0 + (__ldg(p.cache_offsets + l) + rowel) * (FP8 ? 1 : 2);
-                if (FP8) {
-                    const Fp8Scale kq = fp8_scale(__ldg(reinterpret_cast<const float *>(
-                        __ldg(reinterpret_cast<const unsigned long long *>(p.k_scales) + l))));
-                    vq = fp8_scale(__ldg(reinterpret_cast<const float *>(
-                        __ldg(reinterpret_cast<const unsigned long long *>(p.v_scales) + l))));
-#pragma unroll
-                    for (int k = 0; k < 8; k++) {
-                        const uint2 lo =
-                            quantise8(make_uint4(kw[8 * k], kw[8 * k + 1], kw[8 * k + 2], kw[8 * k + 3]), kq);
-                        const uint2 hi =
-                            quantise8(make_uint4(kw[8 * k + 4], kw[8 * k + 5], kw[8 * k + 6], kw[8 * k + 7]), kq);
-                        st16(dst + 16 * k, lo.x, lo.y, hi.x, hi.y);
-                    }
-                } else {
-#pragma unroll
-                    for (int k = 0; k < 16; k++)
-                        st16(dst + 16 * k, kw[4 * k], kw[4 * k + 1], kw[4 * k + 2], kw[4 * k + 3]);
-                }
-            }
-            // V: bf16 as materialised, stored as it is (or encoded); after its
-            // last read the accumulator is handed back to the MMA warp
-#pragma unroll
-            for (int c = 0; c < 4; c++) {
-                uint32_t r[32];
-                tmem_ld32(trow + 128 + 32 * c, r);
-                if (c == 3) {
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0)
-                        asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(saddr(acc_empty + b)) : "memory");
-                }
-                if (slot >= 0) {
-                    uint32_t pk[16];
-#pragma unroll
-                    for (int j = 0; j < 16; j++)
-                        pk[j] = pack_bf16x2(__uint_as_float(r[2 * j]), __uint_as_float(r[2 * j + 1]));
-                    if (FP8) {
-#pragma unroll
-                        for (int k = 0; k < 2; k++) {
-                            const uint2 lo =
-                                quantise8(make_uint4(pk[8 * k], pk[8 * k + 1], pk[8 * k + 2], pk[8 * k + 3]), vq);
-                            const uint2 hi =
-                                quantise8(make_uint4(pk[8 * k + 4], pk[8 * k + 5], pk[8 * k + 6], pk[8 * k + 7]), vq);
-                            st16(dst + 128 + 32 * c + 16 * k, lo.x, lo.y, hi.x, hi.y);
+                            for (int k = 0; k < 4; k++)
+                                st16(dst + 256 + 64 * c + 16 * k, pk[4 * k], pk[4 * k + 1], pk[4 * k + 2], pk[4 * k + 3]);
                         }
-                    } else {
-#pragma unroll
-                        for (int k = 0; k < 4; k++)
-                            st16(dst + 256 + 64 * c + 16 * k, pk[4 * k], pk[4 * k + 1], pk[4 * k + 2], pk[4 * k + 3]);
                     }
                 }
             }
@@ -555,41 +598,82 @@ bool encode_kmajor(CUtensorMap *map, const void *ptr, uint64_t inner, uint64_t o
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int MODE, int ROT, bool FP8>
-cudaError_t launch_gemm(const CUtensorMap &tx, const CUtensorMap &tw, const GemmParams &p, cudaStream_t stream)
+int gemm_sms(cudaError_t &e)
 {
     static std::mutex mu;
-    static bool attr_set[64];
     static int sms_cache[64];
+    int dev = 0;
+    e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return 0;
+    if (dev < 0 || dev >= 64) {
+        e = cudaErrorInvalidDevice;
+        return 0;
+    }
+    std::lock_guard<std::mutex> lock(mu);
+    if (sms_cache[dev] == 0)
+        e = cudaDeviceGetAttribute(&sms_cache[dev], cudaDevAttrMultiProcessorCount, dev);
+    return sms_cache[dev];
+}
+
+// Tall tiles where they save whole waves on a small call: the short tiles'
+// waves against 1.4 x the tall tiles' (a tall tile is twice the work at
+// about 1.4 x the short tile's time, being fed 50% more flops per operand
+// byte), up to 2,048 tokens; larger calls keep the overlapped epilogue.
+bool use_tall(int64_t T, int64_t num_n, int sms)
+{
+    const char *env = std::getenv("DSPARK_PROJ_TILE");  // tests: "tall" or "short" pins one
+    if (env && std::strcmp(env, "tall") == 0)
+        return true;
+    if (env && std::strcmp(env, "short") == 0)
+        return false;
+    if (T > 2048 || sms <= 0)
+        return false;
+    const int64_t waves_short = (num_n * ((T + BM - 1) / BM) + sms - 1) / sms;
+    const int64_t waves_tall = (num_n * ((T + 255) / 256) + sms - 1) / sms;
+    return (double)waves_short > 1.4 * (double)waves_tall;
+}
+
+template <int MODE, int ROT, bool FP8, bool TALL>
+cudaError_t launch_gemm(const CUtensorMap &tx, const CUtensorMap &tw, const GemmParams &p, int sms,
+                        cudaStream_t stream)
+{
+    using C = TileCfg<TALL>;
+    static std::mutex mu;
+    static bool attr_set[64];
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess)
         return e;
     if (dev < 0 || dev >= 64)
         return cudaErrorInvalidDevice;
-    int sms;
     {
         std::lock_guard<std::mutex> lock(mu);
         if (!attr_set[dev]) {
-            e = cudaFuncSetAttribute(proj_gemm_kernel<MODE, ROT, FP8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     (int)kSmemBytes);
+            e = cudaFuncSetAttribute(proj_gemm_kernel<MODE, ROT, FP8, TALL>,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::kSmem);
             if (e != cudaSuccess)
                 return e;
             attr_set[dev] = true;
         }
-        if (sms_cache[dev] == 0) {
-            e = cudaDeviceGetAttribute(&sms_cache[dev], cudaDevAttrMultiProcessorCount, dev);
-            if (e != cudaSuccess)
-                return e;
-        }
-        sms = sms_cache[dev];
     }
     // persistent: one CTA per SM (the shared-memory ring holds one), each
     // walking the tile order with a stride of the grid
-    const int64_t tiles = (int64_t)p.L * p.nkv * ((p.T + BM - 1) / BM);
+    const int64_t tiles = (int64_t)p.L * p.nkv * ((p.T + C::kRows - 1) / C::kRows);
     const int grid = (int)(tiles < sms ? tiles : sms);
-    proj_gemm_kernel<MODE, ROT, FP8><<<grid, kThreadsG, kSmemBytes, stream>>>(tx, tw, p);
+    proj_gemm_kernel<MODE, ROT, FP8, TALL><<<grid, kThreadsG, C::kSmem, stream>>>(tx, tw, p);
     return cudaGetLastError();
+}
+
+template <int MODE, int ROT, bool FP8>
+cudaError_t launch_gemm(const CUtensorMap &tx, const CUtensorMap &tw, const GemmParams &p, cudaStream_t stream)
+{
+    cudaError_t e = cudaSuccess;
+    const int sms = gemm_sms(e);
+    if (e != cudaSuccess)
+        return e;
+    return use_tall(p.T, (int64_t)p.L * p.nkv, sms) ? launch_gemm<MODE, ROT, FP8, true>(tx, tw, p, sms, stream)
+                                                     : launch_gemm<MODE, ROT, FP8, false>(tx, tw, p, sms, stream);
 }
 
 }  // namespace

@@ -8,6 +8,7 @@ states, then the fused writer), through the C ABI.
   bf16 projection is unique -- the projection must equal the oracle's bit
   for bit, and the fused write must match the oracle's write of the oracle's
   projection within the write's own tolerance (tests/parity.py).
+* Every case runs on both tile shapes (128 and 256 tokens per tile).
 * Gaussian inputs: each projected element within |sum of fp32 rounding
   errors| <= hidden * 2^-24 * sum_k |x_k w_k| (any summation order) plus one
   bf16 rounding of the exact dot product; then the oracle writes that
@@ -22,6 +23,15 @@ import workloads as wk
 from parity import compare_caches, device_inputs, to_numpy_caches
 
 pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(autouse=True, params=["short", "tall"])
+def tile(request, monkeypatch):
+    """Every case on both tile shapes: 128-token tiles with the two
+    accumulators alternating, and 256-token tiles filling both at once (the
+    default picks one by the call's size)."""
+    monkeypatch.setenv("DSPARK_PROJ_TILE", request.param)
+    return request.param
 
 
 def bits(x: torch.Tensor) -> np.ndarray:

@@ -478,6 +478,12 @@ def run_ours(args):
         # as in a serving step); --events times isolated launches instead
         side = torch.cuda.Stream()
         side.wait_stream(stream)
+        with torch.cuda.stream(side):
+            # an eager call of every writer on the capture stream first: the
+            # writer makes its work counters outside capture only
+            for i in range(len(writers)):
+                step(i)
+        torch.cuda.synchronize()
         graph = torch.cuda.CUDAGraph()
         with torch.cuda.graph(graph, stream=side):
             for i in range(args.steps):

@@ -112,8 +112,8 @@ class ContextKVWriter:
 
         self._flags = torch.zeros(1, dtype=torch.int32, device=c0.device)
         # work counters of the dynamic tail, one per stream the writer has
-        # launched on: calls on one stream run in order and share a counter,
-        # calls on different streams may overlap and must not
+        # launched on outside capture: calls on one stream run in order and
+        # share a counter, calls on different streams may overlap and must not
         self._work = {}
 
     def _descs(self):
@@ -201,19 +201,20 @@ class ContextKVWriter:
                                   error_flags, self._work_counter(stream), stream)
 
     def _work_counter(self, stream):
+        """The dynamic tail's counter of ``stream`` (None: the fixed split).
+        Counters are made and zeroed outside capture only, so a call captured
+        on a stream the writer has not launched on before takes the fixed
+        split, and a captured call uses its stream's counter: a graph replay
+        must then not overlap the writer's other calls on that stream."""
         import torch
 
         h = _stream_handle(stream)
         c = self._work.get(h)
-        if c is None:
+        if c is None and not torch.cuda.is_current_stream_capturing():
             dev = self.kv_caches[0].device
-            capturing = torch.cuda.is_current_stream_capturing()
-            if capturing and h != torch.cuda.current_stream(dev).cuda_stream:
-                return None  # its zeros could not be ordered before the launch: the fixed split
             c = torch.zeros(2, dtype=torch.int64, device=dev)
-            if not capturing:
-                # zeroed on the current stream: land before a launch on another
-                torch.cuda.current_stream(dev).synchronize()
+            # zeroed on the current stream: land before a launch on another
+            torch.cuda.current_stream(dev).synchronize()
             self._work[h] = c
         return c
 

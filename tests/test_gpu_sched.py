@@ -124,8 +124,9 @@ def test_null_counter_is_the_fixed_split(oracle_lib):
 
 
 def test_graph_replays_reuse_the_counter(oracle_lib):
-    # captured once, replayed twice on the same counter: the second replay
-    # starts from the zero the first one left
+    # captured once, replayed twice on the capture stream's counter (made by
+    # an eager call there first): the second replay starts from the zero the
+    # first one left
     import speculative_decoding_draft_ctx_gb300 as dk
 
     wl = BIG
@@ -133,10 +134,12 @@ def test_graph_replays_reuse_the_counter(oracle_lib):
     d = device_inputs(inp)
     caches = wk.make_caches(wl, device="cuda")
     w = dk.ContextKVWriter(caches, d.extra["k_scales"], d.extra["v_scales"], "fp8")
-    w(d.all_kv, d.knorm_w, d.eps, d.positions, d.cos_sin, wl.rotary_dim, d.slot_mapping)  # tables and counter
-    torch.cuda.synchronize()
     side = torch.cuda.Stream()
     side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):  # the tables, and the capture stream's counter
+        w(d.all_kv, d.knorm_w, d.eps, d.positions, d.cos_sin, wl.rotary_dim, d.slot_mapping)
+    torch.cuda.synchronize()
+    assert side.cuda_stream in w._work
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g, stream=side):
         w(d.all_kv, d.knorm_w, d.eps, d.positions, d.cos_sin, wl.rotary_dim, d.slot_mapping)
@@ -148,3 +151,25 @@ def test_graph_replays_reuse_the_counter(oracle_lib):
         torch.cuda.synchronize()
         check_parity(oracle_lib, inp, caches)
     assert all(int(v) == 0 for c in w._work.values() for v in c.tolist())
+
+
+def test_capture_on_a_new_stream_takes_the_fixed_split(oracle_lib):
+    # no counter is made under capture: the captured write takes the fixed
+    # split and is exact, and no counter exists for that stream afterwards
+    import speculative_decoding_draft_ctx_gb300 as dk
+
+    wl = BIG
+    inp = wk.generate(wl)
+    d = device_inputs(inp)
+    caches = wk.make_caches(wl, device="cuda")
+    w = dk.ContextKVWriter(caches, d.extra["k_scales"], d.extra["v_scales"], "fp8")
+    w.ensure_tables()
+    torch.cuda.synchronize()
+    side = torch.cuda.Stream()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=side):
+        w(d.all_kv, d.knorm_w, d.eps, d.positions, d.cos_sin, wl.rotary_dim, d.slot_mapping)
+    assert side.cuda_stream not in w._work
+    g.replay()
+    torch.cuda.synchronize()
+    check_parity(oracle_lib, inp, caches)

@@ -432,6 +432,41 @@ def test_writer_refuses_bad_tensors(monkeypatch, case):
     assert ei.value.name == "DSPARK_ERR_INVALID_ARG"
 
 
+def test_writer_work_counters_per_stream_and_never_made_under_capture(monkeypatch):
+    """The dynamic tail's counters: one per stream, made zeroed (and waited
+    for) at the first call there outside capture and reused after; a call
+    captured on a stream without one gets none (the fixed split) and makes
+    none, and an existing counter serves captured calls on its stream."""
+    import torch
+    from speculative_decoding_draft_ctx_gb300 import writer as wr
+
+    w = _cpu_writer(monkeypatch)
+    w._work = {}
+    capturing = [False]
+    syncs = []
+
+    class FakeStream:
+        def __init__(self, h):
+            self.cuda_stream = h
+
+        def synchronize(self):
+            syncs.append(self.cuda_stream)
+
+    cur = FakeStream(7)
+    monkeypatch.setattr(torch.cuda, "is_current_stream_capturing", lambda: capturing[0])
+    monkeypatch.setattr(torch.cuda, "current_stream", lambda device=None: cur)
+    monkeypatch.setattr(wr, "_stream_handle", lambda s: cur.cuda_stream if s is None else s)
+    c7 = w._work_counter(None)
+    assert c7.dtype == torch.int64 and c7.tolist() == [0, 0] and syncs == [7]
+    assert w._work_counter(None) is c7 and syncs == [7]  # reused, no second wait
+    c11 = w._work_counter(11)
+    assert c11 is not c7 and c11.tolist() == [0, 0]
+    capturing[0] = True
+    assert w._work_counter(13) is None and 13 not in w._work
+    assert w._work_counter(11) is c11
+    assert len(syncs) == 2
+
+
 def test_writer_refuses_bad_per_layer_slot_mapping(monkeypatch):
     import torch
 

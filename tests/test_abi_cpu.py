@@ -289,6 +289,32 @@ def test_general_write_argument_checks(L):
     assert gcall(num_ctx=0, slot_mapping=None, expect_ok=True) == "DSPARK_OK"
 
 
+def test_sched_write_argument_checks(L):
+    """dspark_ctx_kv_write_sched: exactly one slot source, an 8-byte aligned
+    work counter and pointer table, the write's own checks -- all before any
+    CUDA call."""
+    def scall(expect_ok=False, **over):
+        a = dict(all_kv=FAKE, knorm_w=FAKE, positions=FAKE, slot_mapping=FAKE, layer_slot_mappings=None, num_ctx=4,
+                 cos_sin=FAKE, max_pos=64, layer0_cache=FAKE, num_blocks=4, cache_offsets=FAKE, k_scales=FAKE,
+                 v_scales=FAKE, L=2, nkv=2, block_size=16, rotary_dim=32, eps=1e-6, kv_dtype=0, error_flags=None,
+                 work_counter=None)
+        a.update(over)
+        if expect_ok:
+            dk.dspark_ctx_kv_write_sched(**a, stream=0)
+            return "DSPARK_OK"
+        with pytest.raises(dk.DSparkError) as ei:
+            dk.dspark_ctx_kv_write_sched(**a, stream=0)
+        return ei.value.name
+
+    assert scall(slot_mapping=None) == "DSPARK_ERR_INVALID_ARG"                      # no slot source
+    assert scall(layer_slot_mappings=FAKE) == "DSPARK_ERR_INVALID_ARG"               # two
+    assert scall(slot_mapping=None, layer_slot_mappings=FAKE + 4) == "DSPARK_ERR_ALIGNMENT"
+    assert scall(work_counter=FAKE + 4) == "DSPARK_ERR_ALIGNMENT"                     # counter: 8-byte words
+    assert scall(rotary_dim=24) == "DSPARK_ERR_UNSUPPORTED_ROTARY_DIM"
+    assert scall(block_size=48) == "DSPARK_ERR_BLOCK_SIZE"
+    assert scall(num_ctx=0, slot_mapping=None, expect_ok=True) == "DSPARK_OK"       # nothing to store
+
+
 def test_no_alloc_write_argument_checks(L):
     """dspark_ctx_kv_write_noalloc refuses a layer count beyond its fixed
     device array, and its host-table rules, before any CUDA call."""

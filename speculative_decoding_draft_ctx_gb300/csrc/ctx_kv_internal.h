@@ -41,7 +41,8 @@ cudaError_t launch_pdl(void (*kernel)(Params...), int blocks, int threads, size_
     return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
-// The kernel side of launch_pdl, before any global memory access: wait for
+// The kernel side of launch_pdl, before any global load or store (L2
+// prefetch hints may precede it: they hand no data to the program): wait for
 // the stream's previous kernel to finish and its writes to be visible, then
 // let the next kernel be scheduled as this grid's CTAs exit (it is scheduled
 // only once every CTA of this grid has issued this or exited, so it never

@@ -25,7 +25,8 @@
 // power-of-two block size, else from a multiply-high by the host's
 // Granlund-Montgomery magic number.  The kernel is launched with
 // programmatic dependent launch (launch_pdl): it waits for the stream's
-// previous kernel before its first global access.
+// previous kernel before its first global load or store, and before that
+// wait only prefetches its first slabs, slots and positions into L2.
 //
 // Compute mapping.  A consumer warp handles 4 rows per instruction: 8 lanes
 // per row, each lane holding the D/64 chunks [64k + 8q, 64k + 8q + 8) of K
@@ -238,7 +239,7 @@ __global__ void __launch_bounds__(kThreads, 2) ctx_kv_tma_kernel(const TmaParams
             prefetch_l2(p.positions + t);
         }
     }
-    pdl_enter();  // launched with launch_pdl: the barriers above need no global memory
+    pdl_enter();  // launched with launch_pdl: above, only barriers and L2 prefetch hints
 
     const long long units = p.num_ctx * (long long)NP;
     const long long G = gridDim.x;

@@ -135,7 +135,7 @@ __global__ void __launch_bounds__(32 * kWarps, 4) ctx_kv_warp_kernel(const WarpP
             prefetch_l2(p.positions + t);
         }
     }
-    pdl_enter();  // launched with launch_pdl: the barriers above need no global memory
+    pdl_enter();  // launched with launch_pdl: above, only barriers and L2 prefetch hints
     if (n_my == 0)
         return;  // no units (or a warp beyond the last whole set of L streams): idle
     const uint64_t stream_once = evict_first_policy();  // all_kv: read exactly once

@@ -126,14 +126,13 @@ int dspark_ctx_kv_write_ex(const void *all_kv, const void *knorm_w, const int64_
  * dspark_ctx_kv_write_ex (one shared slot_mapping) or
  * dspark_ctx_kv_write_layer_slots (a device table of per-layer mappings) --
  * exactly one of the two non-NULL -- plus a work counter through which the
- * pipelined kernel hands the last tenth of a call's units (a unit: a token's
- * rows of up to 8 layers) to whichever CTA is free, instead of a fixed CTA
- * (a fixed split waits for its slowest CTA): one unit per claim, runs of 4
- * from 64 units per CTA.  The vLLM DSpark context-KV writer page has no
- * counterpart: its kernel runs one fixed grid.  Calls below 8 units per CTA
- * (the grid is two CTAs per SM: 2,432 units on a 152-SM GPU; 64 units per
- * CTA with per-layer mappings), and calls the pipelined kernel does not
- * take, keep the fixed split and leave the counter untouched.
+ * pipelined kernel hands the last tenth of a large call's units (a unit: a
+ * token's rows of up to 8 layers) in runs of 4 to whichever CTA is free,
+ * instead of a fixed CTA (a fixed split waits for its slowest CTA).  The
+ * vLLM DSpark context-KV writer page has no counterpart: its kernel runs one
+ * fixed grid.  Calls below 64 units per CTA (the grid is two CTAs per SM:
+ * about 19.5k units on a 152-SM GPU), and layouts the pipelined kernel does
+ * not take, keep the fixed split and leave the counter untouched.
  *
  *  work_counter  device, 2 x uint64, 8-byte aligned, owned by the caller:
  *                zero before its first use; every call leaves it zero

@@ -88,7 +88,6 @@ constexpr unsigned kFlagSlot = 0x1u;
 constexpr unsigned kFlagPos = 0x2u;
 constexpr unsigned kFlagTimeout = 0x4u;
 constexpr unsigned kFlagCounter = 0x8u;
-constexpr int kClaimLead = 2;  // units of the last static batch left to issue when the tail's first run is claimed
 constexpr int kMaxTmaLayers = 32;
 
 // A device word that nothing ever sets: the test hook's wait (test_hold_ns)
@@ -428,36 +427,19 @@ __global__ void __launch_bounds__(kThreads, 2) ctx_kv_tma_kernel(const TmaParams
                 asm volatile("cp.async.commit_group;" ::: "memory");
         }
         for (; cur.count > 0 && ok; buf ^= 1) {
-            // The next batch is fetched now -- except the shared tail's first
-            // run after the CTA's last static batch, claimed only when
-            // kClaimLead units of this batch are left to issue: claimed a
-            // whole batch ahead, the tail would be handed out at the start,
-            // i.e. statically.
-            const bool defer = tp.work_counter && !cur.dyn && static_batch(cur.first + 32 * step).count == 0;
-            Batch nxt{0, 1, 0, true};
-            bool have_next = false;
-            auto take_next = [&]() {
-                nxt = defer ? claim() : next_batch(cur);
-                if (nxt.count > 0) {
-                    fetch(nxt, nxt_slot, nxt_pos, buf ^ 1);
-                    if (PL)
-                        asm volatile("cp.async.commit_group;" ::: "memory");
-                }
-                have_next = true;
-            };
-            if (!defer)
-                take_next();
-            if (PL) {
-                if (have_next && nxt.count > 0)
+            const Batch nxt = next_batch(cur);
+            if (nxt.count > 0) {
+                fetch(nxt, nxt_slot, nxt_pos, buf ^ 1);
+                if (PL) {
+                    asm volatile("cp.async.commit_group;" ::: "memory");
                     asm volatile("cp.async.wait_group 1;" ::: "memory");  // this batch's, not the next one's
-                else
-                    asm volatile("cp.async.wait_group 0;" ::: "memory");
+                }
+            } else if (PL) {
+                asm volatile("cp.async.wait_group 0;" ::: "memory");
             }
             vet(cur, cur_slot, cur_pos, buf);
             __syncwarp();  // lane 0 reads the other lanes' prefetched slots below
             for (int i = 0; i < cur.count; i++) {
-                if (defer && !have_next && i == max(0, cur.count - kClaimLead))
-                    take_next();
                 const long long u = cur.first + (long long)i * cur.stride;
                 const long long slot = __shfl_sync(0xffffffffu, cur_slot, i);
                 const long long pos = __shfl_sync(0xffffffffu, cur_pos, i);
@@ -541,8 +523,6 @@ __global__ void __launch_bounds__(kThreads, 2) ctx_kv_tma_kernel(const TmaParams
                     pph ^= 1u;
                 }
             }
-            if (defer && !have_next && ok)
-                take_next();
             ordinal += cur.count;
             cur_slot = nxt_slot;
             cur_pos = nxt_pos;
@@ -1115,18 +1095,16 @@ cudaError_t launch_ctx_kv_write_tma(const CtxKvParams &p, int head_dim, bool fp8
     tp.prefetch_units = units >= 64 * G ? 12 : pl.S;
     if (p.work_counter) {
         // CTAs of a static launch end up to 6% apart and the slowest one ends
-        // it, so from 8 units per CTA the last tenth of the units is handed
-        // out to whichever CTA is free: single units up to 64 per CTA, runs
-        // of 4 beyond (fewer claims).  One box, two runs each, against the
-        // static order: prefill (27 units per CTA) 42.57 -> 42.02 us, long
-        // context (215) 211.2 -> 209.4 us.  With per-layer mappings a claim
-        // also waits for its unit's per-layer slot copies, and single-unit
-        // claims measured slower (prefill 41.4 -> 45.4 us), so those calls
-        // take the tail only from 64 units per CTA, in runs of 4.
-        if (units >= (p.layer_slots ? 64 : 8) * G) {
+        // it, so on large calls the last tenth of the units is handed out in
+        // runs of 4 to whichever CTA is free (long context 211.8 -> 209.5 us,
+        // per-layer mappings 222.8 -> 220.4 us).  Below 64 units per CTA the
+        // claims cost more than they recover (prefill, 27 units per CTA: 1-3
+        // us slower with any tail share and run length tried), so those calls
+        // keep the static order.
+        if (units >= 64 * G) {
             tp.work_counter = p.work_counter;
             tp.static_units = units * 9 / 10 / G * G;
-            tp.claim_units = units >= 64 * G ? 4 : 1;
+            tp.claim_units = 4;
         }
     }
     const uint32_t smem = pl.lay.total;

@@ -15,9 +15,8 @@ from parity import compare_caches, device_inputs, to_numpy_caches
 pytestmark = pytest.mark.gpu
 
 PREFILL = wk.WORKLOADS[3]  # 8192 tokens, 5 layers, 8 KV heads, r = 32, fp8
-# the dynamic tail engages from 8 units per CTA (2,432 tokens here) and claims
-# runs of 4 from 64 (19,456): 20480 tokens in 80 requests, 3 layers and 4 KV
-# heads (a cheap oracle); the prefill-sized tests elsewhere take single units
+# the dynamic tail engages from 64 units per CTA (about 19.5k tokens here):
+# 20480 tokens in 80 requests, 3 layers and 4 KV heads (a cheap oracle)
 BIG = dataclasses.replace(PREFILL, name="thin_20k_fp8", num_ctx=20480, requests=80, num_layers=3,
                           num_kv_heads=4)
 BIG_BF16 = dataclasses.replace(BIG, name="thin_20k_bf16", kv_dtype=wk.KV_BF16)

@@ -16,7 +16,7 @@ from parity import device_inputs
 pytestmark = pytest.mark.gpu
 
 PREFILL = wk.WORKLOADS[3]
-# past the dynamic tail's thresholds (8 and 64 units per CTA): 20480 tokens
+# past the dynamic tail's threshold (64 units per CTA): 20480 tokens
 BIG = dataclasses.replace(PREFILL, name="thin_20k_fp8", num_ctx=20480, requests=80, num_layers=3, num_kv_heads=4)
 BIG_BF16 = dataclasses.replace(BIG, name="thin_20k_bf16", kv_dtype=wk.KV_BF16)
 DRAFT = wk.WORKLOADS[1]  # 512 tokens: the warp-private kernel

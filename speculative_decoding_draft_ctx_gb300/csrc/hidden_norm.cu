@@ -148,7 +148,7 @@ __global__ void __launch_bounds__(kThreadsN) gemma_norm_split_kernel(const uint1
     pdl_enter();
     __shared__ float part[kWarpsN];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int sub = warp & 3, slot = warp >> 2;  // warp within its row, row within the CTA
+    const int slot = warp >> 2;                  // row within the CTA (warp & 3: the warp within its row)
     const int tr = threadIdx.x & 127;            // thread within its row
     const int chunks = hidden >> 3;
     const float inv_n = 1.0f / (float)hidden;

@@ -57,7 +57,6 @@ constexpr int BM = 128, BN = 256, BK = 64, kStages = 4;
 constexpr int kThreadsG = 192;                             // warp 0 TMA, warp 1 MMA, warps 2-5 epilogue
 constexpr uint32_t kABytes = BM * BK * 2;                  // 16 KB
 constexpr uint32_t kBoxBytes = 128 * BK * 2;               // one 128-row weight box, 16 KB
-constexpr uint32_t kStageBytes = kABytes + 2 * kBoxBytes;  // 48 KB
 constexpr uint32_t kTmemCols = 512;  // two 256-column accumulators: the epilogue of one tile overlaps the next
 constexpr int kMaxLayersProj = 32;   // the (1 + w) table of every layer lives in shared memory
 constexpr int kGroupN = 16;          // column tiles per rasterisation group

@@ -104,3 +104,45 @@ def test_cos_sin_rows_are_cos_then_sin_at_the_position_angle():
         ang = p * wl.rope_theta ** (-2.0 * torch.arange(h, dtype=torch.float64) / wl.rotary_dim)
         assert torch.allclose(cs[p, :h], torch.cos(ang), atol=2 ** -8)
         assert torch.allclose(cs[p, h:], torch.sin(ang), atol=2 ** -8)
+
+
+@pytest.mark.parametrize("name", ["qk_tiny", "qk_draft", "qk_draft_fp8"])
+def test_qk_insert_requests_of_seven_consecutive_rows(name):
+    wl = wk.QK_WORKLOADS_BY_NAME[name]
+    inp = wk.generate_qk(wl)
+    R, n, bs = wl.requests, 7, wl.block_size
+    assert wl.num_tokens == R * n
+    assert inp.qkv.shape == (R * n, (wl.num_heads + 2 * wl.num_kv_heads) * 128)
+    assert inp.qkv.dtype == torch.bfloat16
+    pos = inp.positions.view(R, n)
+    assert (pos[:, 1:] - pos[:, :-1] == 1).all() and int(pos.min()) >= 0 and int(pos.max()) < wl.max_pos
+    s = inp.slot_mapping.view(R, n)
+    assert int((s < 0).sum()) == wl.pad_count
+    valid = s >= 0
+    assert torch.equal((s % bs)[valid], (pos % bs)[valid])
+    req = torch.arange(R).view(R, 1).expand(R, n)
+    seen = {}
+    for r, lb, blk in zip(req[valid].tolist(), (pos // bs)[valid].tolist(), (s // bs)[valid].tolist()):
+        assert seen.setdefault((r, lb), blk) == blk
+    assert len(set(seen.values())) == len(seen) and max(seen.values()) < wl.num_blocks
+
+
+@pytest.mark.parametrize("wl", wk.GENERAL_WORKLOADS, ids=lambda w: w.name)
+def test_general_layouts_are_outside_the_pages_kernel(wl):
+    # each general workload breaks one of the pages' layout rules (head dim
+    # 128, rotary dim 16 / 32 / 64, a power-of-two block size) and keeps the
+    # prefill recipe: 32 requests x positions 0..255 through block tables
+    assert not wk.pages_layout(wl)
+    pages_rules = (wl.head_dim == 128, wl.rotary_dim in (16, 32, 64),
+                   wl.block_size & (wl.block_size - 1) == 0)
+    assert not all(pages_rules)
+    inp = wk.generate(wl, with_all_kv=False)
+    assert int((inp.slot_mapping < 0).sum()) == wl.pad_count
+    R, tpr, bs = wl.requests, wl.tokens_per_request, wl.block_size
+    pos = inp.positions.view(R, tpr)
+    assert torch.equal(pos, torch.arange(tpr).expand(R, tpr))
+    s = inp.slot_mapping.view(R, tpr)
+    valid = s >= 0
+    assert torch.equal((s % bs)[valid], (pos % bs)[valid])
+    assert len(torch.unique(s[valid])) == int(valid.sum()) and int(s.max()) < wl.capacity
+    assert inp.cos_sin.shape == (wl.max_pos, wl.rotary_dim)
